@@ -1,0 +1,82 @@
+"""Seeded synthetic inputs for the attention forward workloads.
+
+This module draws random numbers and nothing else: it holds none of the
+attention arithmetic, so the CUDA path and the fp64 oracle can both be fed
+from it without sharing any of the method.
+
+Every workload is iid Gaussian Q, K, V drawn in fp32 from a seeded
+``torch.Generator`` (Q first, then K, then V), scaled by its standard
+deviation and rounded to bfloat16.  The long-sequence workload draws Q and K
+with standard deviation 1.5 (a wider logit spread); all others use 1.
+"""
+from dataclasses import dataclass
+import math
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    Nq: int
+    Nk: int
+    d: int
+    causal: bool
+    sigma_qk: float = 1.0
+    seed: int = 1000
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def decode(self) -> bool:
+        return self.Nq == 1
+
+    def flops(self) -> float:
+        """4 B H Nq Nk d (two GEMMs), halved for the causal mask."""
+        f = 4.0 * self.B * self.H * self.Nq * self.Nk * self.d
+        return f / 2 if self.causal else f
+
+    def algorithmic_bytes(self) -> int:
+        """Bytes read and written once: Q, K, V, O in bf16 and lse in fp32."""
+        bh = self.B * self.H
+        return bh * (2 * self.Nq * self.d * 2 + 2 * self.Nk * self.d * 2 + 4 * self.Nq)
+
+
+# The five workloads of the attention forward study, in order.
+WORKLOADS = {
+    "tiny_b1h1n128d64": Workload("tiny_b1h1n128d64", 1, 1, 128, 128, 64, False, seed=1000),
+    "b4h8n1024d64": Workload("b4h8n1024d64", 4, 8, 1024, 1024, 64, False, seed=1001),
+    "b2h16n4096d128_causal": Workload("b2h16n4096d128_causal", 2, 16, 4096, 4096, 128, True,
+                                      seed=1002),
+    "b1h32n16384d128_causal": Workload("b1h32n16384d128_causal", 1, 32, 16384, 16384, 128,
+                                       True, sigma_qk=1.5, seed=1003),
+    "decode_b64h32nk8192d128": Workload("decode_b64h32nk8192d128", 64, 32, 1, 8192, 128, False,
+                                        seed=1004),
+}
+
+
+def make_qkv(B, H, Nq, Nk, d, seed, device="cpu", sigma_qk=1.0, sigma_v=1.0):
+    """Q [B,H,Nq,d], K and V [B,H,Nk,d], bf16, contiguous, on ``device``."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    q = torch.randn((B, H, Nq, d), generator=g, device=device, dtype=torch.float32)
+    q = (q * sigma_qk).to(torch.bfloat16)
+    k = torch.randn((B, H, Nk, d), generator=g, device=device, dtype=torch.float32)
+    k = (k * sigma_qk).to(torch.bfloat16)
+    v = torch.randn((B, H, Nk, d), generator=g, device=device, dtype=torch.float32)
+    v = (v * sigma_v).to(torch.bfloat16)
+    return q, k, v
+
+
+def make_workload(w: Workload, device="cpu", seed=None):
+    return make_qkv(w.B, w.H, w.Nq, w.Nk, w.d, w.seed if seed is None else seed, device,
+                    sigma_qk=w.sigma_qk)
+
+
+def bf16_bits(t: torch.Tensor):
+    """The raw 16-bit patterns of a bf16 tensor as a numpy uint16 array (CPU copy)."""
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view("uint16")

@@ -1,0 +1,149 @@
+"""fp64 CPU oracle for scaled-dot-product attention (test infrastructure).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It is a thin ctypes wrapper around the
+plain C implementation in ``attn_oracle.c`` (built by ``oracle/build.py``); it
+shares nothing with the CUDA library.
+
+Functions (each follows a passage of the lecture pages, cited in the C file):
+
+* :func:`attention` -- naive attention, S = scale Q K^T, safe softmax, O = P V,
+  lse = m + ln l (CS149 L9 concept 8; PDC L4 section 4.14; CS336 L5 8.1/8.3).
+* :func:`attention_rows` -- the same on a list of (bh, i) rows.
+* :func:`online_softmax_blocks` -- per-block online softmax (CS336 L5 8.2).
+* :func:`softmax_merge` -- two-block merge rule (CS149 L9 concept 9).
+* :func:`attention_blocked` -- tiled FlashAttention forward (CS336 L5 8.3).
+
+Inputs are numpy arrays, either float64 or bfloat16 bit patterns (uint16).
+"""
+import ctypes
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def _declare(lib):
+    """Attach the C signatures to a loaded oracle library."""
+    P = ctypes.c_void_p
+    L = ctypes.c_long
+    D = ctypes.c_double
+    I = ctypes.c_int
+    lib.oracle_attention.argtypes = [P, P, P, I, P, P, L, L, L, L, L, I, D]
+    lib.oracle_attention.restype = I
+    lib.oracle_attention_rows.argtypes = [P, P, P, I, P, L, P, P, L, L, L, L, L, I, D]
+    lib.oracle_attention_rows.restype = I
+    lib.oracle_online_softmax_blocks.argtypes = [P, L, P, L, P, P]
+    lib.oracle_online_softmax_blocks.restype = I
+    lib.oracle_softmax_merge.argtypes = [D, D, P, D, D, P, L, P, P, P]
+    lib.oracle_softmax_merge.restype = None
+    lib.oracle_attention_blocked.argtypes = [P, P, P, P, P, L, L, L, L, L, I, D, L, L]
+    lib.oracle_attention_blocked.restype = I
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = I
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = _declare(ctypes.CDLL(_build.build()))
+    return _lib
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _inputs(q, k, v):
+    q, k, v = (np.ascontiguousarray(x) for x in (q, k, v))
+    if q.dtype == np.uint16 and k.dtype == np.uint16 and v.dtype == np.uint16:
+        return q, k, v, 1
+    q, k, v = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v))
+    return q, k, v, 0
+
+
+def attention(q, k, v, causal=False, scale=None):
+    """Naive fp64 attention.  q: [B,H,Nq,d], k/v: [B,H,Nk,d] (float64 or
+    bf16 bits as uint16).  Returns (o float64 [B,H,Nq,d], lse float64 [B,H,Nq])."""
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    q, k, v, is_bf16 = _inputs(q, k, v)
+    o = np.empty((B, H, Nq, d), np.float64)
+    lse = np.empty((B, H, Nq), np.float64)
+    rc = _load().oracle_attention(_ptr(q), _ptr(k), _ptr(v), is_bf16, _ptr(o), _ptr(lse),
+                                  B, H, Nq, Nk, d, int(bool(causal)), float(scale))
+    if rc != 0:
+        raise ValueError("oracle_attention rejected its arguments")
+    return o, lse
+
+
+def attention_rows(q, k, v, rows, causal=False, scale=None):
+    """Rows ``rows`` (int array [n, 2] of (bh, i)) of naive attention.
+    Returns (o [n, d], lse [n])."""
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    q, k, v, is_bf16 = _inputs(q, k, v)
+    rows = np.ascontiguousarray(rows, dtype=np.int64).reshape(-1, 2)
+    n = rows.shape[0]
+    o = np.empty((n, d), np.float64)
+    lse = np.empty((n,), np.float64)
+    rc = _load().oracle_attention_rows(_ptr(q), _ptr(k), _ptr(v), is_bf16, _ptr(rows), n,
+                                       _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
+                                       int(bool(causal)), float(scale))
+    if rc != 0:
+        raise ValueError("oracle_attention_rows rejected its arguments")
+    return o, lse
+
+
+def online_softmax_blocks(x, ends):
+    """Running (m, l) after each block of x; ``ends`` are exclusive block ends."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    ends = np.ascontiguousarray(ends, dtype=np.int64)
+    m = np.empty(len(ends), np.float64)
+    l = np.empty(len(ends), np.float64)
+    rc = _load().oracle_online_softmax_blocks(_ptr(x), x.size, _ptr(ends), ends.size,
+                                              _ptr(m), _ptr(l))
+    if rc != 0:
+        raise ValueError("bad block list")
+    return m, l
+
+
+def softmax_merge(m1, l1, o1, m2, l2, o2):
+    """Merge two blocks' (m, l, normalised o).  Returns (m, l, o)."""
+    o1 = np.ascontiguousarray(o1, dtype=np.float64)
+    o2 = np.ascontiguousarray(o2, dtype=np.float64)
+    o = np.empty_like(o1)
+    m = ctypes.c_double()
+    l = ctypes.c_double()
+    _load().oracle_softmax_merge(float(m1), float(l1), _ptr(o1), float(m2), float(l2),
+                                 _ptr(o2), o1.size, ctypes.byref(m), ctypes.byref(l), _ptr(o))
+    return m.value, l.value, o
+
+
+def attention_blocked(q, k, v, causal=False, scale=None, block_q=128, block_k=128):
+    """Tiled FlashAttention forward in fp64 (float64 inputs only)."""
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    q, k, v = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v))
+    o = np.empty((B, H, Nq, d), np.float64)
+    lse = np.empty((B, H, Nq), np.float64)
+    rc = _load().oracle_attention_blocked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                          B, H, Nq, Nk, d, int(bool(causal)), float(scale),
+                                          int(block_q), int(block_k))
+    if rc != 0:
+        raise ValueError("oracle_attention_blocked rejected its arguments")
+    return o, lse
+
+
+def threads_used() -> int:
+    """Number of threads the oracle's row loops run on (1 without OpenMP)."""
+    return int(_load().oracle_num_threads())

@@ -1,0 +1,294 @@
+"""Checks that pin the fp64 oracle to facts fixed outside the oracle itself.
+
+Each function raises AssertionError when the oracle disagrees with what the
+lecture pages print or with what the mathematics of attention fixes.  They are
+collected by ``test_oracle_pins.py`` and re-run against deliberately broken
+copies of the oracle by ``test_oracle_mutants.py`` (every plausible mistake has
+to fail at least one of them).
+"""
+import json
+import math
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _rand(shape, seed, scale=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * scale
+
+
+# -- values printed by the pages ---------------------------------------------
+
+def pin_exercise8_online_softmax(orc):
+    """CS336 L5 exercise 8: online softmax of [1, 3 | 2, 5] in two blocks."""
+    g = _golden("cs336_l5_exercise8.json")
+    m, l = orc.online_softmax_blocks(g["x"], g["block_ends"])
+    for b, exp in enumerate(g["after_block"]):
+        assert m[b] == exp["m"], (b, m[b], exp["m"])
+    tol0 = 0.5 * 10 ** -g["after_block"][0]["printed_decimals"]
+    assert abs(l[0] - g["after_block"][0]["l"]) <= tol0, l[0]
+    # the page sums three terms it rounded to 4 decimals: allow 3 half-units
+    tol1 = 1.5 * 10 ** -g["after_block"][1]["printed_decimals"]
+    assert abs(l[1] - g["after_block"][1]["l"]) <= tol1, l[1]
+    t = g["second_update_terms"]
+    half = 0.5 * 10 ** -t["printed_decimals"]
+    assert abs(l[0] * math.exp(m[0] - m[1]) - t["old_l_rescaled"]) <= half
+    # the same m, l through the two-block merge rule
+    mm, ll, _ = orc.softmax_merge(m[0], l[0], np.zeros(1), 5.0, math.exp(2 - 5) + 1.0,
+                                  np.zeros(1))
+    assert mm == 5.0 and abs(ll - l[1]) <= 1e-15
+    # the probability of the last element, through full attention: with q = e0,
+    # k_j = x_j e0, scale 1 and V = I the output row is the softmax row itself
+    x = np.array(g["x"])
+    n = len(x)
+    q = np.zeros((1, 1, 1, n)); q[0, 0, 0, 0] = 1.0
+    k = np.zeros((1, 1, n, n)); k[0, 0, :, 0] = x
+    v = np.eye(n)[None, None]
+    o, lse = orc.attention(q, k, v, causal=False, scale=1.0)
+    p_last = g["softmax_of_last"]
+    assert abs(o[0, 0, 0, -1] - p_last["value"]) <= 0.5 * 10 ** -p_last["printed_decimals"]
+    assert abs(o[0, 0, 0, -1] - math.exp(x[-1] - m[1]) / l[1]) <= 1e-15
+    # L = m + log l with the page's final (m, l)
+    assert abs(lse[0, 0, 0] - (m[1] + math.log(l[1]))) <= 1e-14
+
+
+def pin_memory_table(orc):
+    """CS336 L5 section 8.5: extra memory = one fp32 lse per row, vs 2 n^2 bf16."""
+    g = _golden("cs336_l5_memory_table.json")
+    for row in g["rows"]:
+        n = row["n"]
+        # the oracle returns exactly one logsumexp per query row
+        _, lse = orc.attention(np.zeros((1, 1, 2, 1)), np.zeros((1, 1, 2, 1)),
+                               np.zeros((1, 1, 2, 1)))
+        assert lse.shape == (1, 1, 2)
+        extra = n * 4  # fp32 per row
+        assert round(extra / 1e6, 2) == row["flash_extra_MB"], (n, extra)
+        std = 2 * n * n * 2  # S and P in bf16
+        digits = 1 if row["standard_GB"] >= 10 else 2
+        assert round(std / 1e9, digits) == row["standard_GB"], (n, std)
+
+
+# -- closed forms and invariants ---------------------------------------------
+
+def pin_rows_sum_to_one(orc):
+    """With V = I (d = Nk) the output row is the probability row: rows sum to 1,
+    entries are >= 0, and causal rows are exactly 0 beyond the diagonal."""
+    n = 37
+    q = _rand((2, 3, n, n), 1)
+    k = _rand((2, 3, n, n), 2)
+    v = np.broadcast_to(np.eye(n), (2, 3, n, n)).copy()
+    for causal in (False, True):
+        p, _ = orc.attention(q, k, v, causal=causal, scale=0.3)
+        assert np.all(p >= 0)
+        assert np.max(np.abs(p.sum(-1) - 1.0)) <= 1e-14
+        if causal:
+            upper = np.triu(np.ones((n, n), bool), 1)
+            assert np.all(p[..., upper] == 0.0)
+            assert np.all(p[..., ~upper] > 0.0)
+
+
+def pin_q_zero(orc):
+    """Q = 0: every visible logit is 0, so O_i is the mean of the visible V rows
+    and lse_i = ln(number of visible keys)."""
+    B, H, n, d = 2, 2, 29, 8
+    q = np.zeros((B, H, n, d))
+    k = _rand((B, H, n, d), 3)
+    v = _rand((B, H, n, d), 4)
+    o, lse = orc.attention(q, k, v, causal=False)
+    assert np.max(np.abs(o - v.mean(axis=2, keepdims=True))) <= 1e-14
+    assert np.max(np.abs(lse - math.log(n))) <= 1e-14
+    o, lse = orc.attention(q, k, v, causal=True)
+    prefix = np.cumsum(v, axis=2) / np.arange(1, n + 1)[None, None, :, None]
+    assert np.max(np.abs(o - prefix)) <= 1e-14
+    assert np.max(np.abs(lse - np.log(np.arange(1, n + 1))[None, None])) <= 1e-14
+
+
+def pin_one_hot_dominant(orc):
+    """A key whose logit beats every other by >= 50 takes all the weight:
+    O_i = V_{j*} to within e^-50."""
+    B, H, n, d = 1, 2, 40, 16
+    q = _rand((B, H, n, d), 5) * 0.1
+    k = _rand((B, H, n, d), 6) * 0.1
+    v = _rand((B, H, n, d), 7)
+    jstar, i = 17, 30
+    # key j* points along q_i with q_i . k_j* = 80, far above every other logit
+    k[:, :, jstar, :] = 80.0 * q[:, :, i, :] / np.sum(q[:, :, i, :] ** 2, axis=-1, keepdims=True)
+    o, lse = orc.attention(q, k, v, causal=False, scale=1.0)
+    others = np.einsum("bhc,bhjc->bhj", q[:, :, i, :], np.delete(k, jstar, axis=2))
+    assert np.max(others) < 80.0 - 50.0
+    bound = n * math.exp(-50) * np.max(np.abs(v)) * 2
+    assert np.max(np.abs(o[:, :, i, :] - v[:, :, jstar, :])) <= bound
+    assert np.max(np.abs(lse[:, :, i] - 80.0)) <= 1e-12
+
+
+def pin_causal_row0(orc):
+    """Causal row 0 sees only key 0: O_0 = V_0 and lse_0 = scale q_0 . k_0."""
+    B, H, n, d = 2, 3, 19, 12
+    q, k, v = _rand((B, H, n, d), 8), _rand((B, H, n, d), 9), _rand((B, H, n, d), 10)
+    o, lse = orc.attention(q, k, v, causal=True, scale=0.25)
+    assert np.array_equal(o[:, :, 0, :], v[:, :, 0, :])
+    ref = 0.25 * np.einsum("bhc,bhc->bh", q[:, :, 0, :], k[:, :, 0, :])
+    assert np.max(np.abs(lse[:, :, 0] - ref)) <= 1e-14
+
+
+def pin_v_affine(orc):
+    """Rows of P sum to 1, so O(a V + b) = a O(V) + b, and lse does not change."""
+    B, H, n, d = 1, 2, 33, 8
+    q, k, v = _rand((B, H, n, d), 11), _rand((B, H, n, d), 12), _rand((B, H, n, d), 13)
+    for causal in (False, True):
+        o1, l1 = orc.attention(q, k, v, causal=causal)
+        o2, l2 = orc.attention(q, k, -1.5 * v + 0.75, causal=causal)
+        assert np.max(np.abs(o2 - (-1.5 * o1 + 0.75))) <= 1e-13
+        assert np.array_equal(l1, l2)
+
+
+def pin_key_permutation(orc):
+    """Non-causal attention is a set function of the (key, value) pairs."""
+    B, H, n, d = 2, 2, 31, 8
+    q, k, v = _rand((B, H, n, d), 14), _rand((B, H, n, d), 15), _rand((B, H, n, d), 16)
+    perm = np.random.default_rng(17).permutation(n)
+    o1, l1 = orc.attention(q, k, v)
+    o2, l2 = orc.attention(q, k[:, :, perm], v[:, :, perm])
+    assert np.max(np.abs(o1 - o2)) <= 1e-14
+    assert np.max(np.abs(l1 - l2)) <= 1e-14
+
+
+def pin_scale_is_applied(orc):
+    """S = scale Q K^T: scaling Q by c with scale s equals scale c*s."""
+    B, H, n, d = 1, 1, 21, 8
+    q, k, v = _rand((B, H, n, d), 18), _rand((B, H, n, d), 19), _rand((B, H, n, d), 20)
+    o1, l1 = orc.attention(q * 4.0, k, v, scale=0.125)
+    o2, l2 = orc.attention(q, k, v, scale=0.5)
+    assert np.max(np.abs(o1 - o2)) <= 1e-14 and np.max(np.abs(l1 - l2)) <= 1e-13
+    # and the default is 1 / sqrt(d)
+    o3, l3 = orc.attention(q, k, v)
+    o4, l4 = orc.attention(q, k, v, scale=1.0 / math.sqrt(d))
+    assert np.array_equal(o3, o4) and np.array_equal(l3, l4)
+
+
+# -- blocked / online forms against the unblocked definition ------------------
+
+def pin_blocked_equals_unblocked(orc):
+    """The tiled forward (CS336 L5 8.3) equals naive attention for any block
+    sizes, dividing N or not (CS336 L5 exercise 10a)."""
+    B, H, n, d = 1, 2, 45, 8
+    q, k, v = _rand((B, H, n, d), 21), _rand((B, H, n, d), 22), _rand((B, H, n, d), 23)
+    for causal in (False, True):
+        o, lse = orc.attention(q, k, v, causal=causal)
+        for br, bc in ((1, 1), (7, 5), (16, 16), (45, 45), (64, 3), (8, 64)):
+            ob, lb = orc.attention_blocked(q, k, v, causal=causal, block_q=br, block_k=bc)
+            assert np.max(np.abs(ob - o)) <= 1e-13, (causal, br, bc)
+            assert np.max(np.abs(lb - lse)) <= 1e-13, (causal, br, bc)
+
+
+def pin_merge_rule(orc):
+    """CS149 L9 concept 9: attention over keys [0, s) and [s, n) separately,
+    merged with m = max(m1, m2), l = e^{m1-m} l1 + e^{m2-m} l2, equals attention
+    over all keys (the split-K decode combine)."""
+    n, d = 50, 8
+    q, k, v = _rand((1, 1, 3, d), 24), _rand((1, 1, n, d), 25), _rand((1, 1, n, d), 26)
+    o, lse = orc.attention(q, k, v, scale=0.7)
+    for s in (1, 13, 25, 49):
+        o1, l1 = orc.attention(q, k[:, :, :s], v[:, :, :s], scale=0.7)
+        o2, l2 = orc.attention(q, k[:, :, s:], v[:, :, s:], scale=0.7)
+        for i in range(3):
+            # a block's (m, l) is any pair with m + ln l = its lse; take m = lse, l = 1
+            m, l, om = orc.softmax_merge(l1[0, 0, i], 1.0, o1[0, 0, i], l2[0, 0, i], 1.0,
+                                         o2[0, 0, i])
+            assert abs(m + math.log(l) - lse[0, 0, i]) <= 1e-13
+            assert np.max(np.abs(om - o[0, 0, i])) <= 1e-14
+
+
+# -- independent implementations -----------------------------------------------
+
+def pin_bruteforce_fsum(orc):
+    """Tiny shapes against a second implementation in pure Python with
+    exactly-rounded sums (math.fsum)."""
+    rng = np.random.default_rng(27)
+    for (n, m, d, causal) in ((1, 1, 1, False), (3, 5, 2, False), (6, 6, 3, True), (8, 8, 4, True)):
+        q = rng.standard_normal((1, 1, n, d))
+        k = rng.standard_normal((1, 1, m, d))
+        v = rng.standard_normal((1, 1, m, d))
+        scale = 0.9
+        o, lse = orc.attention(q, k, v, causal=causal, scale=scale)
+        for i in range(n):
+            logits = [scale * math.fsum(q[0, 0, i, c] * k[0, 0, j, c] for c in range(d))
+                      for j in range(m) if not (causal and j > i)]
+            mx = max(logits)
+            w = [math.exp(s - mx) for s in logits]
+            tot = math.fsum(w)
+            assert abs(lse[0, 0, i] - (mx + math.log(tot))) <= 1e-13
+            for c in range(d):
+                ref = math.fsum(w[j] * v[0, 0, j, c] for j in range(len(w))) / tot
+                assert abs(o[0, 0, i, c] - ref) <= 1e-14
+
+
+def pin_torch_crosscheck(orc):
+    """The pages' own checks (CS336 L5 8.2/8.3 demos): agreement with
+    torch.softmax(S) @ V and F.scaled_dot_product_attention in float64."""
+    import torch
+    import torch.nn.functional as F
+    B, H, n, d = 2, 3, 24, 16
+    g = torch.Generator().manual_seed(28)
+    q, k, v = (torch.randn(B, H, n, d, generator=g, dtype=torch.float64) for _ in range(3))
+    for causal in (False, True):
+        o, lse = orc.attention(q.numpy(), k.numpy(), v.numpy(), causal=causal)
+        ref = F.scaled_dot_product_attention(q, k, v, is_causal=causal)
+        s = (q @ k.transpose(-1, -2)) / math.sqrt(d)
+        if causal:
+            s = s.masked_fill(torch.triu(torch.ones(n, n, dtype=torch.bool), 1), float("-inf"))
+        ref2 = torch.softmax(s, dim=-1) @ v
+        assert np.max(np.abs(o - ref.numpy())) <= 1e-12
+        assert np.max(np.abs(o - ref2.numpy())) <= 1e-12
+        assert np.max(np.abs(lse - torch.logsumexp(s, dim=-1).numpy())) <= 1e-12
+
+
+def pin_bf16_widening(orc):
+    """bf16 bit patterns are widened exactly: the uint16 path equals the float64
+    path on the same values (values from torch's own bf16 -> float64)."""
+    import torch
+    g = torch.Generator().manual_seed(29)
+    q, k, v = (torch.randn(1, 2, 9, 8, generator=g).to(torch.bfloat16) for _ in range(3))
+    bits = [t.view(torch.int16).numpy().view(np.uint16) for t in (q, k, v)]
+    wide = [t.to(torch.float64).numpy() for t in (q, k, v)]
+    o1, l1 = orc.attention(*bits, causal=True)
+    o2, l2 = orc.attention(*wide, causal=True)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def pin_rows_equal_full(orc):
+    """The sampled-row entry point returns exactly the full computation's rows."""
+    B, H, n, d = 2, 2, 17, 8
+    q, k, v = _rand((B, H, n, d), 30), _rand((B, H, n, d), 31), _rand((B, H, n, d), 32)
+    o, lse = orc.attention(q, k, v, causal=True)
+    rows = np.array([[0, 0], [3, 16], [1, 5], [2, 9]])
+    orow, lrow = orc.attention_rows(q, k, v, rows, causal=True)
+    for t, (bh, i) in enumerate(rows):
+        assert np.array_equal(orow[t], o.reshape(B * H, n, d)[bh, i])
+        assert lrow[t] == lse.reshape(B * H, n)[bh, i]
+
+
+ALL_PINS = [
+    pin_exercise8_online_softmax,
+    pin_memory_table,
+    pin_rows_sum_to_one,
+    pin_q_zero,
+    pin_one_hot_dominant,
+    pin_causal_row0,
+    pin_v_affine,
+    pin_key_permutation,
+    pin_scale_is_applied,
+    pin_blocked_equals_unblocked,
+    pin_merge_rule,
+    pin_bruteforce_fsum,
+    pin_torch_crosscheck,
+    pin_bf16_widening,
+    pin_rows_equal_full,
+]

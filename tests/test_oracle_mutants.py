@@ -1,0 +1,59 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins
+catch every one of them (the pins are strong enough to notice a dropped term,
+a wrong sign, a wrong index or a swapped operand).  CPU only."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests.oracle_pins import ALL_PINS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c")
+
+# (name, original text, planted mistake); every original occurs exactly once
+MUTANTS = [
+    ("scale_dropped", "srow[j] = scale * dot;", "srow[j] = dot;"),
+    ("exp_sign_flipped", "exp(srow[j] - m);", "exp(m - srow[j]);"),
+    ("not_normalised", "srow[j] /= l;", "srow[j] /= 1.0;"),
+    ("causal_masks_diagonal", "if (causal && j > i) {\n            srow[j] = -INFINITY;",
+     "if (causal && j >= i) {\n            srow[j] = -INFINITY;"),
+    ("causal_mask_transposed", "if (causal && j > i) {\n            srow[j] = -INFINITY;",
+     "if (causal && j < i) {\n            srow[j] = -INFINITY;"),
+    ("lse_without_max", "*lse_out = m + log(l);", "*lse_out = log(l);"),
+    ("lse_base2", "*lse_out = m + log(l);", "*lse_out = m + log2(l);"),
+    ("scores_use_v", "load_elem(k, kvbase + (size_t)j * (size_t)d + (size_t)c, is_bf16)",
+     "load_elem(v, kvbase + (size_t)j * (size_t)d + (size_t)c, is_bf16)"),
+    ("output_uses_k", "o_row[c] += srow[j] * load_elem(v,", "o_row[c] += srow[j] * load_elem(k,"),
+    ("online_no_rescale", "l * exp(m - m_new)) + s;", "l) + s;"),
+    ("merge_sign_flipped", "exp(m1 - m);", "exp(m - m1);"),
+    ("blocked_no_o_rescale", "acc[r * d + c] = alpha * acc[r * d + c] + pv;",
+     "acc[r * d + c] = acc[r * d + c] + pv;"),
+    ("blocked_skips_diagonal_block", "if (causal && j0 > i0 + br - 1)", "if (causal && j0 > i0)"),
+    ("bf16_widening_shift", "(uint32_t)bits << 16;", "(uint32_t)bits << 15;"),
+]
+
+
+def _build_mutant(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, name
+    path_c = tmp_path / f"{name}.c"
+    path_c.write_text(src.replace(old, new))
+    path_so = tmp_path / f"{name}.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-ffp-contract=off",
+                    str(path_c), "-o", str(path_so), "-lm"], check=True)
+    return oracle._declare(ctypes.CDLL(str(path_so)))
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, monkeypatch, name, old, new):
+    lib = _build_mutant(tmp_path, name, old, new)
+    monkeypatch.setattr(oracle, "_lib", lib)
+    failed = []
+    for pin in ALL_PINS:
+        try:
+            pin(oracle)
+        except (AssertionError, ValueError):
+            failed.append(pin.__name__)
+    assert failed, f"no pin noticed the planted mistake {name!r}"
