@@ -13,7 +13,7 @@ def __getattr__(name):
     # The binding is imported on first use so that the input generator works on
     # machines without the built library; every compute entry point raises if
     # the CUDA library is missing.
-    if name in ("attn_fwd", "attn_fwd_decode", "attn_fwd_from_host", "binding"):
-        from . import binding
-        return binding if name == "binding" else getattr(binding, name)
+    if name in ("attention", "attn_fwd", "attn_fwd_decode", "attn_fwd_from_host"):
+        import importlib
+        return getattr(importlib.import_module(__name__ + ".binding"), name)
     raise AttributeError(name)

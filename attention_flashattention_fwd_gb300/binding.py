@@ -1,0 +1,168 @@
+"""ctypes binding of ``libgbattn.so`` (the C ABI in ``include/gbattn.h``).
+
+Argument marshalling only: tensors are checked for device, dtype, shape and
+contiguity, their pointers and the current CUDA stream are handed to the C
+entry points of the same names, and a non-zero status is raised as
+:class:`GbattnError`.  Every step of the computation runs in the CUDA kernels;
+there is no fallback.  If the library has not been built, the first call
+raises.
+"""
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgbattn.so")
+
+ATTN_OK = 0
+_lib = None
+
+
+class GbattnError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def load():
+    """Load the CUDA library (raises if it is missing)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"{LIB_PATH} is not built; run `python -c \"import __graft_entry__ as g; "
+                f"g.build()\"` (or attention_flashattention_fwd_gb300/build_lib.py)")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]
+        lib.attn_fwd.restype = I
+        lib.attn_fwd_decode_workspace_bytes.argtypes = [I, I, I, I]
+        lib.attn_fwd_decode_workspace_bytes.restype = S
+        lib.attn_fwd_decode.argtypes = [P, P, P, P, P, I, I, I, I, F, P, S, P]
+        lib.attn_fwd_decode.restype = I
+        lib.attn_fwd_from_host.argtypes = [P] * 10 + [I, I, I, I, I, I, F, P]
+        lib.attn_fwd_from_host.restype = I
+        lib.attn_status_string.argtypes = [I]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_device_error.argtypes = []
+        lib.attn_device_error.restype = I
+        lib.attn_version.argtypes = []
+        lib.attn_version.restype = I
+        _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().attn_status_string(int(status)).decode()
+
+
+def _check(status, where):
+    if status != ATTN_OK:
+        raise GbattnError(status, where)
+
+
+def _stream_ptr(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _check_inputs(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be bfloat16")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [B, H, N, d] tensor")
+    B, H, Nq, d = q.shape
+    if k.shape != (B, H, k.shape[2], d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, H, Nk, d] with q's B, H and d")
+    return B, H, Nq, k.shape[2], d
+
+
+def attention(q, k, v, causal=False, scale=None, stream=None):
+    """O = softmax(scale Q K^T [+ causal mask]) V and the fp32 logsumexp,
+    through ``attn_fwd_decode`` for a single non-causal query row and
+    ``attn_fwd`` otherwise."""
+    if q.dim() == 4 and q.shape[2] == 1 and not causal:
+        return attn_fwd_decode(q, k, v, scale=scale, stream=stream)
+    return attn_fwd(q, k, v, causal=causal, scale=scale, stream=stream)
+
+
+def attn_fwd(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None):
+    """The C entry point ``attn_fwd`` (prefill kernel) on torch tensors.
+
+    q [B,H,Nq,d], k/v [B,H,Nk,d] bf16 CUDA tensors.  Returns
+    (o bf16 [B,H,Nq,d], lse fp32 [B,H,Nq]).
+    """
+    B, H, Nq, Nk, d = _check_inputs(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    st = load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nk, d,
+                         int(bool(causal)), float(scale), _stream_ptr(stream))
+    _check(st, "attn_fwd")
+    return out, lse
+
+
+def decode_workspace_bytes(B, H, Nk, d) -> int:
+    return int(load().attn_fwd_decode_workspace_bytes(B, H, Nk, d))
+
+
+def attn_fwd_decode(q, k, v, scale=None, out=None, lse=None, workspace=None, stream=None):
+    """Single-query attention forward (q [B,H,1,d]) split over the keys.
+    ``workspace`` (a CUDA uint8 tensor) is allocated here when not given."""
+    B, H, Nq, Nk, d = _check_inputs(q, k, v)
+    if Nq != 1:
+        raise ValueError("attn_fwd_decode takes a single query row (Nq = 1)")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, 1, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, 1), dtype=torch.float32, device=q.device)
+    need = decode_workspace_bytes(B, H, Nk, d)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = _ptr(workspace) if workspace is not None else ctypes.c_void_p(0)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().attn_fwd_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nk, d,
+                                float(scale), ws_ptr, ws_bytes, _stream_ptr(stream))
+    _check(st, "attn_fwd_decode")
+    return out, lse
+
+
+def attn_fwd_from_host(q, k, v, o, lse, dq, dk, dv, do_, dlse, causal=False, scale=None,
+                       stream=None):
+    """End-to-end attn_fwd on pinned HOST tensors (q, k, v in; o, lse out)
+    through the caller's device buffers dq, dk, dv, do_, dlse.  Asynchronous
+    on ``stream``: synchronise before reading o and lse."""
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    for t in (q, k, v, o, lse):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v, o, lse must be contiguous host tensors")
+    for t in (dq, dk, dv, do_, dlse):
+        if not t.is_cuda:
+            raise ValueError("dq, dk, dv, do_, dlse must be CUDA tensors")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = load().attn_fwd_from_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dq),
+                                   _ptr(dk), _ptr(dv), _ptr(do_), _ptr(dlse), B, H, Nq, Nk, d,
+                                   int(bool(causal)), float(scale), _stream_ptr(stream))
+    _check(st, "attn_fwd_from_host")
+    return o, lse
+
+
+def device_error() -> int:
+    """Synchronise and read/clear the kernels' device error word (0 = none)."""
+    return int(load().attn_device_error())

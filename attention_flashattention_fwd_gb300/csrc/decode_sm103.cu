@@ -1,0 +1,248 @@
+// decode_sm103.cu -- single-query attention forward, split over the keys.
+//
+// Decode reads every key and value once and does about one FLOP per byte
+// (CS336 Lecture 5 notes, section 5.3: decode is memory-bound), so the job is
+// to stream K and V at HBM speed:
+//   * the keys of one (b, h) are cut into `splits` contiguous ranges; one CTA
+//     streams one range with coalesced 16-byte loads (a key row of d bf16 is
+//     read by d/8 neighbouring lanes; the lanes of a warp read neighbouring
+//     rows), bypassing L1 because nothing is read twice;
+//   * each group of d/8 lanes keeps its own running max m and sum l and an
+//     fp32 output slice (online softmax, CS336 Lecture 5 notes, section 8.2),
+//     the groups of a CTA are merged through shared memory with the two-block
+//     rule of CS149 Lecture 9 notes, concept 9, and the CTA writes a partial
+//     (o_s, lse_s) to the workspace;
+//   * a second, tiny kernel merges the splits of each (b, h) with the same rule
+//     (the "second launch as a global barrier" of the PDC course, section 5.14)
+//     and writes bf16 O and the fp32 logsumexp.  With a single split the first
+//     kernel writes the final result itself.
+// Scores are kept in base 2 (c = scale * log2 e) as in the prefill kernel.
+#include <cuda_bf16.h>
+
+#include "gbattn_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace gbattn {
+
+namespace {
+
+constexpr int kDecThreads = 256;   // 8 warps
+constexpr int kUnroll = 8;         // key rows in flight per lane group and iteration
+constexpr float kLn2 = 0.69314718055994530942f;
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// dot of 8 bf16 values packed in a uint4 with 8 fp32 values
+__device__ __forceinline__ float dot8(const float (&q)[8], uint4 k) {
+    float s = q[0] * bf_lo(k.x);
+    s = fmaf(q[1], bf_hi(k.x), s);
+    s = fmaf(q[2], bf_lo(k.y), s);
+    s = fmaf(q[3], bf_hi(k.y), s);
+    s = fmaf(q[4], bf_lo(k.z), s);
+    s = fmaf(q[5], bf_hi(k.z), s);
+    s = fmaf(q[6], bf_lo(k.w), s);
+    s = fmaf(q[7], bf_hi(k.w), s);
+    return s;
+}
+
+__device__ __forceinline__ void axpy8(float (&acc)[8], float p, uint4 v) {
+    acc[0] = fmaf(p, bf_lo(v.x), acc[0]);
+    acc[1] = fmaf(p, bf_hi(v.x), acc[1]);
+    acc[2] = fmaf(p, bf_lo(v.y), acc[2]);
+    acc[3] = fmaf(p, bf_hi(v.y), acc[3]);
+    acc[4] = fmaf(p, bf_lo(v.z), acc[4]);
+    acc[5] = fmaf(p, bf_hi(v.z), acc[5]);
+    acc[6] = fmaf(p, bf_lo(v.w), acc[6]);
+    acc[7] = fmaf(p, bf_hi(v.w), acc[7]);
+}
+
+}  // namespace
+
+// One CTA = one (b, h, split).  Lane group g (d/8 lanes) handles keys
+// ks + g, ks + g + G, ... where G = lane groups per CTA.
+template <int D>
+__global__ void __launch_bounds__(kDecThreads)
+    attn_fwd_decode_split_kernel(DecodeParams p) {
+    constexpr int kLanesPerRow = D / 8;              // 16 (d=128) or 8 (d=64)
+    constexpr int kGroupsPerWarp = 32 / kLanesPerRow;
+    constexpr int kGroups = (kDecThreads / 32) * kGroupsPerWarp;
+
+    __shared__ float sm_m[kGroups];
+    __shared__ float sm_l[kGroups];
+    __shared__ float sm_acc[kGroups][D];
+
+    const int bh = blockIdx.x / p.splits;
+    const int split = blockIdx.x % p.splits;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = warp * kGroupsPerWarp + lane / kLanesPerRow;
+    const int sub = lane % kLanesPerRow;  // which 8-element slice of the row
+
+    const int ks = split * p.keys_per_split;
+    const int ke = min(p.Nk, ks + p.keys_per_split);
+
+    float q[8];
+    {
+        const uint4 qr = *reinterpret_cast<const uint4*>(p.q + static_cast<size_t>(bh) * D + sub * 8);
+        q[0] = bf_lo(qr.x); q[1] = bf_hi(qr.x); q[2] = bf_lo(qr.y); q[3] = bf_hi(qr.y);
+        q[4] = bf_lo(qr.z); q[5] = bf_hi(qr.z); q[6] = bf_lo(qr.w); q[7] = bf_hi(qr.w);
+        // fold scale * log2(e) into q once
+#pragma unroll
+        for (int e = 0; e < 8; ++e) q[e] *= p.scale_log2;
+    }
+    const __nv_bfloat16* kbase = p.k + static_cast<size_t>(bh) * p.Nk * D + sub * 8;
+    const __nv_bfloat16* vbase = p.v + static_cast<size_t>(bh) * p.Nk * D + sub * 8;
+
+    float m = -INFINITY, l = 0.f;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+
+    for (int base = ks; base < ke; base += kGroups * kUnroll) {
+        uint4 kr[kUnroll], vr[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int j = base + u * kGroups + g;
+            if (j < ke) {
+                kr[u] = ld_stream(kbase + static_cast<size_t>(j) * D);
+                vr[u] = ld_stream(vbase + static_cast<size_t>(j) * D);
+            } else {
+                kr[u] = make_uint4(0, 0, 0, 0);
+                vr[u] = make_uint4(0, 0, 0, 0);
+            }
+        }
+        float s[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) s[u] = dot8(q, kr[u]);
+        // sum the d/8 partial dots of each row across its lane group
+#pragma unroll
+        for (int off = kLanesPerRow / 2; off >= 1; off >>= 1)
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) s[u] += __shfl_xor_sync(0xffffffffu, s[u], off);
+        float mx = m;
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            if (base + u * kGroups + g >= ke) s[u] = -INFINITY;
+            mx = fmaxf(mx, s[u]);
+        }
+        if (mx == -INFINITY) continue;  // every key of this group is past the range
+        const float alpha = ex2_approx(m - mx);  // m = -inf on the first visit gives 0
+        l *= alpha;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] *= alpha;
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const float pu = ex2_approx(s[u] - mx);
+            l += pu;
+            axpy8(acc, pu, vr[u]);
+        }
+        m = mx;
+    }
+
+    // ---- merge the lane groups of the CTA
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sm_acc[g][sub * 8 + e] = acc[e];
+    if (sub == 0) {
+        sm_m[g] = m;
+        sm_l[g] = l;
+    }
+    __syncthreads();
+    if (threadIdx.x < D) {
+        const int c = threadIdx.x;
+        float M = -INFINITY;
+#pragma unroll 4
+        for (int i = 0; i < kGroups; ++i) M = fmaxf(M, sm_m[i]);
+        float Lsum = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+            for (int i = 0; i < kGroups; ++i) {
+                if (sm_m[i] == -INFINITY) continue;
+                const float w = ex2_approx(sm_m[i] - M);
+                Lsum = fmaf(w, sm_l[i], Lsum);
+                O = fmaf(w, sm_acc[i][c], O);
+            }
+        }
+        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+        if (p.splits == 1) {
+            p.o[static_cast<size_t>(bh) * D + c] = __float2bfloat16_rn(O * inv);
+            if (c == 0) p.lse[bh] = (M + log2f(Lsum)) * kLn2;
+        } else {
+            const size_t ps = static_cast<size_t>(bh) * p.splits + split;
+            p.part_o[ps * D + c] = O * inv;
+            if (c == 0) p.part_lse[ps] = Lsum > 0.f ? M + log2f(Lsum) : -INFINITY;
+        }
+    }
+}
+
+// Merge the splits of one (b, h): lse = log2 sum_s 2^{lse_s},
+// o = sum_s 2^{lse_s - lse} o_s.  One CTA per (b, h), one thread per column.
+template <int D>
+__global__ void __launch_bounds__(D) attn_fwd_decode_combine_kernel(DecodeParams p) {
+    const int bh = blockIdx.x;
+    const int c = threadIdx.x;
+    const float* pl = p.part_lse + static_cast<size_t>(bh) * p.splits;
+    const float* po = p.part_o + static_cast<size_t>(bh) * p.splits * D;
+    float M = -INFINITY;
+    for (int s = 0; s < p.splits; ++s) M = fmaxf(M, pl[s]);
+    float Lsum = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+        for (int s = 0; s < p.splits; ++s) {
+            if (pl[s] == -INFINITY) continue;
+            const float w = ex2_approx(pl[s] - M);
+            Lsum += w;
+            O = fmaf(w, po[static_cast<size_t>(s) * D + c], O);
+        }
+    }
+    p.o[static_cast<size_t>(bh) * D + c] = __float2bfloat16_rn(Lsum > 0.f ? O / Lsum : 0.f);
+    if (c == 0) p.lse[bh] = (M + log2f(Lsum)) * kLn2;
+}
+
+// ------------------------------------------------------------------ host side
+
+// Split policy: aim for a few thousand CTAs (the GPU has 152 SMs), never fewer
+// than 512 keys per split, at most 64 splits.  Pure arithmetic on the sizes.
+void decode_split_plan(long long BH, int Nk, int* splits, int* keys_per_split) {
+    const long long kTargetCtas = 4 * 152 * 4;
+    const int kMinKeys = 512;
+    long long s = (kTargetCtas + BH - 1) / BH;
+    const long long max_by_keys = (Nk + kMinKeys - 1) / kMinKeys;
+    if (s > max_by_keys) s = max_by_keys;
+    if (s > 64) s = 64;
+    if (s < 1) s = 1;
+    int kps = static_cast<int>((Nk + s - 1) / s);
+    s = (Nk + kps - 1) / kps;  // no empty split
+    *splits = static_cast<int>(s);
+    *keys_per_split = kps;
+}
+
+size_t decode_workspace_bytes(long long BH, int Nk, int d) {
+    int splits, kps;
+    decode_split_plan(BH, Nk, &splits, &kps);
+    if (splits <= 1) return 0;
+    const size_t n = static_cast<size_t>(BH) * splits;
+    // partial outputs [BH, splits, d] fp32, then partial lse [BH, splits] fp32
+    return n * d * sizeof(float) + n * sizeof(float);
+}
+
+int launch_decode(int d, const DecodeParams& p, cudaStream_t stream) {
+    const long long grid = static_cast<long long>(p.BH) * p.splits;
+    if (d == 128) {
+        attn_fwd_decode_split_kernel<128><<<static_cast<unsigned>(grid), kDecThreads, 0, stream>>>(p);
+        if (p.splits > 1)
+            attn_fwd_decode_combine_kernel<128><<<p.BH, 128, 0, stream>>>(p);
+    } else {
+        attn_fwd_decode_split_kernel<64><<<static_cast<unsigned>(grid), kDecThreads, 0, stream>>>(p);
+        if (p.splits > 1)
+            attn_fwd_decode_combine_kernel<64><<<p.BH, 64, 0, stream>>>(p);
+    }
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace gbattn

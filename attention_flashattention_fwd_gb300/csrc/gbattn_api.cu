@@ -1,0 +1,191 @@
+// gbattn_api.cu -- the extern "C" entry points of libgbattn (declared in
+// include/gbattn.h): argument validation, TMA descriptor encoding and kernel
+// launches.  Every check happens before the first CUDA call, so a rejected
+// call launches nothing.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "gbattn_internal.h"
+
+using namespace gbattn;
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shared checks of attn_fwd and attn_fwd_from_host (no CUDA call).
+int validate_fwd(const void* q, const void* k, const void* v, const void* o, const void* lse,
+                 int B, int H, int Nq, int Nk, int d, int causal, float scale) {
+    if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0) return ATTN_ERR_INVALID_ARG;
+    if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (causal && Nq != Nk) return ATTN_ERR_UNSUPPORTED;  // mask alignment undefined
+    const long long BH = static_cast<long long>(B) * H;
+    // grid and TMA coordinate range: (b*H + h) and the CTA count fit in int32
+    const long long pairs = (static_cast<long long>(Nq) + 255) / 256;
+    if (BH > 0x7fffffffLL || BH * pairs > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+int g_init_status = ATTN_OK;
+std::once_flag g_init_once;
+
+void init_once() {
+    cudaDriverEntryPointQueryResult qres;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &qres) != cudaSuccess ||
+        qres != cudaDriverEntryPointSuccess || fn == nullptr) {
+        g_init_status = ATTN_ERR_CUDA;
+        return;
+    }
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    g_init_status = prefill_set_attributes();
+}
+
+int ensure_init() {
+    std::call_once(g_init_once, init_once);
+    return g_init_status;
+}
+
+// [BH, N, d] bf16 viewed as a 3-D tensor (d innermost), boxes of 64 x 128 x 1
+// with the 128-byte swizzle the tcgen05 operand descriptors expect.
+int encode_bhnd(CUtensorMap* m, const void* base, long long BH, int N, int d) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                             static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int enqueue_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int Nq, int Nk, int d, int causal, float scale, cudaStream_t stream) {
+    int st = ensure_init();
+    if (st != ATTN_OK) return st;
+    const long long BH = static_cast<long long>(B) * H;
+    CUtensorMap tq, tk, tv;
+    if ((st = encode_bhnd(&tq, q, BH, Nq, d)) != ATTN_OK) return st;
+    if ((st = encode_bhnd(&tk, k, BH, Nk, d)) != ATTN_OK) return st;
+    if ((st = encode_bhnd(&tv, v, BH, Nk, d)) != ATTN_OK) return st;
+    PrefillParams p;
+    p.o = static_cast<__nv_bfloat16*>(o);
+    p.lse = lse;
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.BH = static_cast<int>(BH);
+    p.num_pairs = (Nq + 255) / 256;
+    p.causal = causal;
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    return launch_prefill(d, tq, tk, tv, p, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+             int Nq, int Nk, int d, int causal, float scale, void* stream) {
+    int st = validate_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale);
+    if (st != ATTN_OK) return st;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return ATTN_ERR_MISALIGNED;
+    return enqueue_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale,
+                       static_cast<cudaStream_t>(stream));
+}
+
+size_t attn_fwd_decode_workspace_bytes(int B, int H, int Nk, int d) {
+    if (B <= 0 || H <= 0 || Nk <= 0 || (d != 64 && d != 128)) return 0;
+    return decode_workspace_bytes(static_cast<long long>(B) * H, Nk, d);
+}
+
+int attn_fwd_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                    int H, int Nk, int d, float scale, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+    if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || Nk <= 0) return ATTN_ERR_INVALID_ARG;
+    if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    const long long BH = static_cast<long long>(B) * H;
+    int splits, kps;
+    decode_split_plan(BH, Nk, &splits, &kps);
+    if (BH * splits > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    const size_t need = decode_workspace_bytes(BH, Nk, d);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+        (need > 0 && !aligned16(workspace)))
+        return ATTN_ERR_MISALIGNED;
+    DecodeParams p;
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.k = static_cast<const __nv_bfloat16*>(k);
+    p.v = static_cast<const __nv_bfloat16*>(v);
+    p.o = static_cast<__nv_bfloat16*>(o);
+    p.lse = lse;
+    p.part_o = static_cast<float*>(workspace);
+    p.part_lse = need > 0 ? static_cast<float*>(workspace) + BH * splits * d : nullptr;
+    p.BH = static_cast<int>(BH);
+    p.Nk = Nk;
+    p.splits = splits;
+    p.keys_per_split = kps;
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    return launch_decode(d, p, static_cast<cudaStream_t>(stream));
+}
+
+int attn_fwd_from_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                       void* dq, void* dk, void* dv, void* do_, float* dlse, int B, int H,
+                       int Nq, int Nk, int d, int causal, float scale, void* stream) {
+    int st = validate_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale);
+    if (st != ATTN_OK) return st;
+    if (!dq || !dk || !dv || !do_ || !dlse) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(do_) || !aligned16(dlse))
+        return ATTN_ERR_MISALIGNED;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t BH = static_cast<size_t>(B) * H;
+    const size_t qbytes = BH * Nq * d * 2, kvbytes = BH * Nk * d * 2, lbytes = BH * Nq * 4;
+    if (cudaMemcpyAsync(dq, q, qbytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(dk, k, kvbytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(dv, v, kvbytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    st = enqueue_fwd(dq, dk, dv, do_, dlse, B, H, Nq, Nk, d, causal, scale, s);
+    if (st != ATTN_OK) return st;
+    if (cudaMemcpyAsync(o, do_, qbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(lse, dlse, lbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+const char* attn_status_string(int status) {
+    switch (status) {
+        case ATTN_OK: return "ATTN_OK";
+        case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG: invalid argument";
+        case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED: unsupported configuration";
+        case ATTN_ERR_MISALIGNED: return "ATTN_ERR_MISALIGNED: pointer not 16-byte aligned";
+        case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: CUDA call failed";
+        case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: kernel abandoned a barrier wait";
+        default: return "unknown status";
+    }
+}
+
+int attn_device_error(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+    const unsigned e = read_and_clear_prefill_error();
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    return e ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+int attn_version(void) { return kVersion; }
+
+}  // extern "C"

@@ -1,0 +1,51 @@
+// gbattn_internal.h -- declarations shared by the host API and the kernel
+// translation units of libgbattn.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/gbattn.h"
+
+namespace gbattn {
+
+// Arguments of the prefill kernel besides the three TMA descriptors.
+struct PrefillParams {
+    __nv_bfloat16* o;   // [BH, Nq, d]
+    float* lse;         // [BH, Nq]
+    int Nq, Nk, BH;
+    int num_pairs;      // query-tile pairs per head: ceil(Nq / 256)
+    int causal;
+    float scale_log2;   // scale * log2(e)
+};
+
+// Arguments of the split-K decode kernels.
+struct DecodeParams {
+    const __nv_bfloat16* q;  // [BH, d]
+    const __nv_bfloat16* k;  // [BH, Nk, d]
+    const __nv_bfloat16* v;  // [BH, Nk, d]
+    __nv_bfloat16* o;        // [BH, d]
+    float* lse;              // [BH]
+    float* part_o;           // [BH, splits, d]   (workspace)
+    float* part_lse;         // [BH, splits]      (workspace), log2 units
+    int BH, Nk, splits, keys_per_split;
+    float scale_log2;
+};
+
+// prefill_sm103.cu
+int prefill_set_attributes();
+int launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                   const PrefillParams& p, cudaStream_t stream);
+int prefill_smem_bytes(int d);
+int prefill_grid(int Nq, long long BH);
+unsigned read_and_clear_prefill_error();
+
+// decode_sm103.cu
+void decode_split_plan(long long BH, int Nk, int* splits, int* keys_per_split);
+size_t decode_workspace_bytes(long long BH, int Nk, int d);
+int launch_decode(int d, const DecodeParams& p, cudaStream_t stream);
+
+}  // namespace gbattn

@@ -1,0 +1,446 @@
+// prefill_sm103.cu -- fused attention forward (prefill) for sm_103a.
+//
+// What it computes is the FlashAttention forward of the CS336 Lecture 5
+// notes, section 8.3: for each query block Q_i, for each key/value block
+// (K_j, V_j): S_ij = Q_i K_j^T (scaled), a running row max m and row sum l,
+// P_ij = e^{S_ij - m}, l and O rescaled when m grows, O += P_ij V_j; at the
+// end O /= l and L_i = m_i + log l_i.  Key blocks wholly in the causal future
+// of a query block are skipped (same section).  The blocked softmax merge it
+// relies on is CS149 Lecture 9 notes, concept 9.
+//
+// How it maps onto a GB300 SM (one CTA per SM, 10 warps):
+//   * a CTA owns two consecutive 128-row query tiles of one (b, h) and streams
+//     the key/value tiles they share once;
+//   * warp 9 (one thread) is the TMA producer: Q0/Q1 once, then K_j and V_j
+//     tiles through a ring of shared-memory slots guarded by full/empty
+//     mbarriers with transaction counts (the double buffering of CS149
+//     Lecture 9 concept 2, deeper than two);
+//   * warp 8 (one thread) issues tcgen05.mma: S_t = Q_t K_j^T into Tensor
+//     Memory, then O_t += P_t V_j with P read from Tensor Memory;
+//   * warps 0-3 and 4-7 are the softmax warpgroups of query tiles 0 and 1: a
+//     thread owns one query row (= one TMEM lane), so row max and row sum need
+//     no shuffles; it writes P back as bf16 over its own S columns, rescales
+//     its O row in TMEM when the running max moved up by more than 2^8, and
+//     finally writes O / l and the logsumexp;
+//   * the two query tiles ping-pong: while one warpgroup runs its softmax the
+//     tensor core works on the other tile.
+// Scores use base 2: with c = scale * log2(e), p = 2^{s c - m} and
+// lse = ln2 (m + log2 l), identical in exact arithmetic to the e-based form.
+#include <cuda_bf16.h>
+#include <cuda.h>
+
+#include "gbattn_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace gbattn {
+
+__device__ unsigned int g_prefill_error = 0;
+
+namespace {
+
+constexpr int kBM = 128;            // query rows per tile (MMA M)
+constexpr int kBN = 128;            // keys per tile (MMA N of S = Q K^T)
+constexpr int kThreads = 320;       // 10 warps
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only if m grows by > 2^8
+
+template <int D>
+struct Cfg {
+    static constexpr int kSub = D / 64;                  // 128-byte swizzle atoms along d
+    static constexpr int kSubBytes = 128 * 128;          // one atom column: 128 rows x 128 B
+    static constexpr int kTileBytes = kBM * D * 2;       // a Q, K or V tile in bf16
+    static constexpr int kSlots = (D == 128) ? 4 : 8;    // K/V ring slots
+    static constexpr int kQOff = 0;
+    static constexpr int kRingOff = 2 * kTileBytes;
+    static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
+    // barriers: q, full[kSlots], empty[kSlots], s_full[2], p_ready[2], pv_done[2], final
+    static constexpr int kNumBars = 1 + 2 * kSlots + 6 + 1;
+    static constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
+    static constexpr int kAbortOff = kTmemSlotOff + 4;
+    static constexpr int kSmemBytes = kAbortOff + 4 + 1024;  // + alignment slack
+    // Tensor Memory columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 after it;
+    // P_t (bf16 pairs) overwrites the first 64 columns of S_t.
+    __device__ static uint32_t col_s(int t) { return static_cast<uint32_t>(t) * 128u; }
+    __device__ static uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(t) * D; }
+};
+
+struct Bars {
+    uint32_t q, full0, empty0, s_full0, p_ready0, pv_done0, fin;
+    int slots;
+    __device__ uint32_t full(int i) const { return full0 + 8u * i; }
+    __device__ uint32_t empty(int i) const { return empty0 + 8u * i; }
+    __device__ uint32_t s_full(int t) const { return s_full0 + 8u * t; }
+    __device__ uint32_t p_ready(int t) const { return p_ready0 + 8u * t; }
+    __device__ uint32_t pv_done(int t) const { return pv_done0 + 8u * t; }
+};
+
+__device__ __forceinline__ void flag_abort(volatile int* abort_flag) {
+    *abort_flag = 1;
+    atomicOr(&g_prefill_error, kErrTimeout);
+}
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
+                                              volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0u) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                flag_abort(abort_flag);
+                return false;
+            }
+        }
+    }
+}
+
+}  // namespace
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
+                            const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v, PrefillParams p) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle pattern
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t sQ = sbase + C::kQOff;
+    const uint32_t sRing = sbase + C::kRingOff;
+    Bars bars;
+    bars.slots = C::kSlots;
+    bars.q = sbase + C::kBarOff;
+    bars.full0 = bars.q + 8;
+    bars.empty0 = bars.full0 + 8 * C::kSlots;
+    bars.s_full0 = bars.empty0 + 8 * C::kSlots;
+    bars.p_ready0 = bars.s_full0 + 16;
+    bars.pv_done0 = bars.p_ready0 + 16;
+    bars.fin = bars.pv_done0 + 16;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kTmemSlotOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // ---- work item: a pair of query tiles of one (b, h)
+    const int L = blockIdx.x;
+    int pair, bh;
+    if (p.causal) {  // heaviest pairs (most key tiles) first
+        pair = p.num_pairs - 1 - L / p.BH;
+        bh = L % p.BH;
+    } else {  // consecutive CTAs share a head: its K/V stay in L2
+        pair = L % p.num_pairs;
+        bh = L / p.num_pairs;
+    }
+    const int row0 = pair * 2 * kBM;
+    const int n_kv_all = (p.Nk + kBN - 1) / kBN;
+    // key tiles each query tile visits (causal: up to and including its diagonal)
+    const int n_kv0 = p.causal ? min(n_kv_all, row0 / kBN + 1) : n_kv_all;
+    const int n_kv1 = p.causal ? min(n_kv_all, row0 / kBN + 2) : n_kv_all;
+    const int n_kv_max = max(n_kv0, n_kv1);
+
+    // ---- set-up: barriers (one thread), Tensor Memory (warp 0)
+    if (threadIdx.x == kLoadWarp * 32) {
+        mbar_init(bars.q, 1);
+        for (int i = 0; i < C::kSlots; ++i) {
+            mbar_init(bars.full(i), 1);
+            mbar_init(bars.empty(i), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bars.s_full(t), 1);
+            mbar_init(bars.p_ready(t), 4);  // one arrival per softmax warp
+            mbar_init(bars.pv_done(t), 1);
+        }
+        mbar_init(bars.fin, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) tmem_alloc<kTmemCols>(smem_addr(tmem_slot));
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kLoadWarp) {
+        // ================================================= TMA producer
+        int issued = 0;  // K/V tiles issued into the ring
+        if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            mbar_arrive_expect_tx(bars.q, 2 * C::kTileBytes);
+            for (int t = 0; t < 2; ++t)
+                for (int s = 0; s < C::kSub; ++s)
+                    tma_load_3d(sQ + t * C::kTileBytes + s * C::kSubBytes, &tm_q, bars.q, s * 64,
+                                row0 + t * kBM, bh);
+            bool ok = true;
+            for (int j = 0; j < n_kv_max && ok; ++j) {
+                for (int which = 0; which < 2; ++which) {
+                    const int u = 2 * j + which;
+                    const int slot = u % C::kSlots;
+                    const uint32_t ph = (u / C::kSlots) & 1;
+                    if (u >= C::kSlots && !wait_or_abort(bars.empty(slot), ph ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
+                    const CUtensorMap* tm = which ? &tm_v : &tm_k;
+                    for (int s = 0; s < C::kSub; ++s)
+                        tma_load_3d(sRing + slot * C::kTileBytes + s * C::kSubBytes, tm,
+                                    bars.full(slot), s * 64, j * kBN, bh);
+                    ++issued;
+                }
+            }
+            if (!ok) {
+                // drain: every slot's most recent copy must land before exit
+                for (int u = max(0, issued - C::kSlots); u < issued; ++u)
+                    mbar_wait(bars.full(u % C::kSlots), (u / C::kSlots) & 1);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // ================================================= MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_qk = umma_idesc_bf16(kBM, kBN, false);
+            const uint32_t idesc_pv = umma_idesc_bf16(kBM, D, true);
+            const int total_uses = 2 * n_kv_max;
+            bool ok = wait_or_abort(bars.q, 0, abort_flag);
+            tc_fence_after();
+            for (int j = 0; j < n_kv_max && ok; ++j) {
+                // ---- S_t = Q_t K_j^T
+                const int uk = 2 * j;
+                const int slot_k = uk % C::kSlots;
+                if (!wait_or_abort(bars.full(slot_k), (uk / C::kSlots) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (j >= (t ? n_kv1 : n_kv0)) continue;
+                    // P_t(j-1) lives in S_t's columns: its P V product must be done
+                    if (j > 0 && !wait_or_abort(bars.pv_done(t), (j - 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t qa = sQ + t * C::kTileBytes;
+                    const uint32_t kb = sRing + slot_k * C::kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * C::kSubBytes + (kk & 3) * 32;
+                        umma_ss(tmem + C::col_s(t), umma_desc_sw128(qa + off, 16, 1024),
+                                umma_desc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(bars.s_full(t));
+                }
+                if (!ok) break;
+                if (uk + C::kSlots < total_uses) umma_commit(bars.empty(slot_k));
+
+                // ---- O_t += P_t V_j
+                const int uv = 2 * j + 1;
+                const int slot_v = uv % C::kSlots;
+                if (!wait_or_abort(bars.full(slot_v), (uv / C::kSlots) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (j >= (t ? n_kv1 : n_kv0)) continue;
+                    if (!wait_or_abort(bars.p_ready(t), j & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t vb = sRing + slot_v * C::kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk) {
+                        // P: 16 keys = 8 packed columns; V: 16 key rows of 128 B,
+                        // the two 64-wide halves of d are kSubBytes apart (LBO)
+                        umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8,
+                                umma_desc_sw128(vb + kk * 16 * 128, C::kSubBytes, 1024), idesc_pv,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(bars.pv_done(t));
+                }
+                if (!ok) break;
+                if (uv + C::kSlots < total_uses) umma_commit(bars.empty(slot_v));
+            }
+            // every MMA this thread issued has completed once `fin` flips
+            umma_commit(bars.fin);
+            mbar_wait(bars.fin, 0);
+        }
+        __syncwarp();
+    } else {
+        // ================================================= softmax warpgroups
+        const int t = warp >> 2;          // query tile 0 or 1
+        const int wq = warp & 3;          // TMEM lane quarter
+        const int r = wq * 32 + lane;     // row within the tile
+        const int row = row0 + t * kBM + r;
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_off + C::col_s(t);
+        const uint32_t tO = tmem + lane_off + C::col_o(t);
+        const float cl2 = p.scale_log2;
+        float m_ref = -INFINITY;  // running reference max, log2 units
+        float l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < (t ? n_kv1 : n_kv0); ++j) {
+            ok = wait_or_abort(bars.s_full(t), j & 1, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            float s[kBN];
+            {
+                uint32_t raw[32];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    tmem_ld32(tS + q4 * 32, raw);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) s[q4 * 32 + c] = __uint_as_float(raw[c]);
+                }
+            }
+            const int key0 = j * kBN;
+            const bool ragged = key0 + kBN > p.Nk;
+            const bool diag = p.causal && (key0 + kBN - 1 > row0 + t * kBM);
+            if (ragged || diag) {
+                const int lim = p.causal ? min(p.Nk - 1, row) : p.Nk - 1;  // last visible key
+#pragma unroll
+                for (int c = 0; c < kBN; ++c)
+                    if (key0 + c > lim) s[c] = -INFINITY;
+            }
+            float mx = s[0];
+#pragma unroll
+            for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+            const float m_tile = mx * cl2;
+            float alpha = 1.f;
+            if (j == 0) {
+                m_ref = m_tile;
+            } else if (m_tile > m_ref + kRescaleThreshold) {
+                alpha = ex2_approx(m_ref - m_tile);
+                m_ref = m_tile;
+            }
+            l *= alpha;
+            const float mneg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+            float lsum0 = 0.f, lsum1 = 0.f;
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const float p0 = ex2_approx(fmaf(s[h * 32 + 2 * c], cl2, mneg));
+                    const float p1 = ex2_approx(fmaf(s[h * 32 + 2 * c + 1], cl2, mneg));
+                    lsum0 += p0;
+                    lsum1 += p1;
+                    pk[c] = pack_bf16x2(p0, p1);
+                }
+                tmem_st16(tS + h * 16, pk);  // P over the first 64 columns of S
+            }
+            l += lsum0 + lsum1;
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                // O_t row *= alpha.  The previous P V product is complete: S_t(j)
+                // was only issued after it finished.
+#pragma unroll 1
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + ch * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                    tmem_st32(tO + ch * 32, o);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.p_ready(t));
+        }
+        // ---- epilogue: O / l and the logsumexp
+        if (ok && (t ? n_kv1 : n_kv0) > 0) {
+            ok = wait_or_abort(bars.pv_done(t), ((t ? n_kv1 : n_kv0) - 1) & 1, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok && (t ? n_kv1 : n_kv0) > 0) {
+            tc_fence_after();
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.Nq + row) * D;
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+                uint32_t o[32];
+                tmem_ld32(tO + ch * 32, o);
+                tmem_wait_ld();
+                if (row < p.Nq) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        pk[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l,
+                                            __uint_as_float(o[2 * c + 1]) * inv_l);
+                    uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
+                                             pk[4 * v4 + 3]);
+                }
+            }
+            if (row < p.Nq)
+                p.lse[static_cast<size_t>(bh) * p.Nq + row] =
+                    (m_ref + log2f(l)) * 0.69314718055994530942f;
+        }
+    }
+
+    // ---- teardown: all Tensor Memory traffic is complete; free the columns
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc<kTmemCols>(tmem);
+}
+
+// ------------------------------------------------------------------ host side
+
+int prefill_set_attributes() {
+    if (cudaFuncSetAttribute(attn_fwd_prefill_kernel<128>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<128>::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_fwd_prefill_kernel<64>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<64>::kSmemBytes) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+template <int D>
+static int launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const PrefillParams& p, cudaStream_t stream) {
+    using C = Cfg<D>;
+    const long long grid = static_cast<long long>(p.num_pairs) * p.BH;
+    attn_fwd_prefill_kernel<D><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
+        tq, tk, tv, p);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                   const PrefillParams& p, cudaStream_t stream) {
+    return d == 128 ? launch_prefill_d<128>(tq, tk, tv, p, stream)
+                    : launch_prefill_d<64>(tq, tk, tv, p, stream);
+}
+
+int prefill_smem_bytes(int d) { return d == 128 ? Cfg<128>::kSmemBytes : Cfg<64>::kSmemBytes; }
+
+int prefill_grid(int Nq, long long BH) {
+    const long long pairs = (Nq + 2 * kBM - 1) / (2 * kBM);
+    return static_cast<int>(pairs * BH);
+}
+
+unsigned read_and_clear_prefill_error() {
+    unsigned v = 0, zero = 0;
+    cudaMemcpyFromSymbol(&v, g_prefill_error, sizeof v);
+    cudaMemcpyToSymbol(g_prefill_error, &zero, sizeof zero);
+    return v;
+}
+
+}  // namespace gbattn

@@ -1,0 +1,142 @@
+/*
+ * gbattn.h -- C ABI of the fused attention forward for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (from the lecture pages this library follows):
+ *   O = softmax(scale * Q K^T [+ causal mask]) V,   lse_i = log sum_j e^{scale q_i . k_j}
+ * "Attention(Q,K,V) = softmax(QK^T / sqrt(d_k)) V" (PDC course Lecture 4,
+ * section 4.14; CS336 Lecture 5 notes, section 8.1), evaluated block by block
+ * with the online softmax and the logsumexp L_i = m_i + log l_i kept per row
+ * (CS336 Lecture 5 notes, section 8.3).  The score matrix never reaches HBM.
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are contiguous, row-major, head dimension innermost:
+ *       q  bf16 [B, H, Nq, d]      k, v  bf16 [B, H, Nk, d]
+ *       o  bf16 [B, H, Nq, d]      lse   fp32 [B, H, Nq]  (natural log)
+ *     "bf16" is IEEE bfloat16 (1-8-7) stored in 2 bytes.
+ *   - Device pointers must be 16-byte aligned.  The caller owns every buffer;
+ *     the library allocates nothing on any call.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Compute calls
+ *     are asynchronous: GBATTN_OK means "enqueued".  Faults inside a kernel
+ *     surface at the caller's next synchronisation, as in CUDA.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     rejected call launches nothing and touches no buffer.
+ *   - Nothing is thrown across the ABI; every call returns a status code.
+ *   - Thread safety: calls may be made from several host threads; the only
+ *     shared host state is a once-initialised table of kernel attributes.
+ */
+#ifndef GBATTN_H
+#define GBATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, non-finite or
+                                  non-positive scale, too-small workspace */
+    ATTN_ERR_UNSUPPORTED = 2,  /* d not in {64, 128}; causal with Nq != Nk;
+                                  sizes beyond the index range of the kernels */
+    ATTN_ERR_MISALIGNED = 3,   /* a device pointer is not 16-byte aligned */
+    ATTN_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
+    ATTN_ERR_TIMEOUT = 5       /* a kernel gave up waiting on one of its own
+                                  pipeline barriers (reported by
+                                  attn_device_error, never by a launch) */
+} attn_status_t;
+
+/*
+ * attn_fwd -- prefill / full attention forward.
+ *
+ * Computes, for every (b, h) and query row i < Nq:
+ *   s_ij   = scale * sum_c q[b,h,i,c] k[b,h,j,c]            for j < Nk
+ *   s_ij   = -inf if causal and j > i                      (key j masked for j > i)
+ *   o[b,h,i,:] = sum_j softmax_j(s_i.) v[b,h,j,:]          (bf16, round-to-nearest-even)
+ *   lse[b,h,i] = log sum_j e^{s_ij}                          (fp32, natural log)
+ * FlashAttention forward with the online softmax (CS336 Lecture 5 notes,
+ * sections 8.2-8.3; CS149 Lecture 9 notes, concept 9); causal key blocks
+ * wholly in the future of a query block are skipped.
+ *
+ *   q, k, v  device, bf16, layouts above; read only.
+ *   o        device, bf16 [B,H,Nq,d]; written.
+ *   lse      device, fp32 [B,H,Nq]; written.  May not be NULL.
+ *   B, H, Nq, Nk >= 1;  d in {64, 128};  causal in {0, 1} (causal needs Nq == Nk).
+ *   scale    > 0 and finite; the usual value is 1/sqrt(d).
+ *   stream   cudaStream_t.
+ * Internal arithmetic: fp32 scores and accumulators on the tensor cores,
+ * probabilities rounded to bf16 before the P V product, fp32 row sums.
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED,
+ * ATTN_ERR_MISALIGNED or ATTN_ERR_CUDA.
+ */
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+             int B, int H, int Nq, int Nk, int d, int causal, float scale, void *stream);
+
+/*
+ * attn_fwd_decode_workspace_bytes -- bytes of device workspace attn_fwd_decode
+ * needs for these sizes (0 when a single split covers every key).  Pure host
+ * arithmetic; never touches the GPU.  Returns 0 for invalid sizes as well.
+ */
+size_t attn_fwd_decode_workspace_bytes(int B, int H, int Nk, int d);
+
+/*
+ * attn_fwd_decode -- single-query (Nq = 1) attention forward, split over keys.
+ *
+ * Same result as attn_fwd with Nq = 1, causal = 0.  Decode is memory-bound
+ * (CS336 Lecture 5 notes, section 5.3: arithmetic intensity about 1 FLOP per
+ * byte), so the keys of each (b, h) are cut into splits that stream K and V
+ * once with 16-byte coalesced loads; each split keeps its own running max and
+ * sum and writes a partial (o_s, lse_s) to the workspace; a second kernel
+ * merges the splits with the two-block rule m = max(m1, m2),
+ * l = e^{m1-m} l1 + e^{m2-m} l2 (CS149 Lecture 9 notes, concept 9).
+ *
+ *   q        device bf16 [B,H,1,d];  k, v device bf16 [B,H,Nk,d].
+ *   o        device bf16 [B,H,1,d];  lse device fp32 [B,H,1].
+ *   workspace  device scratch of at least attn_fwd_decode_workspace_bytes()
+ *              bytes, 16-byte aligned (NULL allowed when that is 0).  Its
+ *              contents on entry do not matter; it is overwritten.  Two calls
+ *              in flight at once must not share a workspace.
+ * Returns as attn_fwd; a too-small workspace is ATTN_ERR_INVALID_ARG.
+ */
+int attn_fwd_decode(const void *q, const void *k, const void *v, void *o, float *lse,
+                    int B, int H, int Nk, int d, float scale,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * attn_fwd_from_host -- attn_fwd on HOST buffers, end to end.
+ *
+ * Enqueues on `stream`: host->device copies of q, k, v into the caller's
+ * device buffers dq, dk, dv; attn_fwd on them into do_, dlse; device->host
+ * copies of the results into o and lse.  The host buffers should be pinned
+ * (page-locked) for the copies to be asynchronous.  The call returns once
+ * everything is enqueued; the caller synchronises the stream before reading
+ * o and lse.  Same arguments, sizes and status codes as attn_fwd; every
+ * pointer must be non-NULL and the device ones 16-byte aligned.
+ */
+int attn_fwd_from_host(const void *q, const void *k, const void *v, void *o, float *lse,
+                       void *dq, void *dk, void *dv, void *do_, float *dlse,
+                       int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                       void *stream);
+
+/* attn_status_string -- a static, human-readable name for a status code. */
+const char *attn_status_string(int status);
+
+/*
+ * attn_device_error -- synchronises the current device, then reads and
+ * clears the library's device-side error word.  Returns ATTN_OK when no
+ * kernel reported a problem since the last call, ATTN_ERR_TIMEOUT when a
+ * kernel abandoned a bounded wait on one of its own barriers (it then wrote
+ * no valid output), or ATTN_ERR_CUDA if the synchronisation failed.
+ */
+int attn_device_error(void);
+
+/* attn_version -- library version as major*10000 + minor*100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBATTN_H */

@@ -1,0 +1,108 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point the
+header declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_flashattention_fwd_gb300 import binding, build_lib
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "gbattn.h")
+OK, INVALID, UNSUPPORTED, MISALIGNED = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[a-z_ ]+[ *]+\**(attn_[a-z0-9_]+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("attn_fwd", "attn_fwd_decode", "attn_fwd_decode_workspace_bytes",
+              "attn_fwd_from_host", "attn_status_string", "attn_device_error", "attn_version"):
+        assert n in names, names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libgbattn.so does not export {name}"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.attn_version() >= 100
+    for st in range(6):
+        assert binding.status_string(st).startswith("ATTN_")
+    assert binding.status_string(99) == "unknown status"
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
+
+
+def fwd(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=1, Nq=128, Nk=128, d=64,
+        causal=0, scale=0.125):
+    P = ctypes.c_void_p
+    return lib.attn_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, Nq, Nk, d, causal, scale, P(0))
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=0), INVALID), (dict(k=0), INVALID), (dict(v=0), INVALID), (dict(o=0), INVALID),
+    (dict(lse=0), INVALID), (dict(B=0), INVALID), (dict(H=-1), INVALID), (dict(Nq=0), INVALID),
+    (dict(Nk=0), INVALID), (dict(scale=float("nan")), INVALID), (dict(scale=float("inf")), INVALID),
+    (dict(scale=0.0), INVALID), (dict(scale=-1.0), INVALID), (dict(causal=2), INVALID),
+    (dict(d=96), UNSUPPORTED), (dict(d=256), UNSUPPORTED), (dict(d=0), UNSUPPORTED),
+    (dict(causal=1, Nq=128, Nk=256), UNSUPPORTED),
+    (dict(B=1 << 20, H=1 << 12), UNSUPPORTED),
+    (dict(q=FAKE + 8), MISALIGNED), (dict(o=FAKE + 2), MISALIGNED), (dict(lse=FAKE + 4), MISALIGNED),
+])
+def test_attn_fwd_rejects_before_launch(lib, kw, expect):
+    assert fwd(lib, **kw) == expect
+
+
+def test_decode_workspace_bytes_is_host_arithmetic(lib):
+    # 2048 heads of 8192 keys: two splits, d + 1 floats per (head, split)
+    assert lib.attn_fwd_decode_workspace_bytes(64, 32, 8192, 128) == 2048 * 2 * (128 + 1) * 4
+    # few heads: more splits, at least 512 keys each
+    assert lib.attn_fwd_decode_workspace_bytes(1, 1, 8192, 128) == 16 * (128 + 1) * 4
+    # a single split needs no workspace
+    assert lib.attn_fwd_decode_workspace_bytes(64, 32, 300, 64) == 0
+    assert lib.attn_fwd_decode_workspace_bytes(1, 1, 0, 64) == 0
+    assert lib.attn_fwd_decode_workspace_bytes(1, 1, 100, 96) == 0
+
+
+def test_decode_rejects_before_launch(lib):
+    P = ctypes.c_void_p
+    need = lib.attn_fwd_decode_workspace_bytes(1, 1, 8192, 128)
+
+    def dec(q=FAKE, ws=FAKE, ws_bytes=need, d=128, scale=0.1, Nk=8192):
+        return lib.attn_fwd_decode(P(q), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1, 1, Nk, d, scale,
+                                   P(ws), ws_bytes, P(0))
+
+    assert dec(q=0) == INVALID
+    assert dec(ws=0) == INVALID
+    assert dec(ws_bytes=need - 1) == INVALID
+    assert dec(scale=-1.0) == INVALID
+    assert dec(d=80) == UNSUPPORTED
+    assert dec(Nk=0) == INVALID
+    assert dec(q=FAKE + 8) == MISALIGNED
+    assert dec(ws=FAKE + 4) == MISALIGNED
+
+
+def test_from_host_rejects_before_launch(lib):
+    P = ctypes.c_void_p
+    args = [P(FAKE)] * 10
+    args[7] = P(0)  # dv missing
+    assert lib.attn_fwd_from_host(*args, 1, 1, 128, 128, 64, 0, 0.125, P(0)) == INVALID
+    args = [P(FAKE)] * 10
+    args[6] = P(FAKE + 8)  # dk misaligned
+    assert lib.attn_fwd_from_host(*args, 1, 1, 128, 128, 64, 0, 0.125, P(0)) == MISALIGNED
+    args = [P(FAKE)] * 10
+    assert lib.attn_fwd_from_host(*args, 1, 1, 128, 128, 72, 0, 0.125, P(0)) == UNSUPPORTED

@@ -1,0 +1,288 @@
+"""The CUDA path against the fp64 oracle, element by element, through the C ABI.
+
+Tolerances are the ones the study states for bf16 inputs and outputs:
+O within 2e-2 max-abs and 1e-3 mean-abs of the fp64 result, lse within 2e-3.
+Inputs come from the seeded generator; large workloads are checked on sampled
+rows (rows are independent, so a sampled row is checked exactly).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_flashattention_fwd_gb300 import binding
+from attention_flashattention_fwd_gb300.inputs import WORKLOADS, bf16_bits, make_qkv, make_workload
+
+O_MAX, O_MEAN, LSE_MAX = 2e-2, 1e-3, 2e-3
+
+pytestmark = pytest.mark.gpu
+
+
+def _dev():
+    return torch.device("cuda:0")
+
+
+def _assert_close(o, lse, ro, rl, what=""):
+    o = np.asarray(o, dtype=np.float64)
+    lse = np.asarray(lse, dtype=np.float64)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse)), f"{what}: non-finite output"
+    e = np.abs(o - ro)
+    el = np.abs(lse - rl)
+    msg = f"{what}: O max {e.max():.3g} mean {e.mean():.3g}, lse max {el.max():.3g}"
+    assert e.max() <= O_MAX and e.mean() <= O_MEAN and el.max() <= LSE_MAX, msg
+    return e.max(), e.mean(), el.max()
+
+
+def _full_check(q, k, v, causal, scale=None, what=""):
+    o, lse = binding.attn_fwd(q, k, v, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), causal=causal,
+                              scale=scale)
+    return _assert_close(o.float().cpu().numpy(), lse.cpu().numpy(), ro, rl, what)
+
+
+# --------------------------------------------------------------- prefill shapes
+
+PREFILL_SHAPES = [
+    # B, H, Nq, Nk, d, causal
+    (1, 1, 128, 128, 64, False),    # the tiny workload's shape
+    (1, 2, 256, 256, 64, False),
+    (1, 2, 256, 256, 128, False),
+    (2, 2, 384, 384, 128, True),
+    (1, 2, 300, 300, 64, True),     # ragged last tile
+    (1, 1, 77, 77, 128, True),      # less than one tile
+    (1, 1, 77, 77, 64, False),
+    (1, 3, 200, 513, 128, False),   # Nq != Nk, ragged keys
+    (1, 1, 128, 50, 64, False),     # fewer keys than a tile
+    (1, 1, 5, 3, 128, False),
+    (1, 1, 1, 1, 64, False),        # one query, one key
+    (1, 1, 1, 700, 128, False),     # a single query row through the prefill kernel
+    (1, 1, 1000, 1000, 128, True),  # many tiles, ragged, causal
+    (2, 1, 640, 640, 64, True),
+    (1, 1, 1280, 1280, 128, False),
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,causal", PREFILL_SHAPES,
+                         ids=[f"b{B}h{H}q{Nq}k{Nk}d{d}{'c' if c else ''}"
+                              for B, H, Nq, Nk, d, c in PREFILL_SHAPES])
+def test_prefill_matches_oracle(B, H, Nq, Nk, d, causal):
+    q, k, v = make_qkv(B, H, Nq, Nk, d, seed=11 + Nq + Nk + d, device=_dev())
+    _full_check(q, k, v, causal, what=f"{(B, H, Nq, Nk, d, causal)}")
+
+
+def test_prefill_scale_argument():
+    q, k, v = make_qkv(1, 2, 256, 256, 128, seed=21, device=_dev())
+    _full_check(q, k, v, True, scale=0.3, what="scale=0.3")
+    _full_check(q, k, v, False, scale=0.02, what="scale=0.02")
+
+
+def test_prefill_wide_logits():
+    # sigma 3 logits: large row maxima, many rescales of the running max
+    q, k, v = make_qkv(1, 2, 512, 512, 128, seed=22, device=_dev(), sigma_qk=1.7)
+    _full_check(q, k, v, True, what="wide logits causal")
+    _full_check(q, k, v, False, what="wide logits")
+
+
+def test_tiny_workload():
+    w = WORKLOADS["tiny_b1h1n128d64"]
+    q, k, v = make_workload(w, device=_dev())
+    _full_check(q, k, v, w.causal, scale=w.scale, what=w.name)
+
+
+def test_b4h8n1024d64_workload_all_rows():
+    w = WORKLOADS["b4h8n1024d64"]
+    q, k, v = make_workload(w, device=_dev())
+    _full_check(q, k, v, w.causal, scale=w.scale, what=w.name)
+
+
+def _sampled_rows(w, rng, full_heads, n_random, extra_rows):
+    BH = w.B * w.H
+    rows = []
+    for bh in full_heads:
+        rows += [(bh, i) for i in range(w.Nq)]
+    for i in extra_rows:
+        rows.append((rng.integers(BH), i))
+    rows += [(rng.integers(BH), rng.integers(w.Nq)) for _ in range(n_random)]
+    return np.array(rows, dtype=np.int64)
+
+
+def _rows_check(w, full_heads, n_random, extra_rows):
+    q, k, v = make_workload(w, device=_dev())
+    o, lse = binding.attn_fwd(q, k, v, causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(1234)
+    rows = _sampled_rows(w, rng, full_heads, n_random, extra_rows)
+    ro, rl = oracle.attention_rows(bf16_bits(q), bf16_bits(k), bf16_bits(v), rows,
+                                   causal=w.causal, scale=w.scale)
+    BH = w.B * w.H
+    idx = torch.as_tensor(rows[:, 0] * w.Nq + rows[:, 1], device=o.device)
+    og = o.reshape(BH * w.Nq, w.d).index_select(0, idx).float().cpu().numpy()
+    lg = lse.reshape(BH * w.Nq).index_select(0, idx).cpu().numpy()
+    return _assert_close(og, lg, ro, rl, w.name)
+
+
+def test_b2h16n4096d128_causal_sampled():
+    w = WORKLOADS["b2h16n4096d128_causal"]
+    _rows_check(w, full_heads=[0, w.B * w.H - 1], n_random=256,
+                extra_rows=[0, 127, 128, 255, 256, 4095])
+
+
+def test_b1h32n16384d128_causal_sampled():
+    w = WORKLOADS["b1h32n16384d128_causal"]
+    _rows_check(w, full_heads=[], n_random=384,
+                extra_rows=[0, 1, 127, 128, 255, 256, 8191, 8192, 16383] + list(range(0, 512, 7)))
+
+
+# ---------------------------------------------------------------- decode
+
+DECODE_SHAPES = [
+    # B, H, Nk, d
+    (1, 1, 1, 64),
+    (1, 1, 511, 128),
+    (1, 1, 513, 128),
+    (2, 3, 3000, 64),
+    (2, 4, 8192, 128),
+    (1, 1, 20000, 128),
+    (3, 5, 777, 64),
+    (16, 32, 1024, 128),
+]
+
+
+@pytest.mark.parametrize("B,H,Nk,d", DECODE_SHAPES,
+                         ids=[f"b{B}h{H}k{Nk}d{d}" for B, H, Nk, d in DECODE_SHAPES])
+def test_decode_matches_oracle(B, H, Nk, d):
+    q, k, v = make_qkv(B, H, 1, Nk, d, seed=31 + Nk + d, device=_dev())
+    o, lse = binding.attn_fwd_decode(q, k, v)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v))
+    _assert_close(o.float().cpu().numpy(), lse.cpu().numpy(), ro, rl, f"decode {B, H, Nk, d}")
+
+
+def test_decode_workload_sampled_heads():
+    w = WORKLOADS["decode_b64h32nk8192d128"]
+    q, k, v = make_workload(w, device=_dev())
+    need = binding.decode_workspace_bytes(w.B, w.H, w.Nk, w.d)
+    ws = torch.empty(need, dtype=torch.uint8, device=_dev())
+    o, lse = binding.attn_fwd_decode(q, k, v, scale=w.scale, workspace=ws)
+    torch.cuda.synchronize()
+    BH = w.B * w.H
+    sel = np.sort(np.random.default_rng(99).choice(BH, 256, replace=False))
+    sel[0], sel[-1] = 0, BH - 1
+    idx = torch.as_tensor(sel, device=_dev())
+    qs = q.reshape(BH, 1, 1, w.d).index_select(0, idx).reshape(1, len(sel), 1, w.d)
+    ks = k.reshape(BH, w.Nk, w.d).index_select(0, idx).reshape(1, len(sel), w.Nk, w.d)
+    vs = v.reshape(BH, w.Nk, w.d).index_select(0, idx).reshape(1, len(sel), w.Nk, w.d)
+    ro, rl = oracle.attention(bf16_bits(qs), bf16_bits(ks), bf16_bits(vs), scale=w.scale)
+    og = o.reshape(BH, w.d).index_select(0, idx).float().cpu().numpy().reshape(ro.shape)
+    lg = lse.reshape(BH).index_select(0, idx).cpu().numpy().reshape(rl.shape)
+    _assert_close(og, lg, ro, rl, w.name)
+
+
+def test_decode_equals_prefill_path():
+    q, k, v = make_qkv(2, 4, 1, 2500, 128, seed=41, device=_dev())
+    o1, l1 = binding.attn_fwd_decode(q, k, v)
+    o2, l2 = binding.attn_fwd(q, k, v)
+    torch.cuda.synchronize()
+    assert (o1.float() - o2.float()).abs().max().item() <= O_MAX
+    assert (l1 - l2).abs().max().item() <= LSE_MAX
+
+
+def test_decode_rejects_small_workspace():
+    q, k, v = make_qkv(1, 1, 1, 8192, 128, seed=42, device=_dev())
+    need = binding.decode_workspace_bytes(1, 1, 8192, 128)
+    assert need > 0
+    ws = torch.empty(need - 16, dtype=torch.uint8, device=_dev())
+    with pytest.raises(binding.GbattnError) as ei:
+        binding.attn_fwd_decode(q, k, v, workspace=ws)
+    assert ei.value.status == 1
+
+
+# ------------------------------------------------- invariants through the kernels
+
+def test_q_zero_gives_mean_of_visible_values():
+    B, H, N, d = 1, 2, 300, 128
+    _, k, v = make_qkv(B, H, N, N, d, seed=51, device=_dev())
+    q = torch.zeros((B, H, N, d), dtype=torch.bfloat16, device=_dev())
+    vd = v.double().cpu()
+    o, lse = binding.attn_fwd(q, k, v, causal=False)
+    torch.cuda.synchronize()
+    assert (o.double().cpu() - vd.mean(dim=2, keepdim=True)).abs().max().item() <= O_MAX
+    assert (lse.double().cpu() - math.log(N)).abs().max().item() <= LSE_MAX
+    o, lse = binding.attn_fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    prefix = vd.cumsum(dim=2) / torch.arange(1, N + 1, dtype=torch.float64)[None, None, :, None]
+    assert (o.double().cpu() - prefix).abs().max().item() <= O_MAX
+    ln = torch.log(torch.arange(1, N + 1, dtype=torch.float64))[None, None]
+    assert (lse.double().cpu() - ln).abs().max().item() <= LSE_MAX
+    # decode: the column mean of V
+    od, ld = binding.attn_fwd_decode(q[:, :, :1].contiguous(), k, v)
+    torch.cuda.synchronize()
+    assert (od.double().cpu() - vd.mean(dim=2, keepdim=True)).abs().max().item() <= O_MAX
+    assert (ld.double().cpu() - math.log(N)).abs().max().item() <= LSE_MAX
+
+
+def test_causal_row0_is_v0():
+    q, k, v = make_qkv(2, 3, 256, 256, 64, seed=52, device=_dev())
+    o, lse = binding.attn_fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o[:, :, 0], v[:, :, 0])
+    ref = (q[:, :, 0].double() * k[:, :, 0].double()).sum(-1) / 8.0
+    assert (lse[:, :, 0].double() - ref).abs().max().item() <= LSE_MAX
+
+
+def test_dominant_logit_selects_its_value_row():
+    B, H, N, d = 1, 2, 384, 128
+    q, k, v = make_qkv(B, H, N, N, d, seed=53, device=_dev())
+    q = (q.float() * 0.05).to(torch.bfloat16)
+    k = (k.float() * 0.05).to(torch.bfloat16)
+    jstar, i = 200, 300
+    qi = q[:, :, i].double()
+    k[:, :, jstar] = (60.0 * qi / (qi * qi).sum(-1, keepdim=True)).to(torch.bfloat16)
+    o, lse = binding.attn_fwd(q, k, v, causal=False, scale=1.0)
+    torch.cuda.synchronize()
+    assert (o[:, :, i].float() - v[:, :, jstar].float()).abs().max().item() <= O_MAX
+    logit = (q[:, :, i].double() * k[:, :, jstar].double()).sum(-1)
+    assert (lse[:, :, i].double() - logit).abs().max().item() <= 5e-2
+
+
+def test_value_affine_map():
+    q, k, v = make_qkv(1, 2, 256, 256, 128, seed=54, device=_dev())
+    v2 = (v.float() * 0.5 + 0.25).to(torch.bfloat16)  # exact in bf16 for |v| < 2^7
+    o1, l1 = binding.attn_fwd(q, k, v, causal=True)
+    o2, l2 = binding.attn_fwd(q, k, v2, causal=True)
+    torch.cuda.synchronize()
+    assert (o2.float() - (o1.float() * 0.5 + 0.25)).abs().max().item() <= O_MAX
+    assert torch.equal(l1, l2)
+
+
+def test_deterministic_and_stream_aware():
+    q, k, v = make_qkv(2, 4, 640, 640, 128, seed=55, device=_dev())
+    o1, l1 = binding.attn_fwd(q, k, v, causal=True)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o2, l2 = binding.attn_fwd(q, k, v, causal=True, stream=s)
+    s.synchronize()
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_from_host_end_to_end():
+    B, H, N, d = 1, 4, 512, 128
+    q, k, v = make_qkv(B, H, N, N, d, seed=56, device="cpu")
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    oh = torch.empty((B, H, N, d), dtype=torch.bfloat16).pin_memory()
+    lh = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    dq, dk, dv = (torch.empty_like(t, device=_dev()) for t in (q, k, v))
+    do_ = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=_dev())
+    dl = torch.empty((B, H, N), dtype=torch.float32, device=_dev())
+    binding.attn_fwd_from_host(qh, kh, vh, oh, lh, dq, dk, dv, do_, dl, causal=True)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), causal=True)
+    _assert_close(oh.float().numpy(), lh.numpy(), ro, rl, "from_host")
+
+
+def test_no_device_error_reported():
+    assert binding.device_error() == 0
