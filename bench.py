@@ -1,0 +1,490 @@
+#!/usr/bin/env python
+"""Benchmark of the fused attention forward on GB300.
+
+One step is one pass of the whole hot path over one batch of synthetic
+input: the prefill kernel on the causal B=2, H=16, N=4096, d=128 workload
+(the headline: attention fwd TFLOP/s against the bf16 tensor peak), the
+prefill kernel on the causal B=1, H=32, N=16384, d=128 long-sequence workload,
+and the split-K decode (split kernel + combine kernel) on the
+B=64, H=32, Nk=8192, d=128 decode workload (HBM GB/s).  L2 is flushed (256 MiB
+write) before every step.  Each kernel is timed with CUDA events on the
+stream it is launched on.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+N > 1 runs N independent replicas (one per GPU, launched by torchrun): the
+path has no exchange step.  ``--impl reference`` times the fp64 CPU oracle on
+the host cores instead, on bounded samples of the same workload.
+Prints one JSON line (rank 0).
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s & % of BF16 tensor peak; decode-shape HBM GB/s"
+HEADLINE = "b2h16n4096d128_causal"
+LONG = "b1h32n16384d128_causal"
+DECODE = "decode_b64h32nk8192d128"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+CPU_SAMPLE_SECONDS = 10.0
+BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gbattn", "reference"], default="gbattn")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the oracle timing (for quick runs)")
+    ap.add_argument("--case", default=None,
+                    help="run only this workload's kernel(s) (profiling runs); prints its time")
+    a = ap.parse_args()
+    a.warmup = max(3, a.warmup)
+    a.steps = max(1, a.steps)
+    return a
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _sources_sha(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "attention_flashattention_fwd_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+PREFILL_SOURCES = ["prefill_sm103.cu", "sm103_ptx.cuh"]
+DECODE_SOURCES = ["decode_sm103.cu", "sm103_ptx.cuh"]
+
+
+def profiled_traffic(profile_name, sources):
+    """DRAM bytes per launch recorded in profiles/<profile_name>.md by an ncu
+    capture, or None when the kernel sources changed since the capture."""
+    path = os.path.join(ROOT, "profiles", profile_name + ".md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    s = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != _sources_sha(sources):
+        return None
+    return int(m.group(1))
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the GPU is timed."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax = float(f[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": [], "samples": 0}
+        loaded = [x for x in sm if smax is None or x > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- distribution
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(values, world, device=None):
+    """Element-wise maximum of a list of floats over all ranks (the slowest
+    replica sets the time)."""
+    if world <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.cpu().tolist()
+
+
+# ------------------------------------------------------------------ oracle
+
+def oracle_rows_tflops(w, q, k, v, rows):
+    """Run the fp64 oracle on `rows` of workload `w`; returns (TFLOP/s, seconds,
+    FLOPs, o, lse).  FLOPs per row = 4 d (visible keys), the same count the
+    GPU metric uses (4 B H Nq Nk d, halved for causal)."""
+    import numpy as np
+
+    import oracle
+    visible = (rows[:, 1] + 1) if w.causal else np.full(len(rows), w.Nk)
+    flops = float(4 * w.d * visible.sum())
+    t0 = time.perf_counter()
+    o, lse = oracle.attention_rows(q, k, v, rows, causal=w.causal, scale=w.scale)
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, dt, flops, o, lse
+
+
+def head_rows(w, bh, stride=1, offset=0):
+    import numpy as np
+    i = np.arange(offset, w.Nq, stride, dtype=np.int64)
+    return np.stack([np.full_like(i, bh), i], axis=1)
+
+
+def cpu_baseline_leg(w, q_bits, k_bits, v_bits, o_gpu=None, lse_gpu=None):
+    """Time the oracle, as it stands, on whole heads of the headline workload
+    until about CPU_SAMPLE_SECONDS have passed."""
+    import numpy as np
+
+    import oracle
+    BH = w.B * w.H
+    tot_flops, tot_s, heads = 0.0, 0.0, 0
+    worst_o, worst_l = 0.0, 0.0
+    order = np.random.default_rng(2024).permutation(BH)
+    for bh in order:
+        rows = head_rows(w, int(bh))
+        _, dt, fl, o, lse = oracle_rows_tflops(w, q_bits, k_bits, v_bits, rows)
+        tot_flops += fl
+        tot_s += dt
+        heads += 1
+        if o_gpu is not None:
+            og = o_gpu[int(bh)].astype(np.float64)
+            worst_o = max(worst_o, float(np.abs(og - o).max()))
+            worst_l = max(worst_l, float(np.abs(lse_gpu[int(bh)] - lse).max()))
+        if tot_s >= CPU_SAMPLE_SECONDS:
+            break
+    out = {"value": tot_flops / tot_s / 1e12, "unit": "TFLOP/s", "cores": oracle.threads_used(),
+           "kind": "oracle",
+           "sample": f"{heads} of {BH} (b,h) heads of {w.name}, all {w.Nq} query rows each "
+                     f"({tot_flops / 1e9:.1f} GFLOP in {tot_s:.1f} s, fp64 naive, OpenMP over rows)"}
+    if o_gpu is not None:
+        out["gpu_vs_oracle_on_sample"] = {"o_max_abs": worst_o, "lse_max_abs": worst_l}
+    return out
+
+
+# ------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    # rank 0 alone times the oracle; the other ranks exit at once without work
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    import torch  # noqa: F401
+
+    import oracle
+    from attention_flashattention_fwd_gb300.inputs import WORKLOADS, bf16_bits, make_workload
+    w = WORKLOADS[HEADLINE]
+    q, k, v = make_workload(w, device="cpu")
+    qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
+    BH = w.B * w.H
+    stride = 8  # a step = every 8th query row of one head (512 rows, ~0.5 GFLOP)
+    times, flops = [], []
+    for s in range(args.warmup + args.steps):
+        rows = head_rows(w, s % BH, stride=stride, offset=s % stride)
+        _, dt, fl, _, _ = oracle_rows_tflops(w, qb, kb, vb, rows)
+        if s >= args.warmup:
+            times.append(dt)
+            flops.append(fl)
+    value = sum(flops) / sum(times) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                   "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads_used(),
+                         "kind": "oracle",
+                         "sample": f"each step: every {stride}th query row of one (b,h) head of "
+                                   f"{w.name} (fp64 naive)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_case(args):
+    """One workload alone: W warm-up launches then K timed launches (used to
+    profile a single kernel with ncu)."""
+    import torch
+
+    from attention_flashattention_fwd_gb300 import binding
+    from attention_flashattention_fwd_gb300.inputs import WORKLOADS, make_workload
+    w = WORKLOADS[args.case]
+    binding.load()
+    dev = torch.device("cuda", 0)
+    q, k, v = make_workload(w, device=dev)
+    o, lse = torch.empty_like(q), torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    ws = None
+    if w.decode:
+        ws = torch.empty(max(1, binding.decode_workspace_bytes(w.B, w.H, w.Nk, w.d)),
+                         dtype=torch.uint8, device=dev)
+
+    def launch():
+        if w.decode:
+            binding.attn_fwd_decode(q, k, v, scale=w.scale, out=o, lse=lse, workspace=ws)
+        else:
+            binding.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)
+
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        launch()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    if binding.device_error() != 0:
+        raise RuntimeError("a kernel reported a device-side error")
+    val = (w.algorithmic_bytes() / ms / 1e6, "GB/s") if w.decode else (w.flops() / ms / 1e9,
+                                                                         "TFLOP/s")
+    print(json.dumps({"case": w.name, "ms_per_launch": ms, "value": val[0], "unit": val[1],
+                      "steps": args.steps, "warmup": args.warmup, "l2": "not flushed"}))
+
+
+def run_gpu(args):
+    rank, world, local = dist_init()
+    import numpy as np
+    import torch
+
+    from attention_flashattention_fwd_gb300 import binding
+    from attention_flashattention_fwd_gb300.inputs import WORKLOADS, bf16_bits, make_workload
+
+    binding.load()  # raises if the CUDA library is missing: no fallback
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+
+    w3, w4, w5 = WORKLOADS[HEADLINE], WORKLOADS[LONG], WORKLOADS[DECODE]
+    q3, k3, v3 = make_workload(w3, device=dev)
+    q4, k4, v4 = make_workload(w4, device=dev)
+    q5, k5, v5 = make_workload(w5, device=dev)
+    o3, l3 = torch.empty_like(q3), torch.empty(q3.shape[:3], dtype=torch.float32, device=dev)
+    o4, l4 = torch.empty_like(q4), torch.empty(q4.shape[:3], dtype=torch.float32, device=dev)
+    o5, l5 = torch.empty_like(q5), torch.empty(q5.shape[:3], dtype=torch.float32, device=dev)
+    ws5 = torch.empty(max(1, binding.decode_workspace_bytes(w5.B, w5.H, w5.Nk, w5.d)),
+                      dtype=torch.uint8, device=dev)
+    splits = binding.decode_workspace_bytes(w5.B, w5.H, w5.Nk, w5.d) > 0
+    launches_per_step = 1 + 1 + (2 if splits else 1)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev):
+        flush.zero_()
+        ev[0].record(stream)
+        binding.attn_fwd(q3, k3, v3, causal=True, scale=w3.scale, out=o3, lse=l3, stream=stream)
+        ev[1].record(stream)
+        binding.attn_fwd(q4, k4, v4, causal=True, scale=w4.scale, out=o4, lse=l4, stream=stream)
+        ev[2].record(stream)
+        binding.attn_fwd_decode(q5, k5, v5, scale=w5.scale, out=o5, lse=l5, workspace=ws5,
+                                stream=stream)
+        ev[3].record(stream)
+
+    def mk():
+        return [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+
+    for _ in range(args.warmup):
+        step(mk())
+    torch.cuda.synchronize()
+
+    def timed_region():
+        evs = [mk() for _ in range(args.steps)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+        barrier(world)
+        torch.cuda.synchronize()
+        sampler.start()
+        t0.record(stream)
+        for ev in evs:
+            step(ev)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        sampler.stop()
+        barrier(world)
+        ms = [0.0, 0.0, 0.0]
+        for ev in evs:
+            for i in range(3):
+                ms[i] += ev[i].elapsed_time(ev[i + 1])
+        return ms, t0.elapsed_time(t1), sampler.summary()
+
+    ms, total_ms, clocks = timed_region()
+    if any(r in clocks["reasons"] for r in BAD_REASONS):
+        ms, total_ms, clocks = timed_region()  # re-measure once
+        clocks["remeasured"] = True
+    if binding.device_error() != 0:
+        raise RuntimeError("a kernel reported a device-side error during the benchmark")
+    ms3, ms4, ms5, total_ms = max_over_ranks(ms + [total_ms], world, device=dev)
+    K = args.steps
+
+    def prefill_part(w, ms_sum, sources, prof):
+        per_launch = ms_sum / K
+        tflops = world * K * w.flops() / (ms_sum * 1e-3) / 1e12
+        achieved = w.flops() / (per_launch * 1e-3) / 1e12
+        return {
+            "workload": w.name, "value": tflops, "unit": "TFLOP/s", "ms_per_launch": per_launch,
+            "frac_of_2250": achieved / 2250.0,
+            "roofline": {"bound": "tensor", "achieved": achieved,
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": achieved / peaks["bf16_tflops"],
+                         "traffic": profiled_traffic(prof, sources),
+                         "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)"},
+        }
+
+    p3 = prefill_part(w3, ms3, PREFILL_SOURCES, "ncu_prefill_" + HEADLINE)
+    p4 = prefill_part(w4, ms4, PREFILL_SOURCES, "ncu_prefill_" + LONG)
+    per5 = ms5 / K
+    gbs = w5.algorithmic_bytes() / (per5 * 1e-3) / 1e9
+    p5 = {"workload": w5.name, "value": world * gbs, "unit": "GB/s", "ms_per_call": per5,
+          "frac_of_8000": gbs / 8000.0,
+          "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                       "frac": gbs / peaks["hbm_gbs"],
+                       "traffic": profiled_traffic("ncu_decode_" + DECODE, DECODE_SOURCES),
+                       "peak_source": f"{peak_src} HBM copy (MEASURED_PEAKS.json)"}}
+
+    # ---- end to end through the C ABI with host buffers (headline workload)
+    qh, kh, vh = (t.cpu().pin_memory() for t in (q3, k3, v3))
+    oh = torch.empty(q3.shape, dtype=torch.bfloat16).pin_memory()
+    lh = torch.empty(q3.shape[:3], dtype=torch.float32).pin_memory()
+    e2e_steps = min(K, 20)
+    for _ in range(3):
+        binding.attn_fwd_from_host(qh, kh, vh, oh, lh, q3, k3, v3, o3, l3, causal=True,
+                                   scale=w3.scale, stream=stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        binding.attn_fwd_from_host(qh, kh, vh, oh, lh, q3, k3, v3, o3, l3, causal=True,
+                                   scale=w3.scale, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    (e2e_ms,) = max_over_ranks([e0.elapsed_time(e1)], world, device=dev)
+    e2e = {"value": world * e2e_steps * w3.flops() / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": int(qh.nbytes + kh.nbytes + vh.nbytes),
+           "d2h_bytes_per_step": int(oh.nbytes + lh.nbytes),
+           "ms_per_step": e2e_ms / e2e_steps,
+           "path": "attn_fwd_from_host (pinned host q,k,v -> device -> kernel -> host o,lse)"}
+
+    line = {
+        "metric": METRIC, "value": p3["value"], "unit": "TFLOP/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": total_ms / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded iid Gaussian Q,K,V rounded to bf16)",
+        "config": {"workload": HEADLINE, "B": w3.B, "H": w3.H, "Nq": w3.Nq, "Nk": w3.Nk,
+                   "d": w3.d, "causal": True, "scale": w3.scale,
+                   "step": f"prefill {HEADLINE} + prefill {LONG} + decode {DECODE}",
+                   "l2": "flushed before every step (256 MiB write)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": p3["roofline"],
+        "parts": {HEADLINE: p3, LONG: p4, DECODE: p5},
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": launches_per_step * K,
+    }
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        BH = w3.B * w3.H
+        o_np = o3.reshape(BH, w3.Nq, w3.d).float().cpu().numpy()
+        l_np = l3.reshape(BH, w3.Nq).cpu().numpy()
+        line["cpu_baseline"] = cpu_baseline_leg(w3, bf16_bits(q3), bf16_bits(k3), bf16_bits(v3),
+                                                o_np, l_np)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    if args.case:
+        run_case(args)
+        return
+    run_gpu(args)
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
