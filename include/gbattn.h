@@ -120,6 +120,39 @@ int attn_fwd_from_host(const void *q, const void *k, const void *v, void *o, flo
                        int B, int H, int Nq, int Nk, int d, int causal, float scale,
                        void *stream);
 
+/*
+ * attn_fwd_decode_no_alloc -- attn_fwd_decode for callers that cannot
+ * allocate device memory.  The lecture pages have no counterpart of this
+ * call; it exists for users of this library.
+ *
+ * attn_fwd_decode needs the caller to provide a workspace.  Some callers
+ * cannot call cudaMalloc: a plugin inside a host application that owns and
+ * budgets all device memory, or a latency-critical serving loop in which
+ * cudaMalloc/cudaFree are not allowed because they can synchronise the whole
+ * device.  This call computes the same result as attn_fwd_decode but keeps
+ * the split partials in a fixed scratch array of
+ * ATTN_DECODE_NO_ALLOC_SCRATCH_BYTES that lives in the library's own device
+ * memory (every GPU that loads the library holds it until the process exits).
+ * The call allocates nothing; the caller still passes q, k, v, o and lse.
+ *
+ *   Arguments and layouts as attn_fwd_decode, without the workspace.
+ *   Sizes whose partials need more than ATTN_DECODE_NO_ALLOC_SCRATCH_BYTES
+ *   (i.e. attn_fwd_decode_workspace_bytes(B, H, Nk, d) is larger) are
+ *   rejected with ATTN_ERR_UNSUPPORTED before anything is launched; use
+ *   attn_fwd_decode with your own workspace for them.
+ *   The first call on each device looks up the scratch array's device
+ *   address (cudaGetSymbolAddress) with that device current; make that first
+ *   call before any stream capture.
+ *   All calls share the one array and it keeps the previous call's contents;
+ *   nothing in it needs to start at zero.  Calls whose kernels overlap on the
+ *   GPU (other streams, other host threads) race on the array: order them on
+ *   one stream or wait for one to finish before the next.
+ * Returns as attn_fwd_decode.
+ */
+#define ATTN_DECODE_NO_ALLOC_SCRATCH_BYTES (2u << 20) /* 2 MiB */
+int attn_fwd_decode_no_alloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                             int B, int H, int Nk, int d, float scale, void *stream);
+
 /* attn_status_string -- a static, human-readable name for a status code. */
 const char *attn_status_string(int status);
 
