@@ -206,69 +206,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ================================================= MMA issuer
+        // Issue order per key tile j (after the prologue S_0(0), S_1(0)):
+        //   O_0 += P_0(j) V_j,  S_0(j+1) = Q_0 K_{j+1}^T,  O_1 += P_1(j) V_j,  S_1(j+1)
+        // so that while warpgroup t runs the softmax of S_t(j+1), the tensor core
+        // works on the other tile's two products.  S_t(j+1) overwrites the TMEM
+        // columns P_t(j) is read from by the product issued just before it; the
+        // MMAs of one thread run in issue order, so the read comes first.
         if (lane == 0) {
             const uint32_t idesc_qk = umma_idesc_bf16(kBM, kBN, false);
             const uint32_t idesc_pv = umma_idesc_bf16(kBM, D, true);
-            const int total_uses = 2 * n_kv_max;
-            bool ok = wait_or_abort(bars.q, 0, abort_flag);
-            tc_fence_after();
-            for (int j = 0; j < n_kv_max && ok; ++j) {
-                // ---- S_t = Q_t K_j^T
-                const int uk = 2 * j;
-                const int slot_k = uk % C::kSlots;
-                if (!wait_or_abort(bars.full(slot_k), (uk / C::kSlots) & 1, abort_flag)) {
-                    ok = false;
-                    break;
+            const int total_uses = 2 * n_kv_max;  // ring use 2j = K_j, 2j + 1 = V_j
+            auto wait_use = [&](int u) {
+                return wait_or_abort(bars.full(u % C::kSlots), (u / C::kSlots) & 1, abort_flag);
+            };
+            auto release_use = [&](int u) {
+                if (u + C::kSlots < total_uses) umma_commit(bars.empty(u % C::kSlots));
+            };
+            auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T
+                const uint32_t qa = sQ + t * C::kTileBytes;
+                const uint32_t kb = sRing + ((2 * j) % C::kSlots) * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::kSubBytes + (kk & 3) * 32;
+                    umma_ss(tmem + C::col_s(t), umma_desc_sw128(qa + off, 16, 1024),
+                            umma_desc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
                 }
+                umma_commit(bars.s_full(t));
+            };
+            auto issue_pv = [&](int t, int j) {  // O_t += P_t V_j
+                const uint32_t vb = sRing + ((2 * j + 1) % C::kSlots) * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    // P: 16 keys = 8 packed columns; V: 16 key rows of 128 B,
+                    // the two 64-wide halves of d are kSubBytes apart (LBO)
+                    umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8,
+                            umma_desc_sw128(vb + kk * 16 * 128, C::kSubBytes, 1024), idesc_pv,
+                            (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                umma_commit(bars.pv_done(t));
+            };
+            bool ok = wait_or_abort(bars.q, 0, abort_flag) && wait_use(0);
+            if (ok) {
                 tc_fence_after();
+                issue_s(0, 0);  // n_kv0, n_kv1 >= 1
+                issue_s(1, 0);
+                release_use(0);
+            }
+            for (int j = 0; j < n_kv_max && ok; ++j) {
+                ok = wait_use(2 * j + 1);  // V_j
+                bool k_next_ready = false;
                 for (int t = 0; t < 2 && ok; ++t) {
                     if (j >= (t ? n_kv1 : n_kv0)) continue;
-                    // P_t(j-1) lives in S_t's columns: its P V product must be done
-                    if (j > 0 && !wait_or_abort(bars.pv_done(t), (j - 1) & 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
+                    if (!(ok = wait_or_abort(bars.p_ready(t), j & 1, abort_flag))) break;
                     tc_fence_after();
-                    const uint32_t qa = sQ + t * C::kTileBytes;
-                    const uint32_t kb = sRing + slot_k * C::kTileBytes;
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * C::kSubBytes + (kk & 3) * 32;
-                        umma_ss(tmem + C::col_s(t), umma_desc_sw128(qa + off, 16, 1024),
-                                umma_desc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                    issue_pv(t, j);
+                    if (j + 1 < (t ? n_kv1 : n_kv0)) {
+                        if (!k_next_ready) {
+                            if (!(ok = wait_use(2 * j + 2))) break;
+                            tc_fence_after();
+                            k_next_ready = true;
+                        }
+                        issue_s(t, j + 1);
                     }
-                    umma_commit(bars.s_full(t));
                 }
                 if (!ok) break;
-                if (uk + C::kSlots < total_uses) umma_commit(bars.empty(slot_k));
-
-                // ---- O_t += P_t V_j
-                const int uv = 2 * j + 1;
-                const int slot_v = uv % C::kSlots;
-                if (!wait_or_abort(bars.full(slot_v), (uv / C::kSlots) & 1, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (j >= (t ? n_kv1 : n_kv0)) continue;
-                    if (!wait_or_abort(bars.p_ready(t), j & 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t vb = sRing + slot_v * C::kTileBytes;
-#pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk) {
-                        // P: 16 keys = 8 packed columns; V: 16 key rows of 128 B,
-                        // the two 64-wide halves of d are kSubBytes apart (LBO)
-                        umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8,
-                                umma_desc_sw128(vb + kk * 16 * 128, C::kSubBytes, 1024), idesc_pv,
-                                (j > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    umma_commit(bars.pv_done(t));
-                }
-                if (!ok) break;
-                if (uv + C::kSlots < total_uses) umma_commit(bars.empty(slot_v));
+                release_use(2 * j + 1);
+                if (k_next_ready) release_use(2 * j + 2);
             }
             // every MMA this thread issued has completed once `fin` flips
             umma_commit(bars.fin);
@@ -290,20 +293,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int j = 0; j < (t ? n_kv1 : n_kv0); ++j) {
             ok = wait_or_abort(bars.s_full(t), j & 1, abort_flag);
+            // S_t(j) is issued after P_t(j-1) V_{j-1}, so that product is done;
+            // consume its pv_done phase here so every phase is observed in order
+            if (ok && j > 0) ok = wait_or_abort(bars.pv_done(t), (j - 1) & 1, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            float s[kBN];
-            {
-                uint32_t raw[32];
+            // S row: four 32-column loads in flight, one wait
+            uint32_t sr[kBN];
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    tmem_ld32(tS + q4 * 32, raw);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) s[q4 * 32 + c] = __uint_as_float(raw[c]);
-                }
-            }
+            for (int q4 = 0; q4 < 4; ++q4)
+                tmem_ld32(tS + q4 * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[q4 * 32]));
+            tmem_wait_ld();
+            float* s = reinterpret_cast<float*>(sr);
             const int key0 = j * kBN;
             const bool ragged = key0 + kBN > p.Nk;
             const bool diag = p.causal && (key0 + kBN - 1 > row0 + t * kBM);
@@ -313,9 +315,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < kBN; ++c)
                     if (key0 + c > lim) s[c] = -INFINITY;
             }
-            float mx = s[0];
+            // row max: eight independent 3-input max chains, then a short tree
+            float mc[8];
 #pragma unroll
-            for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+            for (int i = 0; i < 8; ++i) mc[i] = fmaxf(s[i], s[i + 8]);
+#pragma unroll
+            for (int c = 16; c < kBN; c += 16)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mc[i] = fmax3(mc[i], s[c + i], s[c + 8 + i]);
+            const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]),
+                                   fmaxf(fmax3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7])));
             const float m_tile = mx * cl2;
             float alpha = 1.f;
             if (j == 0) {
@@ -326,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             l *= alpha;
             const float mneg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-            float lsum0 = 0.f, lsum1 = 0.f;
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial row sums
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
                 uint32_t pk[16];
@@ -334,16 +343,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 16; ++c) {
                     const float p0 = ex2_approx(fmaf(s[h * 32 + 2 * c], cl2, mneg));
                     const float p1 = ex2_approx(fmaf(s[h * 32 + 2 * c + 1], cl2, mneg));
-                    lsum0 += p0;
-                    lsum1 += p1;
+                    ls[(c & 1) * 2] += p0;
+                    ls[(c & 1) * 2 + 1] += p1;
                     pk[c] = pack_bf16x2(p0, p1);
                 }
                 tmem_st16(tS + h * 16, pk);  // P over the first 64 columns of S
             }
-            l += lsum0 + lsum1;
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                // O_t row *= alpha.  The previous P V product is complete: S_t(j)
-                // was only issued after it finished.
+                // O_t row *= alpha.  The previous P V product is complete (its
+                // pv_done phase was observed above).
 #pragma unroll 1
                 for (int ch = 0; ch < D / 32; ++ch) {
                     uint32_t o[32];
