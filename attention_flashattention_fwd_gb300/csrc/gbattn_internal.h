@@ -8,7 +8,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
-#include "../../include/gbattn.h"
+#include "gbattn.h"  // include/ is on the include path
 
 namespace gbattn {
 

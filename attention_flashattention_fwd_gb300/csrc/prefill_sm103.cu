@@ -222,25 +222,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto release_use = [&](int u) {
                 if (u + C::kSlots < total_uses) umma_commit(bars.empty(u % C::kSlots));
             };
+            // Descriptors are built once; the k-steps only move the start address
+            // (bits 0-13 of the low word, in 16-byte units), which never carries.
+            const uint64_t dq0 = umma_desc_sw128(sQ, 16, 1024);
+            const uint64_t dk0 = umma_desc_sw128(sRing, 16, 1024);
+            const uint64_t dv0 = umma_desc_sw128(sRing, C::kSubBytes, 1024);
             auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T
-                const uint32_t qa = sQ + t * C::kTileBytes;
-                const uint32_t kb = sRing + ((2 * j) % C::kSlots) * C::kTileBytes;
+                const uint64_t da = dq0 + ((t * C::kTileBytes) >> 4);
+                const uint64_t db = dk0 + ((((2 * j) % C::kSlots) * C::kTileBytes) >> 4);
+                const uint32_t dst = tmem + C::col_s(t);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::kSubBytes + (kk & 3) * 32;
-                    umma_ss(tmem + C::col_s(t), umma_desc_sw128(qa + off, 16, 1024),
-                            umma_desc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                    const uint32_t off = ((kk >> 2) * C::kSubBytes + (kk & 3) * 32) >> 4;
+                    umma_ss(dst, da + off, db + off, idesc_qk, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(bars.s_full(t));
             };
             auto issue_pv = [&](int t, int j) {  // O_t += P_t V_j
-                const uint32_t vb = sRing + ((2 * j + 1) % C::kSlots) * C::kTileBytes;
+                const uint64_t db = dv0 + ((((2 * j + 1) % C::kSlots) * C::kTileBytes) >> 4);
+                const uint32_t dst = tmem + C::col_o(t);
+                const uint32_t pa = tmem + C::col_s(t);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
                     // P: 16 keys = 8 packed columns; V: 16 key rows of 128 B,
                     // the two 64-wide halves of d are kSubBytes apart (LBO)
-                    umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8,
-                            umma_desc_sw128(vb + kk * 16 * 128, C::kSubBytes, 1024), idesc_pv,
+                    umma_ts(dst, pa + kk * 8, db + ((kk * 16 * 128) >> 4), idesc_pv,
                             (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(bars.pv_done(t));
