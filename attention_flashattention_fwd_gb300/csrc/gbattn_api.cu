@@ -2,6 +2,7 @@
 // include/gbattn.h): argument validation, TMA descriptor encoding and kernel
 // launches.  Every check happens before the first CUDA call, so a rejected
 // call launches nothing.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -56,6 +57,28 @@ int ensure_init() {
     return g_init_status;
 }
 
+// Streaming multiprocessors of the current device (cached per device).
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_num_sms[kMaxDevices];
+
+int current_sm_count(int* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (dev >= 0 && dev < kMaxDevices) {
+        const int cached = g_num_sms[dev].load(std::memory_order_relaxed);
+        if (cached > 0) {
+            *out = cached;
+            return ATTN_OK;
+        }
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return ATTN_ERR_CUDA;
+    if (dev >= 0 && dev < kMaxDevices) g_num_sms[dev].store(n, std::memory_order_relaxed);
+    *out = n;
+    return ATTN_OK;
+}
+
 // [BH, N, d] bf16 viewed as a 3-D tensor (d innermost), boxes of 64 x 128 x 1
 // with the 128-byte swizzle the tcgen05 operand descriptors expect.
 int encode_bhnd(CUtensorMap* m, const void* base, long long BH, int N, int d) {
@@ -76,6 +99,8 @@ int enqueue_fwd(const void* q, const void* k, const void* v, void* o, float* lse
                 int Nq, int Nk, int d, int causal, float scale, cudaStream_t stream) {
     int st = ensure_init();
     if (st != ATTN_OK) return st;
+    int num_sms = 0;
+    if ((st = current_sm_count(&num_sms)) != ATTN_OK) return st;
     const long long BH = static_cast<long long>(B) * H;
     CUtensorMap tq, tk, tv;
     if ((st = encode_bhnd(&tq, q, BH, Nq, d)) != ATTN_OK) return st;
@@ -90,7 +115,7 @@ int enqueue_fwd(const void* q, const void* k, const void* v, void* o, float* lse
     p.num_pairs = (Nq + 255) / 256;
     p.causal = causal;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
-    return launch_prefill(d, tq, tk, tv, p, stream);
+    return launch_prefill(d, tq, tk, tv, p, num_sms, stream);
 }
 
 }  // namespace

@@ -37,10 +37,10 @@ struct DecodeParams {
 
 // prefill_sm103.cu
 int prefill_set_attributes();
+// Persistent launch: min(work items, num_sms) CTAs, one per SM.
 int launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                   const PrefillParams& p, cudaStream_t stream);
+                   const PrefillParams& p, int num_sms, cudaStream_t stream);
 int prefill_smem_bytes(int d);
-int prefill_grid(int Nq, long long BH);
 unsigned read_and_clear_prefill_error();
 
 // decode_sm103.cu

@@ -8,20 +8,25 @@
 // of a query block are skipped (same section).  The blocked softmax merge it
 // relies on is CS149 Lecture 9 notes, concept 9.
 //
-// How it maps onto a GB300 SM (one CTA per SM, 10 warps):
-//   * a CTA owns two consecutive 128-row query tiles of one (b, h) and streams
-//     the key/value tiles they share once;
-//   * warp 9 (one thread) is the TMA producer: Q0/Q1 once, then K_j and V_j
-//     tiles through a ring of shared-memory slots guarded by full/empty
-//     mbarriers with transaction counts (the double buffering of CS149
-//     Lecture 9 concept 2, deeper than two);
+// How it maps onto a GB300 SM (persistent: one CTA per SM, 10 warps):
+//   * a work item is a pair of consecutive 128-row query tiles of one (b, h);
+//     the two tiles share every key/value tile they visit.  Items are ordered
+//     heaviest first (causal) and dealt to the CTAs in a snake order
+//     (0..G-1, G-1..0, ...), which balances the causal triangle as well as a
+//     greedy longest-first schedule;
+//   * warp 9 (one thread) is the TMA producer: Q_0/Q_1 of an item (as soon as
+//     the previous item's last Q K^T products are done), then K_j and V_j tiles
+//     through a ring of shared-memory slots guarded by full/empty mbarriers
+//     with transaction counts (the double buffering of CS149 Lecture 9
+//     concept 2, deeper than two), running ahead across item boundaries;
 //   * warp 8 (one thread) issues tcgen05.mma: S_t = Q_t K_j^T into Tensor
 //     Memory, then O_t += P_t V_j with P read from Tensor Memory;
 //   * warps 0-3 and 4-7 are the softmax warpgroups of query tiles 0 and 1: a
 //     thread owns one query row (= one TMEM lane), so row max and row sum need
 //     no shuffles; it writes P back as bf16 over its own S columns, rescales
 //     its O row in TMEM when the running max moved up by more than 2^8, and
-//     finally writes O / l and the logsumexp;
+//     at the end of an item writes O / l and the logsumexp, then hands the O
+//     columns back to the MMA warp for the next item;
 //   * the two query tiles ping-pong: while one warpgroup runs its softmax the
 //     tensor core works on the other tile.
 // Scores use base 2: with c = scale * log2(e), p = 2^{s c - m} and
@@ -55,8 +60,9 @@ struct Cfg {
     static constexpr int kQOff = 0;
     static constexpr int kRingOff = 2 * kTileBytes;
     static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
-    // barriers: q, full[kSlots], empty[kSlots], s_full[2], p_ready[2], pv_done[2], final
-    static constexpr int kNumBars = 1 + 2 * kSlots + 6 + 1;
+    // barriers: full[kSlots], empty[kSlots], then per query tile q_full, q_empty,
+    // s_full, p_ready, pv_done, o_free, then fin
+    static constexpr int kNumBars = 2 * kSlots + 12 + 1;
     static constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
     static constexpr int kAbortOff = kTmemSlotOff + 4;
     static constexpr int kSmemBytes = kAbortOff + 4 + 1024;  // + alignment slack
@@ -67,14 +73,50 @@ struct Cfg {
 };
 
 struct Bars {
-    uint32_t q, full0, empty0, s_full0, p_ready0, pv_done0, fin;
-    int slots;
+    uint32_t full0, empty0, tile0, fin;
     __device__ uint32_t full(int i) const { return full0 + 8u * i; }
     __device__ uint32_t empty(int i) const { return empty0 + 8u * i; }
-    __device__ uint32_t s_full(int t) const { return s_full0 + 8u * t; }
-    __device__ uint32_t p_ready(int t) const { return p_ready0 + 8u * t; }
-    __device__ uint32_t pv_done(int t) const { return pv_done0 + 8u * t; }
+    // six barriers per query tile t
+    __device__ uint32_t q_full(int t) const { return tile0 + 8u * (6 * t + 0); }
+    __device__ uint32_t q_empty(int t) const { return tile0 + 8u * (6 * t + 1); }
+    __device__ uint32_t s_full(int t) const { return tile0 + 8u * (6 * t + 2); }
+    __device__ uint32_t p_ready(int t) const { return tile0 + 8u * (6 * t + 3); }
+    __device__ uint32_t pv_done(int t) const { return tile0 + 8u * (6 * t + 4); }
+    __device__ uint32_t o_free(int t) const { return tile0 + 8u * (6 * t + 5); }
 };
+
+// Geometry of work item `idx` (0 <= idx < num_pairs * BH).
+struct Item {
+    int bh, row0, n_kv0, n_kv1;
+    __device__ int n_kv(int t) const { return t ? n_kv1 : n_kv0; }
+    __device__ int n_kv_max() const { return max(n_kv0, n_kv1); }
+};
+
+__device__ __forceinline__ Item item_at(const PrefillParams& p, int idx) {
+    Item it;
+    int pair;
+    if (p.causal) {  // heaviest pairs (most key tiles) first
+        pair = p.num_pairs - 1 - idx / p.BH;
+        it.bh = idx % p.BH;
+    } else {  // a head's pairs are consecutive: its K/V stay in L2
+        pair = idx % p.num_pairs;
+        it.bh = idx / p.num_pairs;
+    }
+    it.row0 = pair * 2 * kBM;
+    const int n_kv_all = (p.Nk + kBN - 1) / kBN;
+    // key tiles each query tile visits (causal: up to and including its diagonal)
+    it.n_kv0 = p.causal ? min(n_kv_all, it.row0 / kBN + 1) : n_kv_all;
+    it.n_kv1 = p.causal ? min(n_kv_all, it.row0 / kBN + 2) : n_kv_all;
+    return it;
+}
+
+// k-th item of this CTA in the snake deal, or -1 when there are no more.
+__device__ __forceinline__ int item_index(int k, int n_items) {
+    const int G = static_cast<int>(gridDim.x);
+    const int c = static_cast<int>(blockIdx.x);
+    const long long idx = static_cast<long long>(k) * G + ((k & 1) ? G - 1 - c : c);
+    return idx < n_items ? static_cast<int>(idx) : -1;
+}
 
 __device__ __forceinline__ void flag_abort(volatile int* abort_flag) {
     *abort_flag = 1;
@@ -114,48 +156,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sQ = sbase + C::kQOff;
     const uint32_t sRing = sbase + C::kRingOff;
     Bars bars;
-    bars.slots = C::kSlots;
-    bars.q = sbase + C::kBarOff;
-    bars.full0 = bars.q + 8;
+    bars.full0 = sbase + C::kBarOff;
     bars.empty0 = bars.full0 + 8 * C::kSlots;
-    bars.s_full0 = bars.empty0 + 8 * C::kSlots;
-    bars.p_ready0 = bars.s_full0 + 16;
-    bars.pv_done0 = bars.p_ready0 + 16;
-    bars.fin = bars.pv_done0 + 16;
+    bars.tile0 = bars.empty0 + 8 * C::kSlots;
+    bars.fin = bars.tile0 + 8 * 12;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kTmemSlotOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    // ---- work item: a pair of query tiles of one (b, h)
-    const int L = blockIdx.x;
-    int pair, bh;
-    if (p.causal) {  // heaviest pairs (most key tiles) first
-        pair = p.num_pairs - 1 - L / p.BH;
-        bh = L % p.BH;
-    } else {  // consecutive CTAs share a head: its K/V stay in L2
-        pair = L % p.num_pairs;
-        bh = L / p.num_pairs;
-    }
-    const int row0 = pair * 2 * kBM;
-    const int n_kv_all = (p.Nk + kBN - 1) / kBN;
-    // key tiles each query tile visits (causal: up to and including its diagonal)
-    const int n_kv0 = p.causal ? min(n_kv_all, row0 / kBN + 1) : n_kv_all;
-    const int n_kv1 = p.causal ? min(n_kv_all, row0 / kBN + 2) : n_kv_all;
-    const int n_kv_max = max(n_kv0, n_kv1);
+    const int n_items = p.num_pairs * p.BH;
 
     // ---- set-up: barriers (one thread), Tensor Memory (warp 0)
     if (threadIdx.x == kLoadWarp * 32) {
-        mbar_init(bars.q, 1);
         for (int i = 0; i < C::kSlots; ++i) {
             mbar_init(bars.full(i), 1);
             mbar_init(bars.empty(i), 1);
         }
         for (int t = 0; t < 2; ++t) {
+            mbar_init(bars.q_full(t), 1);
+            mbar_init(bars.q_empty(t), 1);
             mbar_init(bars.s_full(t), 1);
             mbar_init(bars.p_ready(t), 4);  // one arrival per softmax warp
             mbar_init(bars.pv_done(t), 1);
+            mbar_init(bars.o_free(t), 4);   // one arrival per softmax warp
         }
         mbar_init(bars.fin, 1);
         *abort_flag = 0;
@@ -169,32 +193,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kLoadWarp) {
         // ================================================= TMA producer
-        int issued = 0;  // K/V tiles issued into the ring
         if (lane == 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
-            mbar_arrive_expect_tx(bars.q, 2 * C::kTileBytes);
-            for (int t = 0; t < 2; ++t)
-                for (int s = 0; s < C::kSub; ++s)
-                    tma_load_3d(sQ + t * C::kTileBytes + s * C::kSubBytes, &tm_q, bars.q, s * 64,
-                                row0 + t * kBM, bh);
+            int issued = 0;  // ring uses (K or V tiles) issued so far
             bool ok = true;
-            for (int j = 0; j < n_kv_max && ok; ++j) {
-                for (int which = 0; which < 2; ++which) {
-                    const int u = 2 * j + which;
-                    const int slot = u % C::kSlots;
-                    const uint32_t ph = (u / C::kSlots) & 1;
-                    if (u >= C::kSlots && !wait_or_abort(bars.empty(slot), ph ^ 1, abort_flag)) {
-                        ok = false;
+            for (int k = 0; ok; ++k) {
+                const int idx = item_index(k, n_items);
+                if (idx < 0) break;
+                const Item it = item_at(p, idx);
+                for (int t = 0; t < 2 && ok; ++t) {
+                    // the previous item's last Q_t K^T product has finished
+                    if (k > 0 && !(ok = wait_or_abort(bars.q_empty(t), (k - 1) & 1, abort_flag)))
                         break;
-                    }
-                    mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
-                    const CUtensorMap* tm = which ? &tm_v : &tm_k;
+                    mbar_arrive_expect_tx(bars.q_full(t), C::kTileBytes);
                     for (int s = 0; s < C::kSub; ++s)
-                        tma_load_3d(sRing + slot * C::kTileBytes + s * C::kSubBytes, tm,
-                                    bars.full(slot), s * 64, j * kBN, bh);
-                    ++issued;
+                        tma_load_3d(sQ + t * C::kTileBytes + s * C::kSubBytes, &tm_q,
+                                    bars.q_full(t), s * 64, it.row0 + t * kBM, it.bh);
+                }
+                for (int j = 0; j < it.n_kv_max() && ok; ++j) {
+                    for (int which = 0; which < 2; ++which) {
+                        const int u = issued;  // K_j is use 2j, V_j is use 2j + 1 of the item
+                        const int slot = u % C::kSlots;
+                        if (u >= C::kSlots &&
+                            !(ok = wait_or_abort(bars.empty(slot), ((u / C::kSlots) & 1) ^ 1,
+                                                 abort_flag)))
+                            break;
+                        mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
+                        const CUtensorMap* tm = which ? &tm_v : &tm_k;
+                        for (int s = 0; s < C::kSub; ++s)
+                            tma_load_3d(sRing + slot * C::kTileBytes + s * C::kSubBytes, tm,
+                                        bars.full(slot), s * 64, j * kBN, it.bh);
+                        ++issued;
+                    }
                 }
             }
             if (!ok) {
@@ -206,30 +238,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ================================================= MMA issuer
-        // Issue order per key tile j (after the prologue S_0(0), S_1(0)):
+        // Issue order per key tile j of an item (after the item's S_0(0), S_1(0)):
         //   O_0 += P_0(j) V_j,  S_0(j+1) = Q_0 K_{j+1}^T,  O_1 += P_1(j) V_j,  S_1(j+1)
         // so that while warpgroup t runs the softmax of S_t(j+1), the tensor core
         // works on the other tile's two products.  S_t(j+1) overwrites the TMEM
         // columns P_t(j) is read from by the product issued just before it; the
         // MMAs of one thread run in issue order, so the read comes first.
+        // The thread issues nothing but MMAs and the commits the softmax needs:
+        // one tcgen05.mma takes it about as long to issue as an M128 N128 K16
+        // product takes to run, so ring slots are released by the softmax of
+        // tile 1 instead (see there) and P V completion is only committed at
+        // the end of an item.
         if (lane == 0) {
             const uint32_t idesc_qk = umma_idesc_bf16(kBM, kBN, false);
             const uint32_t idesc_pv = umma_idesc_bf16(kBM, D, true);
-            const int total_uses = 2 * n_kv_max;  // ring use 2j = K_j, 2j + 1 = V_j
-            auto wait_use = [&](int u) {
-                return wait_or_abort(bars.full(u % C::kSlots), (u / C::kSlots) & 1, abort_flag);
-            };
-            auto release_use = [&](int u) {
-                if (u + C::kSlots < total_uses) umma_commit(bars.empty(u % C::kSlots));
+            int u = 0;             // ring use of the current K tile
+            int iter[2] = {0, 0};  // key tiles processed per query tile, over all items
+            auto wait_use = [&](int use) {
+                return wait_or_abort(bars.full(use % C::kSlots), (use / C::kSlots) & 1,
+                                     abort_flag);
             };
             // Descriptors are built once; the k-steps only move the start address
             // (bits 0-13 of the low word, in 16-byte units), which never carries.
             const uint64_t dq0 = umma_desc_sw128(sQ, 16, 1024);
             const uint64_t dk0 = umma_desc_sw128(sRing, 16, 1024);
             const uint64_t dv0 = umma_desc_sw128(sRing, C::kSubBytes, 1024);
-            auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T
+            auto issue_s = [&](int t, int use) {  // S_t = Q_t K^T, K in ring use `use`
                 const uint64_t da = dq0 + ((t * C::kTileBytes) >> 4);
-                const uint64_t db = dk0 + ((((2 * j) % C::kSlots) * C::kTileBytes) >> 4);
+                const uint64_t db = dk0 + (((use % C::kSlots) * C::kTileBytes) >> 4);
                 const uint32_t dst = tmem + C::col_s(t);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -238,8 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 umma_commit(bars.s_full(t));
             };
-            auto issue_pv = [&](int t, int j) {  // O_t += P_t V_j
-                const uint64_t db = dv0 + ((((2 * j + 1) % C::kSlots) * C::kTileBytes) >> 4);
+            auto issue_pv = [&](int t, int use, bool first) {  // O_t (+)= P_t V
+                const uint64_t db = dv0 + (((use % C::kSlots) * C::kTileBytes) >> 4);
                 const uint32_t dst = tmem + C::col_o(t);
                 const uint32_t pa = tmem + C::col_s(t);
 #pragma unroll
@@ -247,37 +283,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // P: 16 keys = 8 packed columns; V: 16 key rows of 128 B,
                     // the two 64-wide halves of d are kSubBytes apart (LBO)
                     umma_ts(dst, pa + kk * 8, db + ((kk * 16 * 128) >> 4), idesc_pv,
-                            (j > 0 || kk > 0) ? 1u : 0u);
+                            (!first || kk > 0) ? 1u : 0u);
                 }
-                umma_commit(bars.pv_done(t));
             };
-            bool ok = wait_or_abort(bars.q, 0, abort_flag) && wait_use(0);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0, 0);  // n_kv0, n_kv1 >= 1
-                issue_s(1, 0);
-                release_use(0);
-            }
-            for (int j = 0; j < n_kv_max && ok; ++j) {
-                ok = wait_use(2 * j + 1);  // V_j
-                bool k_next_ready = false;
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (j >= (t ? n_kv1 : n_kv0)) continue;
-                    if (!(ok = wait_or_abort(bars.p_ready(t), j & 1, abort_flag))) break;
-                    tc_fence_after();
-                    issue_pv(t, j);
-                    if (j + 1 < (t ? n_kv1 : n_kv0)) {
-                        if (!k_next_ready) {
-                            if (!(ok = wait_use(2 * j + 2))) break;
-                            tc_fence_after();
-                            k_next_ready = true;
-                        }
-                        issue_s(t, j + 1);
-                    }
-                }
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int idx = item_index(k, n_items);
+                if (idx < 0) break;
+                const Item it = item_at(p, idx);
+                const int nmax = it.n_kv_max();
+                // prologue of the item: S_0(0), S_1(0)
+                ok = wait_or_abort(bars.q_full(0), k & 1, abort_flag) &&
+                     wait_or_abort(bars.q_full(1), k & 1, abort_flag) && wait_use(u);
                 if (!ok) break;
-                release_use(2 * j + 1);
-                if (k_next_ready) release_use(2 * j + 2);
+                tc_fence_after();
+                for (int t = 0; t < 2; ++t) {
+                    issue_s(t, u);  // n_kv0, n_kv1 >= 1
+                    if (it.n_kv(t) == 1) umma_commit(bars.q_empty(t));
+                }
+                for (int j = 0; j < nmax && ok; ++j) {
+                    const int uv = u + 1, uk = u + 2;  // V_j, K_{j+1}
+                    ok = wait_use(uv);
+                    bool k_next_ready = false;
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (j >= it.n_kv(t)) continue;
+                        if (!(ok = wait_or_abort(bars.p_ready(t), iter[t] & 1, abort_flag)))
+                            break;
+                        // O_t of the previous item has been read by its epilogue
+                        if (j == 0 && k > 0 &&
+                            !(ok = wait_or_abort(bars.o_free(t), (k - 1) & 1, abort_flag)))
+                            break;
+                        tc_fence_after();
+                        issue_pv(t, uv, j == 0);
+                        ++iter[t];
+                        if (j + 1 < it.n_kv(t)) {
+                            if (!k_next_ready) {
+                                if (!(ok = wait_use(uk))) break;
+                                tc_fence_after();
+                                k_next_ready = true;
+                            }
+                            issue_s(t, uk);
+                            if (j + 2 == it.n_kv(t)) umma_commit(bars.q_empty(t));
+                        } else {
+                            umma_commit(bars.pv_done(t));  // O_t of this item is complete
+                        }
+                    }
+                    u += 2;
+                }
             }
             // every MMA this thread issued has completed once `fin` flips
             umma_commit(bars.fin);
@@ -289,101 +341,119 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = warp >> 2;          // query tile 0 or 1
         const int wq = warp & 3;          // TMEM lane quarter
         const int r = wq * 32 + lane;     // row within the tile
-        const int row = row0 + t * kBM + r;
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t tS = tmem + lane_off + C::col_s(t);
         const uint32_t tO = tmem + lane_off + C::col_o(t);
         const float cl2 = p.scale_log2;
-        float m_ref = -INFINITY;  // running reference max, log2 units
-        float l = 0.f;
+        int iter = 0;  // key tiles processed by this tile over all items
         bool ok = true;
-        for (int j = 0; j < (t ? n_kv1 : n_kv0); ++j) {
-            ok = wait_or_abort(bars.s_full(t), j & 1, abort_flag);
-            // S_t(j) is issued after P_t(j-1) V_{j-1}, so that product is done;
-            // consume its pv_done phase here so every phase is observed in order
-            if (ok && j > 0) ok = wait_or_abort(bars.pv_done(t), (j - 1) & 1, abort_flag);
+        for (int k = 0; ok; ++k) {
+            const int idx = item_index(k, n_items);
+            if (idx < 0) break;
+            const Item it = item_at(p, idx);
+            const int row = it.row0 + t * kBM + r;
+            const int nkv = it.n_kv(t);
+            float m_ref = -INFINITY;  // running reference max, log2 units
+            float l = 0.f;
+            for (int j = 0; j < nkv; ++j, ++iter) {
+                ok = wait_or_abort(bars.s_full(t), iter & 1, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                // S_t(j) was issued after every earlier product of this CTA, so its
+                // completion means K_j (last read by S_1(j)) and V_{j-1} (last read
+                // by P_1(j-1) V_{j-1}) are free: tile 1, which visits every key
+                // tile of an item, hands their ring slots back to the producer.
+                // K_j and V_j are ring uses 2 iter and 2 iter + 1.
+                if (t == 1 && wq == 0 && lane == 0) {
+                    mbar_arrive(bars.empty((2 * iter) % C::kSlots));
+                    if (j > 0) mbar_arrive(bars.empty((2 * iter - 1) % C::kSlots));
+                }
+                // S row: four 32-column loads in flight, one wait
+                uint32_t sr[kBN];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    tmem_ld32(tS + q4 * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[q4 * 32]));
+                tmem_wait_ld();
+                float* s = reinterpret_cast<float*>(sr);
+                const int key0 = j * kBN;
+                const bool ragged = key0 + kBN > p.Nk;
+                const bool diag = p.causal && (key0 + kBN - 1 > it.row0 + t * kBM);
+                if (ragged || diag) {
+                    const int lim = p.causal ? min(p.Nk - 1, row) : p.Nk - 1;  // last visible key
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c)
+                        if (key0 + c > lim) s[c] = -INFINITY;
+                }
+                // row max: eight independent 3-input max chains, then a short tree
+                float mc[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mc[i] = fmaxf(s[i], s[i + 8]);
+#pragma unroll
+                for (int c = 16; c < kBN; c += 16)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mc[i] = fmax3(mc[i], s[c + i], s[c + 8 + i]);
+                const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]),
+                                       fmaxf(fmax3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7])));
+                const float m_tile = mx * cl2;
+                float alpha = 1.f;
+                if (j == 0) {
+                    m_ref = m_tile;
+                } else if (m_tile > m_ref + kRescaleThreshold) {
+                    alpha = ex2_approx(m_ref - m_tile);
+                    m_ref = m_tile;
+                }
+                l *= alpha;
+                const float mneg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+                // p = 2^(s c - m), the argument two at a time (packed fp32 FMA); the
+                // row sum keeps four independent chains
+                const float2 c2 = make_float2(cl2, cl2), m2 = make_float2(mneg, mneg);
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const float2 x = ffma2(make_float2(s[h * 32 + 2 * c], s[h * 32 + 2 * c + 1]),
+                                               c2, m2);
+                        const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                        ls[(c & 1) * 2] += pp.x;
+                        ls[(c & 1) * 2 + 1] += pp.y;
+                        pk[c] = pack_bf16x2(pp.x, pp.y);
+                    }
+                    tmem_st16(tS + h * 16, pk);  // P over the first 64 columns of S
+                }
+                l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                    // O_t row *= alpha.  The previous P V product is complete: S_t(j)
+                    // was issued after it.
+#pragma unroll 1
+                    for (int ch = 0; ch < D / 32; ++ch) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + ch * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                        tmem_st32(tO + ch * 32, o);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.p_ready(t));
+            }
+            if (!ok) break;
+            // ---- epilogue of the item: O / l and the logsumexp
+            ok = wait_or_abort(bars.pv_done(t), k & 1, abort_flag);  // one phase per item
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            // S row: four 32-column loads in flight, one wait
-            uint32_t sr[kBN];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-                tmem_ld32(tS + q4 * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[q4 * 32]));
-            tmem_wait_ld();
-            float* s = reinterpret_cast<float*>(sr);
-            const int key0 = j * kBN;
-            const bool ragged = key0 + kBN > p.Nk;
-            const bool diag = p.causal && (key0 + kBN - 1 > row0 + t * kBM);
-            if (ragged || diag) {
-                const int lim = p.causal ? min(p.Nk - 1, row) : p.Nk - 1;  // last visible key
-#pragma unroll
-                for (int c = 0; c < kBN; ++c)
-                    if (key0 + c > lim) s[c] = -INFINITY;
-            }
-            // row max: eight independent 3-input max chains, then a short tree
-            float mc[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mc[i] = fmaxf(s[i], s[i + 8]);
-#pragma unroll
-            for (int c = 16; c < kBN; c += 16)
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mc[i] = fmax3(mc[i], s[c + i], s[c + 8 + i]);
-            const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]),
-                                   fmaxf(fmax3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7])));
-            const float m_tile = mx * cl2;
-            float alpha = 1.f;
-            if (j == 0) {
-                m_ref = m_tile;
-            } else if (m_tile > m_ref + kRescaleThreshold) {
-                alpha = ex2_approx(m_ref - m_tile);
-                m_ref = m_tile;
-            }
-            l *= alpha;
-            const float mneg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial row sums
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const float p0 = ex2_approx(fmaf(s[h * 32 + 2 * c], cl2, mneg));
-                    const float p1 = ex2_approx(fmaf(s[h * 32 + 2 * c + 1], cl2, mneg));
-                    ls[(c & 1) * 2] += p0;
-                    ls[(c & 1) * 2 + 1] += p1;
-                    pk[c] = pack_bf16x2(p0, p1);
-                }
-                tmem_st16(tS + h * 16, pk);  // P over the first 64 columns of S
-            }
-            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                // O_t row *= alpha.  The previous P V product is complete (its
-                // pv_done phase was observed above).
-#pragma unroll 1
-                for (int ch = 0; ch < D / 32; ++ch) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + ch * 32, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                    tmem_st32(tO + ch * 32, o);
-                }
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bars.p_ready(t));
-        }
-        // ---- epilogue: O / l and the logsumexp
-        if (ok && (t ? n_kv1 : n_kv0) > 0) {
-            ok = wait_or_abort(bars.pv_done(t), ((t ? n_kv1 : n_kv0) - 1) & 1, abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-        }
-        if (ok && (t ? n_kv1 : n_kv0) > 0) {
-            tc_fence_after();
+            // the item's last V tile is free once its last P V product is done
+            if (t == 1 && wq == 0 && lane == 0)
+                mbar_arrive(bars.empty((2 * iter - 1) % C::kSlots));
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
-            __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.Nq + row) * D;
+            __nv_bfloat16* orow = p.o + (static_cast<size_t>(it.bh) * p.Nq + row) * D;
 #pragma unroll
             for (int ch = 0; ch < D / 32; ++ch) {
                 uint32_t o[32];
@@ -402,8 +472,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              pk[4 * v4 + 3]);
                 }
             }
+            // O_t has been read: the next item's first P V product may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.o_free(t));
             if (row < p.Nq)
-                p.lse[static_cast<size_t>(bh) * p.Nq + row] =
+                p.lse[static_cast<size_t>(it.bh) * p.Nq + row] =
                     (m_ref + log2f(l)) * 0.69314718055994530942f;
         }
     }
@@ -430,26 +504,22 @@ int prefill_set_attributes() {
 
 template <int D>
 static int launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const PrefillParams& p, cudaStream_t stream) {
+                            const PrefillParams& p, int num_sms, cudaStream_t stream) {
     using C = Cfg<D>;
-    const long long grid = static_cast<long long>(p.num_pairs) * p.BH;
+    const long long items = static_cast<long long>(p.num_pairs) * p.BH;
+    const long long grid = items < num_sms ? items : num_sms;  // one persistent CTA per SM
     attn_fwd_prefill_kernel<D><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
         tq, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 int launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                   const PrefillParams& p, cudaStream_t stream) {
-    return d == 128 ? launch_prefill_d<128>(tq, tk, tv, p, stream)
-                    : launch_prefill_d<64>(tq, tk, tv, p, stream);
+                   const PrefillParams& p, int num_sms, cudaStream_t stream) {
+    return d == 128 ? launch_prefill_d<128>(tq, tk, tv, p, num_sms, stream)
+                    : launch_prefill_d<64>(tq, tk, tv, p, num_sms, stream);
 }
 
 int prefill_smem_bytes(int d) { return d == 128 ? Cfg<128>::kSmemBytes : Cfg<64>::kSmemBytes; }
-
-int prefill_grid(int Nq, long long BH) {
-    const long long pairs = (Nq + 2 * kBM - 1) / (2 * kBM);
-    return static_cast<int>(pairs * BH);
-}
 
 unsigned read_and_clear_prefill_error() {
     unsigned v = 0, zero = 0;
