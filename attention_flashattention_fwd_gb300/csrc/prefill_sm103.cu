@@ -8,7 +8,7 @@
 // of a query block are skipped (same section).  The blocked softmax merge it
 // relies on is CS149 Lecture 9 notes, concept 9.
 //
-// How it maps onto a GB300 SM (persistent: one CTA per SM, 10 warps):
+// How it maps onto a GB300 SM (persistent: one CTA per SM, 12 warps):
 //   * a work item is a pair of consecutive 128-row query tiles of one (b, h);
 //     the two tiles share every key/value tile they visit.  Items are ordered
 //     heaviest first (causal) and dealt to the CTAs in a snake order
@@ -24,9 +24,9 @@
 //   * warps 0-3 and 4-7 are the softmax warpgroups of query tiles 0 and 1: a
 //     thread owns one query row (= one TMEM lane), so row max and row sum need
 //     no shuffles; it writes P back as bf16 over its own S columns, rescales
-//     its O row in TMEM when the running max moved up by more than 2^8, and
-//     at the end of an item writes O / l and the logsumexp, then hands the O
-//     columns back to the MMA warp for the next item;
+//     its O row in TMEM when a key tile lies far above the running reference
+//     max, and at the end of an item writes O / l and the logsumexp, then
+//     hands the O columns back to the MMA warp for the next item;
 //   * the two query tiles ping-pong: while one warpgroup runs its softmax the
 //     tensor core works on the other tile.
 // Scores use base 2: with c = scale * log2(e), p = 2^{s c - m} and
@@ -45,11 +45,19 @@ namespace {
 
 constexpr int kBM = 128;            // query rows per tile (MMA M)
 constexpr int kBN = 128;            // keys per tile (MMA N of S = Q K^T)
-constexpr int kThreads = 320;       // 10 warps
+constexpr int kThreads = 384;       // 12 warps: 8 softmax, MMA, TMA, 2 idle
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
+// Register split.  The launch gives every thread 168 registers (65536 / 384,
+// rounded down to 8): 384 x 168 = 64512.  The warpgroup of the MMA and TMA warps
+// gives most of its share to the two softmax warpgroups:
+// 128 x 112 + 256 x 192 = 63488 <= 64512.
+constexpr uint32_t kSoftmaxRegs = 192;
+constexpr uint32_t kControlRegs = 112;
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only if m grows by > 2^8
+// A key tile whose row sum against the stale reference max exceeds this moves
+// the reference (2^62: far from fp32 overflow for O and l).
+constexpr float kTileSumLimit = 4.611686018427387904e18f;
 
 template <int D>
 struct Cfg {
@@ -191,6 +199,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    if (warp >= 8) {
+    // ====================================================== control warpgroup
+    setmaxnreg_dec<kControlRegs>();
     if (warp == kLoadWarp) {
         // ================================================= TMA producer
         if (lane == 0) {
@@ -199,34 +210,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_v);
             int issued = 0;  // ring uses (K or V tiles) issued so far
             bool ok = true;
+            auto load_q = [&](int k, int t, const Item& it) {
+                // the previous item's last Q_t K^T product has finished
+                if (k > 0 && !(ok = wait_or_abort(bars.q_empty(t), (k - 1) & 1, abort_flag)))
+                    return;
+                mbar_arrive_expect_tx(bars.q_full(t), C::kTileBytes);
+                for (int s = 0; s < C::kSub; ++s)
+                    tma_load_3d(sQ + t * C::kTileBytes + s * C::kSubBytes, &tm_q, bars.q_full(t),
+                                s * 64, it.row0 + t * kBM, it.bh);
+            };
+            auto load_kv = [&](int which, int j, const Item& it) {  // K_j (0) or V_j (1)
+                const int u = issued;  // K_j is use 2j, V_j is use 2j + 1 of the item
+                const int slot = u % C::kSlots;
+                if (u >= C::kSlots &&
+                    !(ok = wait_or_abort(bars.empty(slot), ((u / C::kSlots) & 1) ^ 1, abort_flag)))
+                    return;
+                mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
+                const CUtensorMap* tm = which ? &tm_v : &tm_k;
+                for (int s = 0; s < C::kSub; ++s)
+                    tma_load_3d(sRing + slot * C::kTileBytes + s * C::kSubBytes, tm,
+                                bars.full(slot), s * 64, j * kBN, it.bh);
+                ++issued;
+            };
             for (int k = 0; ok; ++k) {
                 const int idx = item_index(k, n_items);
                 if (idx < 0) break;
                 const Item it = item_at(p, idx);
-                for (int t = 0; t < 2 && ok; ++t) {
-                    // the previous item's last Q_t K^T product has finished
-                    if (k > 0 && !(ok = wait_or_abort(bars.q_empty(t), (k - 1) & 1, abort_flag)))
-                        break;
-                    mbar_arrive_expect_tx(bars.q_full(t), C::kTileBytes);
-                    for (int s = 0; s < C::kSub; ++s)
-                        tma_load_3d(sQ + t * C::kTileBytes + s * C::kSubBytes, &tm_q,
-                                    bars.q_full(t), s * 64, it.row0 + t * kBM, it.bh);
-                }
-                for (int j = 0; j < it.n_kv_max() && ok; ++j) {
-                    for (int which = 0; which < 2; ++which) {
-                        const int u = issued;  // K_j is use 2j, V_j is use 2j + 1 of the item
-                        const int slot = u % C::kSlots;
-                        if (u >= C::kSlots &&
-                            !(ok = wait_or_abort(bars.empty(slot), ((u / C::kSlots) & 1) ^ 1,
-                                                 abort_flag)))
-                            break;
-                        mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
-                        const CUtensorMap* tm = which ? &tm_v : &tm_k;
+                // in the order the MMA warp needs them: Q_0, K_0, Q_1, V_0, K_1, V_1, ...
+                load_q(k, 0, it);
+                if (ok) load_kv(0, 0, it);
+                if (ok) load_q(k, 1, it);
+                if (ok) load_kv(1, 0, it);
+                // warm L2 with the next item's query tiles (read once, from DRAM)
+                const int nidx = item_index(k + 1, n_items);
+                if (ok && nidx >= 0) {
+                    const Item nx = item_at(p, nidx);
+                    for (int t = 0; t < 2; ++t)
                         for (int s = 0; s < C::kSub; ++s)
-                            tma_load_3d(sRing + slot * C::kTileBytes + s * C::kSubBytes, tm,
-                                        bars.full(slot), s * 64, j * kBN, it.bh);
-                        ++issued;
-                    }
+                            tma_prefetch_l2_3d(&tm_q, s * 64, nx.row0 + t * kBM, nx.bh);
+                }
+                for (int j = 1; j < it.n_kv_max() && ok; ++j) {
+                    load_kv(0, j, it);
+                    if (ok) load_kv(1, j, it);
                 }
             }
             if (!ok) {
@@ -292,15 +317,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (idx < 0) break;
                 const Item it = item_at(p, idx);
                 const int nmax = it.n_kv_max();
-                // prologue of the item: S_0(0), S_1(0)
-                ok = wait_or_abort(bars.q_full(0), k & 1, abort_flag) &&
-                     wait_or_abort(bars.q_full(1), k & 1, abort_flag) && wait_use(u);
-                if (!ok) break;
-                tc_fence_after();
-                for (int t = 0; t < 2; ++t) {
+                // prologue of the item: S_0(0) once Q_0 and K_0 are in, then S_1(0)
+                for (int t = 0; t < 2 && ok; ++t) {
+                    ok = wait_or_abort(bars.q_full(t), k & 1, abort_flag) && (t == 1 || wait_use(u));
+                    if (!ok) break;
+                    tc_fence_after();
                     issue_s(t, u);  // n_kv0, n_kv1 >= 1
                     if (it.n_kv(t) == 1) umma_commit(bars.q_empty(t));
                 }
+                if (!ok) break;
                 for (int j = 0; j < nmax && ok; ++j) {
                     const int uv = u + 1, uk = u + 2;  // V_j, K_{j+1}
                     ok = wait_use(uv);
@@ -336,8 +361,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(bars.fin, 0);
         }
         __syncwarp();
+    }  // warps 10 and 11 have no role
     } else {
         // ================================================= softmax warpgroups
+        setmaxnreg_inc<kSoftmaxRegs>();
         const int t = warp >> 2;          // query tile 0 or 1
         const int wq = warp & 3;          // TMEM lane quarter
         const int r = wq * 32 + lane;     // row within the tile
@@ -386,58 +413,72 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (key0 + c > lim) s[c] = -INFINITY;
                 }
                 // row max: eight independent 3-input max chains, then a short tree
-                float mc[8];
+                auto row_max = [&]() {
+                    float mc[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mc[i] = fmaxf(s[i], s[i + 8]);
+                    for (int i = 0; i < 8; ++i) mc[i] = fmaxf(s[i], s[i + 8]);
 #pragma unroll
-                for (int c = 16; c < kBN; c += 16)
+                    for (int c = 16; c < kBN; c += 16)
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) mc[i] = fmax3(mc[i], s[c + i], s[c + 8 + i]);
-                const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]),
-                                       fmaxf(fmax3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7])));
-                const float m_tile = mx * cl2;
-                float alpha = 1.f;
-                if (j == 0) {
-                    m_ref = m_tile;
-                } else if (m_tile > m_ref + kRescaleThreshold) {
-                    alpha = ex2_approx(m_ref - m_tile);
-                    m_ref = m_tile;
-                }
-                l *= alpha;
-                const float mneg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-                // p = 2^(s c - m), the argument two at a time (packed fp32 FMA); the
-                // row sum keeps four independent chains
-                const float2 c2 = make_float2(cl2, cl2), m2 = make_float2(mneg, mneg);
-                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                        for (int i = 0; i < 8; ++i) mc[i] = fmax3(mc[i], s[c + i], s[c + 8 + i]);
+                    return fmaxf(fmax3(mc[0], mc[1], mc[2]),
+                                 fmaxf(fmax3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7])));
+                };
+                // P = 2^(s c - m_ref) into TMEM, with packed fp32 FMA and adds (two
+                // lanes of work per instruction); returns this tile's row sum
+                auto emit_p = [&]() {
+                    const float mneg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+                    const float2 c2 = make_float2(cl2, cl2), m2 = make_float2(mneg, mneg);
+                    float2 ls0 = make_float2(0.f, 0.f), ls1 = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    uint32_t pk[16];
+                    for (int h = 0; h < 4; ++h) {
+                        uint32_t pk[16];
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const float2 x = ffma2(make_float2(s[h * 32 + 2 * c], s[h * 32 + 2 * c + 1]),
-                                               c2, m2);
-                        const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                        ls[(c & 1) * 2] += pp.x;
-                        ls[(c & 1) * 2 + 1] += pp.y;
-                        pk[c] = pack_bf16x2(pp.x, pp.y);
+                        for (int c = 0; c < 16; ++c) {
+                            const float2 x = ffma2(
+                                make_float2(s[h * 32 + 2 * c], s[h * 32 + 2 * c + 1]), c2, m2);
+                            const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                            if (c & 1) ls1 = fadd2(ls1, pp); else ls0 = fadd2(ls0, pp);
+                            pk[c] = pack_bf16x2(pp.x, pp.y);
+                        }
+                        tmem_st16(tS + h * 16, pk);  // P over the first 64 columns of S
                     }
-                    tmem_st16(tS + h * 16, pk);  // P over the first 64 columns of S
-                }
-                l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                    // O_t row *= alpha.  The previous P V product is complete: S_t(j)
-                    // was issued after it.
+                    return (ls0.x + ls0.y) + (ls1.x + ls1.y);
+                };
+                // The reference m_ref is the row max of the item's first key tile and
+                // is only moved when a later tile would overflow against it: O and l
+                // share the reference, so any reference gives the same O / l, and
+                // fp32 / bf16 keep full relative precision for p up to 2^62.  Most
+                // tiles therefore need no row max at all.
+                if (j == 0) m_ref = row_max() * cl2;
+                float lt = emit_p();
+                if (__any_sync(0xffffffffu, !(lt <= kTileSumLimit))) {
+                    // rare: move this row's reference to the tile max, rescale O and l,
+                    // and write P again (rows that did not move write the same P)
+                    float alpha = 1.f;
+                    if (!(lt <= kTileSumLimit)) {
+                        const float m_tile = row_max() * cl2;
+                        alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - m_tile);
+                        m_ref = m_tile;
+                        l *= alpha;
+                    }
+                    if (j > 0) {
+                        // O_t row *= alpha.  The previous P V product is complete:
+                        // S_t(j) was issued after it.
 #pragma unroll 1
-                    for (int ch = 0; ch < D / 32; ++ch) {
-                        uint32_t o[32];
-                        tmem_ld32(tO + ch * 32, o);
-                        tmem_wait_ld();
+                        for (int ch = 0; ch < D / 32; ++ch) {
+                            uint32_t o[32];
+                            tmem_ld32(tO + ch * 32, o);
+                            tmem_wait_ld();
 #pragma unroll
-                        for (int c = 0; c < 32; ++c)
-                            o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                        tmem_st32(tO + ch * 32, o);
+                            for (int c = 0; c < 32; ++c)
+                                o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                            tmem_st32(tO + ch * 32, o);
+                        }
                     }
+                    lt = emit_p();
                 }
+                l += lt;
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();

@@ -38,6 +38,7 @@ LONG = "b1h32n16384d128_causal"
 DECODE = "decode_b64h32nk8192d128"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
+LAUNCH_COVER_CYCLES = 400_000  # ~0.2 ms device-side spin before each timed step
 CPU_SAMPLE_SECONDS = 10.0
 BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
 
@@ -307,6 +308,7 @@ def run_case(args):
         launch()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(LAUNCH_COVER_CYCLES)
     e0.record()
     for _ in range(args.steps):
         launch()
@@ -350,6 +352,9 @@ def run_gpu(args):
 
     def step(ev):
         flush.zero_()
+        # keep the GPU busy while the host enqueues this step's launches, so the
+        # events below time the kernels and not host-side launch latency
+        torch.cuda._sleep(LAUNCH_COVER_CYCLES)
         ev[0].record(stream)
         binding.attn_fwd(q3, k3, v3, causal=True, scale=w3.scale, out=o3, lse=l3, stream=stream)
         ev[1].record(stream)
