@@ -53,6 +53,8 @@ def parse_args():
                     help="skip the oracle timing (for quick runs)")
     ap.add_argument("--case", default=None,
                     help="run only this workload's kernel(s) (profiling runs); prints its time")
+    ap.add_argument("--shape", default=None,
+                    help="with --case custom: B,H,Nq,Nk,d,causal of a profiling workload")
     a = ap.parse_args()
     a.warmup = max(3, a.warmup)
     a.steps = max(1, a.steps)
@@ -287,8 +289,13 @@ def run_case(args):
     import torch
 
     from attention_flashattention_fwd_gb300 import binding
-    from attention_flashattention_fwd_gb300.inputs import WORKLOADS, make_workload
-    w = WORKLOADS[args.case]
+    from attention_flashattention_fwd_gb300.inputs import WORKLOADS, Workload, make_workload
+    if args.case == "custom":
+        B, H, Nq, Nk, d, causal = (int(x) for x in args.shape.split(","))
+        w = Workload(f"b{B}h{H}q{Nq}k{Nk}d{d}{'_causal' if causal else ''}", B, H, Nq, Nk, d,
+                     bool(causal), seed=2000)
+    else:
+        w = WORKLOADS[args.case]
     binding.load()
     dev = torch.device("cuda", 0)
     q, k, v = make_workload(w, device=dev)
