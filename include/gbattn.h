@@ -16,7 +16,7 @@
  *   - Device pointers must be 16-byte aligned.  The caller owns every buffer;
  *     the library allocates nothing on any call.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Compute calls
- *     are asynchronous: GBATTN_OK means "enqueued".  Faults inside a kernel
+ *     are asynchronous: ATTN_OK means "enqueued".  Faults inside a kernel
  *     surface at the caller's next synchronisation, as in CUDA.
  *   - Arguments are validated on the host before anything is launched; a
  *     rejected call launches nothing and touches no buffer.
