@@ -16,6 +16,13 @@
  *   - CS336 Lecture 5 notes section 8.3 (FlashAttention forward): the
  *     logsumexp L_i = m_i + log l_i kept per row; causal masking drops keys
  *     "in the future" of the query (key j masked for j > i).
+ *   - PDC course Lecture 4, section 4.9 (the KV cache that grows during
+ *     inference): with Nq < Nk the Nq queries are read as the LAST Nq
+ *     positions of a sequence of Nk tokens whose keys and values are all
+ *     given, so query i sits at position i + (Nk - Nq) and sees keys
+ *     j <= i + (Nk - Nq).  With Nq == Nk this is the plain j > i rule.  A
+ *     causal call with Nq > Nk would leave rows with no visible key and is
+ *     rejected.
  *   - CS149 Lecture 9 notes concept 9 (blocked softmax): the two-block merge
  *     rule m = max(m1, m2), l = e^{m1-m} l1 + e^{m2-m} l2.
  *   - CS336 Lecture 5 notes section 8.2 (online softmax): the per-block update
@@ -73,7 +80,7 @@ static double load_elem(const void *p, size_t idx, int is_bf16)
 /*
  * Row i of head bh: materialise the score row S_i. (length Nk) and the
  * probability row P_i., then O_i = sum_j P_ij V_j and lse_i = m_i + ln l_i.
- * Masked keys (causal j > i) carry -inf and contribute e^{-inf} = 0.
+ * Masked keys (causal j > i + (Nk - Nq)) carry -inf and contribute e^{-inf} = 0.
  * `srow` is caller scratch of Nk doubles.
  */
 static void attention_row(const void *q, const void *k, const void *v, int is_bf16,
@@ -82,11 +89,12 @@ static void attention_row(const void *q, const void *k, const void *v, int is_bf
 {
     const size_t qbase = ((size_t)bh * (size_t)Nq + (size_t)i) * (size_t)d;
     const size_t kvbase = (size_t)bh * (size_t)Nk * (size_t)d;
+    const long pos = i + (Nk - Nq); /* position of query i in the sequence */
 
     /* S_ij = scale * sum_c Q_ic K_jc, masked entries -inf */
     double m = -INFINITY;
     for (long j = 0; j < Nk; ++j) {
-        if (causal && j > i) {
+        if (causal && j > pos) {
             srow[j] = -INFINITY;
             continue;
         }
@@ -129,7 +137,7 @@ ORACLE_ABI int oracle_attention(const void *q, const void *k, const void *v, int
                                 double *o, double *lse, long B, long H, long Nq, long Nk,
                                 long d, int causal, double scale)
 {
-    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || d <= 0)
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || d <= 0 || (causal && Nq > Nk))
         return -1;
     const long rows = B * H * Nq;
     int err = 0;
@@ -162,7 +170,7 @@ ORACLE_ABI int oracle_attention_rows(const void *q, const void *k, const void *v
                                      long B, long H, long Nq, long Nk, long d, int causal,
                                      double scale)
 {
-    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || d <= 0 || nrows < 0)
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || d <= 0 || nrows < 0 || (causal && Nq > Nk))
         return -1;
     for (long t = 0; t < nrows; ++t)
         if (rows[2 * t] < 0 || rows[2 * t] >= B * H || rows[2 * t + 1] < 0 ||
@@ -263,8 +271,10 @@ ORACLE_ABI int oracle_attention_blocked(const double *q, const double *k, const 
                                         long Nk, long d, int causal, double scale, long Br,
                                         long Bc)
 {
-    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || d <= 0 || Br <= 0 || Bc <= 0)
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || d <= 0 || Br <= 0 || Bc <= 0 ||
+        (causal && Nq > Nk))
         return -1;
+    const long off = Nk - Nq; /* query i sits at position i + off */
     double *S = (double *)malloc((size_t)Br * (size_t)Bc * sizeof(double));
     double *m = (double *)malloc((size_t)Br * sizeof(double));
     double *l = (double *)malloc((size_t)Br * sizeof(double));
@@ -286,7 +296,7 @@ ORACLE_ABI int oracle_attention_blocked(const double *q, const double *k, const 
                     acc[r * d + c] = 0.0;
             }
             for (long j0 = 0; j0 < Nk; j0 += Bc) {
-                if (causal && j0 > i0 + br - 1)
+                if (causal && j0 > i0 + br - 1 + off)
                     break; /* every key of this block is after every query row */
                 const long bc = (j0 + Bc <= Nk) ? Bc : Nk - j0;
                 for (long r = 0; r < br; ++r) {
@@ -295,7 +305,7 @@ ORACLE_ABI int oracle_attention_blocked(const double *q, const double *k, const 
                     for (long t = 0; t < bc; ++t) {
                         const long j = j0 + t;
                         double s = -INFINITY;
-                        if (!(causal && j > i)) {
+                        if (!(causal && j > i + off)) {
                             double dot = 0.0;
                             for (long c = 0; c < d; ++c)
                                 dot += qh[i * d + c] * kh[j * d + c];

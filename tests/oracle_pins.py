@@ -186,6 +186,14 @@ def pin_blocked_equals_unblocked(orc):
             ob, lb = orc.attention_blocked(q, k, v, causal=causal, block_q=br, block_k=bc)
             assert np.max(np.abs(ob - o)) <= 1e-13, (causal, br, bc)
             assert np.max(np.abs(lb - lse)) <= 1e-13, (causal, br, bc)
+    # fewer queries than keys (a chunk at the end of the sequence)
+    qc = q[:, :, 26:]
+    for causal in (False, True):
+        o, lse = orc.attention(qc, k, v, causal=causal)
+        for br, bc in ((1, 1), (7, 5), (16, 16), (4, 19)):
+            ob, lb = orc.attention_blocked(qc, k, v, causal=causal, block_q=br, block_k=bc)
+            assert np.max(np.abs(ob - o)) <= 1e-13, (causal, br, bc)
+            assert np.max(np.abs(lb - lse)) <= 1e-13, (causal, br, bc)
 
 
 def pin_merge_rule(orc):
@@ -212,7 +220,8 @@ def pin_bruteforce_fsum(orc):
     """Tiny shapes against a second implementation in pure Python with
     exactly-rounded sums (math.fsum)."""
     rng = np.random.default_rng(27)
-    for (n, m, d, causal) in ((1, 1, 1, False), (3, 5, 2, False), (6, 6, 3, True), (8, 8, 4, True)):
+    for (n, m, d, causal) in ((1, 1, 1, False), (3, 5, 2, False), (6, 6, 3, True), (8, 8, 4, True),
+                              (3, 7, 2, True), (1, 4, 3, True)):
         q = rng.standard_normal((1, 1, n, d))
         k = rng.standard_normal((1, 1, m, d))
         v = rng.standard_normal((1, 1, m, d))
@@ -220,7 +229,7 @@ def pin_bruteforce_fsum(orc):
         o, lse = orc.attention(q, k, v, causal=causal, scale=scale)
         for i in range(n):
             logits = [scale * math.fsum(q[0, 0, i, c] * k[0, 0, j, c] for c in range(d))
-                      for j in range(m) if not (causal and j > i)]
+                      for j in range(m) if not (causal and j > i + (m - n))]
             mx = max(logits)
             w = [math.exp(s - mx) for s in logits]
             tot = math.fsum(w)
@@ -228,6 +237,24 @@ def pin_bruteforce_fsum(orc):
             for c in range(d):
                 ref = math.fsum(w[j] * v[0, 0, j, c] for j in range(len(w))) / tot
                 assert abs(o[0, 0, i, c] - ref) <= 1e-14
+
+
+def pin_causal_chunk_is_suffix(orc):
+    """A KV cache that grows during inference (PDC L4 section 4.9): attending
+    with the last Nq queries of a sequence against all of its Nk keys gives
+    exactly the last Nq rows of causal attention over the whole sequence,
+    whatever the split (prefill in chunks = prefill at once; Nq = 1 is a decode
+    step, which sees every key)."""
+    B, H, n, d = 2, 2, 29, 8
+    q, k, v = _rand((B, H, n, d), 33), _rand((B, H, n, d), 34), _rand((B, H, n, d), 35)
+    o, lse = orc.attention(q, k, v, causal=True, scale=0.6)
+    for nq in (1, 5, 13, 28):
+        oc, lc = orc.attention(q[:, :, n - nq:], k, v, causal=True, scale=0.6)
+        assert np.array_equal(oc, o[:, :, n - nq:]), nq
+        assert np.array_equal(lc, lse[:, :, n - nq:]), nq
+    # the last row sees every key: a one-query causal call is the non-causal one
+    od, ld = orc.attention(q[:, :, n - 1:], k, v, causal=False, scale=0.6)
+    assert np.array_equal(od, o[:, :, n - 1:]) and np.array_equal(ld, lse[:, :, n - 1:])
 
 
 def pin_torch_crosscheck(orc):
@@ -288,6 +315,7 @@ ALL_PINS = [
     pin_blocked_equals_unblocked,
     pin_merge_rule,
     pin_bruteforce_fsum,
+    pin_causal_chunk_is_suffix,
     pin_torch_crosscheck,
     pin_bf16_widening,
     pin_rows_equal_full,

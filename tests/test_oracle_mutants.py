@@ -17,10 +17,11 @@ MUTANTS = [
     ("scale_dropped", "srow[j] = scale * dot;", "srow[j] = dot;"),
     ("exp_sign_flipped", "exp(srow[j] - m);", "exp(m - srow[j]);"),
     ("not_normalised", "srow[j] /= l;", "srow[j] /= 1.0;"),
-    ("causal_masks_diagonal", "if (causal && j > i) {\n            srow[j] = -INFINITY;",
-     "if (causal && j >= i) {\n            srow[j] = -INFINITY;"),
-    ("causal_mask_transposed", "if (causal && j > i) {\n            srow[j] = -INFINITY;",
-     "if (causal && j < i) {\n            srow[j] = -INFINITY;"),
+    ("causal_masks_diagonal", "if (causal && j > pos) {", "if (causal && j >= pos) {"),
+    ("causal_mask_transposed", "if (causal && j > pos) {", "if (causal && j < pos) {"),
+    ("causal_chunk_top_left", "const long pos = i + (Nk - Nq);", "const long pos = i;"),
+    ("causal_chunk_offset_sign", "const long pos = i + (Nk - Nq);",
+     "const long pos = i + (Nq - Nk);"),
     ("lse_without_max", "*lse_out = m + log(l);", "*lse_out = log(l);"),
     ("lse_base2", "*lse_out = m + log(l);", "*lse_out = m + log2(l);"),
     ("scores_use_v", "load_elem(k, kvbase + (size_t)j * (size_t)d + (size_t)c, is_bf16)",
@@ -30,7 +31,11 @@ MUTANTS = [
     ("merge_sign_flipped", "exp(m1 - m);", "exp(m - m1);"),
     ("blocked_no_o_rescale", "acc[r * d + c] = alpha * acc[r * d + c] + pv;",
      "acc[r * d + c] = acc[r * d + c] + pv;"),
-    ("blocked_skips_diagonal_block", "if (causal && j0 > i0 + br - 1)", "if (causal && j0 > i0)"),
+    ("blocked_skips_diagonal_block", "if (causal && j0 > i0 + br - 1 + off)",
+     "if (causal && j0 > i0 + off)"),
+    ("blocked_chunk_stops_early", "if (causal && j0 > i0 + br - 1 + off)",
+     "if (causal && j0 > i0 + br - 1)"),
+    ("blocked_chunk_top_left", "if (!(causal && j > i + off)) {", "if (!(causal && j > i)) {"),
     ("bf16_widening_shift", "(uint32_t)bits << 16;", "(uint32_t)bits << 15;"),
 ]
 
