@@ -88,9 +88,11 @@ def _check_inputs(q, k, v):
 
 def attention(q, k, v, causal=False, scale=None, stream=None):
     """O = softmax(scale Q K^T [+ causal mask]) V and the fp32 logsumexp,
-    through ``attn_fwd_decode`` for a single non-causal query row and
-    ``attn_fwd`` otherwise."""
-    if q.dim() == 4 and q.shape[2] == 1 and not causal:
+    through ``attn_fwd_decode`` for a single query row and ``attn_fwd``
+    otherwise.  A causal query block is the newest Nq tokens of the Nk-token
+    sequence (query i sees keys j <= i + Nk - Nq), so one causal query row
+    sees every key and is the decode step."""
+    if q.dim() == 4 and q.shape[2] == 1:
         return attn_fwd_decode(q, k, v, scale=scale, stream=stream)
     return attn_fwd(q, k, v, causal=causal, scale=scale, stream=stream)
 

@@ -27,7 +27,9 @@ int validate_fwd(const void* q, const void* k, const void* v, const void* o, con
     if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
-    if (causal && Nq != Nk) return ATTN_ERR_UNSUPPORTED;  // mask alignment undefined
+    if (causal && Nq > Nk) return ATTN_ERR_UNSUPPORTED;  // rows with no visible key
+    // query positions i + (Nk - Nq) and padded tile rows stay within int32
+    if (static_cast<long long>(Nq) + Nk + 512 > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
     const long long BH = static_cast<long long>(B) * H;
     // grid and TMA coordinate range: (b*H + h) and the CTA count fit in int32
     const long long pairs = (static_cast<long long>(Nq) + 255) / 256;
@@ -114,6 +116,7 @@ int enqueue_fwd(const void* q, const void* k, const void* v, void* o, float* lse
     p.BH = static_cast<int>(BH);
     p.num_pairs = (Nq + 255) / 256;
     p.causal = causal;
+    p.causal_off = causal ? Nk - Nq : 0;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
     return launch_prefill(d, tq, tk, tv, p, num_sms, stream);
 }

@@ -19,6 +19,7 @@ struct PrefillParams {
     int Nq, Nk, BH;
     int num_pairs;      // query-tile pairs per head: ceil(Nq / 256)
     int causal;
+    int causal_off;     // Nk - Nq when causal: query i sees keys j <= i + causal_off
     float scale_log2;   // scale * log2(e)
 };
 

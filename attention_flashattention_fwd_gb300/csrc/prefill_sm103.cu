@@ -112,9 +112,12 @@ __device__ __forceinline__ Item item_at(const PrefillParams& p, int idx) {
     }
     it.row0 = pair * 2 * kBM;
     const int n_kv_all = (p.Nk + kBN - 1) / kBN;
-    // key tiles each query tile visits (causal: up to and including its diagonal)
-    it.n_kv0 = p.causal ? min(n_kv_all, it.row0 / kBN + 1) : n_kv_all;
-    it.n_kv1 = p.causal ? min(n_kv_all, it.row0 / kBN + 2) : n_kv_all;
+    // key tiles each query tile visits (causal: up to the tile holding the last
+    // key its last row sees, key row0 + 127 + causal_off for tile 0); tile 1
+    // visits every tile tile 0 does, and at most one more
+    const int last0 = it.row0 + kBM - 1 + p.causal_off;
+    it.n_kv0 = p.causal ? min(n_kv_all, last0 / kBN + 1) : n_kv_all;
+    it.n_kv1 = p.causal ? min(n_kv_all, (last0 + kBM) / kBN + 1) : n_kv_all;
     return it;
 }
 
@@ -405,9 +408,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float* s = reinterpret_cast<float*>(sr);
                 const int key0 = j * kBN;
                 const bool ragged = key0 + kBN > p.Nk;
-                const bool diag = p.causal && (key0 + kBN - 1 > it.row0 + t * kBM);
+                const bool diag =
+                    p.causal && (key0 + kBN - 1 > it.row0 + t * kBM + p.causal_off);
                 if (ragged || diag) {
-                    const int lim = p.causal ? min(p.Nk - 1, row) : p.Nk - 1;  // last visible key
+                    // last visible key of this row
+                    const int lim = p.causal ? min(p.Nk - 1, row + p.causal_off) : p.Nk - 1;
 #pragma unroll
                     for (int c = 0; c < kBN; ++c)
                         if (key0 + c > lim) s[c] = -INFINITY;

@@ -39,7 +39,7 @@ typedef enum {
     ATTN_OK = 0,
     ATTN_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, non-finite or
                                   non-positive scale, too-small workspace */
-    ATTN_ERR_UNSUPPORTED = 2,  /* d not in {64, 128}; causal with Nq != Nk;
+    ATTN_ERR_UNSUPPORTED = 2,  /* d not in {64, 128}; causal with Nq > Nk;
                                   sizes beyond the index range of the kernels */
     ATTN_ERR_MISALIGNED = 3,   /* a device pointer is not 16-byte aligned */
     ATTN_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
@@ -53,17 +53,23 @@ typedef enum {
  *
  * Computes, for every (b, h) and query row i < Nq:
  *   s_ij   = scale * sum_c q[b,h,i,c] k[b,h,j,c]            for j < Nk
- *   s_ij   = -inf if causal and j > i                      (key j masked for j > i)
+ *   s_ij   = -inf if causal and j > i + (Nk - Nq)          (key j in the future of query i)
  *   o[b,h,i,:] = sum_j softmax_j(s_i.) v[b,h,j,:]          (bf16, round-to-nearest-even)
  *   lse[b,h,i] = log sum_j e^{s_ij}                          (fp32, natural log)
  * FlashAttention forward with the online softmax (CS336 Lecture 5 notes,
  * sections 8.2-8.3; CS149 Lecture 9 notes, concept 9); causal key blocks
  * wholly in the future of a query block are skipped.
+ * Causal with Nq < Nk: the queries are the newest Nq tokens of a sequence of
+ * Nk tokens whose keys and values are all given (chunked prefill against a
+ * KV cache, the cache that grows during inference of the PDC course
+ * Lecture 4, section 4.9), so query i sits at position i + (Nk - Nq).  With
+ * Nq == Nk this is the usual j > i mask; Nq > Nk would leave rows with no
+ * visible key and is rejected.
  *
  *   q, k, v  device, bf16, layouts above; read only.
  *   o        device, bf16 [B,H,Nq,d]; written.
  *   lse      device, fp32 [B,H,Nq]; written.  May not be NULL.
- *   B, H, Nq, Nk >= 1;  d in {64, 128};  causal in {0, 1} (causal needs Nq == Nk).
+ *   B, H, Nq, Nk >= 1;  d in {64, 128};  causal in {0, 1} (causal needs Nq <= Nk).
  *   scale    > 0 and finite; the usual value is 1/sqrt(d).
  *   stream   cudaStream_t.
  * Internal arithmetic: fp32 scores and accumulators on the tensor cores,

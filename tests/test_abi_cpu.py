@@ -59,7 +59,8 @@ def fwd(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=1, Nq=128, Nk=128,
     (dict(Nk=0), INVALID), (dict(scale=float("nan")), INVALID), (dict(scale=float("inf")), INVALID),
     (dict(scale=0.0), INVALID), (dict(scale=-1.0), INVALID), (dict(causal=2), INVALID),
     (dict(d=96), UNSUPPORTED), (dict(d=256), UNSUPPORTED), (dict(d=0), UNSUPPORTED),
-    (dict(causal=1, Nq=128, Nk=256), UNSUPPORTED),
+    (dict(causal=1, Nq=256, Nk=128), UNSUPPORTED),  # rows with no visible key
+    (dict(Nq=1 << 30, Nk=1 << 30), UNSUPPORTED),     # query positions beyond int32
     (dict(B=1 << 20, H=1 << 12), UNSUPPORTED),
     (dict(q=FAKE + 8), MISALIGNED), (dict(o=FAKE + 2), MISALIGNED), (dict(lse=FAKE + 4), MISALIGNED),
 ])
