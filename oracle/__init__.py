@@ -13,6 +13,10 @@ Functions (each follows a passage of the lecture pages, cited in the C file):
 * :func:`online_softmax_blocks` -- per-block online softmax (CS336 L5 8.2).
 * :func:`softmax_merge` -- two-block merge rule (CS149 L9 concept 9).
 * :func:`attention_blocked` -- tiled FlashAttention forward (CS336 L5 8.3).
+* :func:`attention_bwd` -- gradients dQ, dK, dV for an upstream dO (CS336 L5
+  8.4), with D_i taken from its definition sum_j P_ij dP_ij.
+* :func:`attention_bwd_dq_rows`, :func:`attention_bwd_dkdv_keys` -- the same on
+  listed query rows / key rows, for sampled checks of large problems.
 
 Inputs are numpy arrays, either float64 or bfloat16 bit patterns (uint16).
 """
@@ -41,6 +45,12 @@ def _declare(lib):
     lib.oracle_softmax_merge.restype = None
     lib.oracle_attention_blocked.argtypes = [P, P, P, P, P, L, L, L, L, L, I, D, L, L]
     lib.oracle_attention_blocked.restype = I
+    lib.oracle_attention_bwd.argtypes = [P, P, P, P, I, P, P, P, L, L, L, L, L, I, D]
+    lib.oracle_attention_bwd.restype = I
+    lib.oracle_attention_bwd_dq_rows.argtypes = [P, P, P, P, I, P, L, P, P, L, L, L, L, L, I, D]
+    lib.oracle_attention_bwd_dq_rows.restype = I
+    lib.oracle_attention_bwd_dkdv_keys.argtypes = [P, P, P, P, I, P, L, P, P, L, L, L, L, L, I, D]
+    lib.oracle_attention_bwd_dkdv_keys.restype = I
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = I
     return lib
@@ -57,12 +67,11 @@ def _ptr(a):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
-def _inputs(q, k, v):
-    q, k, v = (np.ascontiguousarray(x) for x in (q, k, v))
-    if q.dtype == np.uint16 and k.dtype == np.uint16 and v.dtype == np.uint16:
-        return q, k, v, 1
-    q, k, v = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v))
-    return q, k, v, 0
+def _inputs(*xs):
+    xs = tuple(np.ascontiguousarray(x) for x in xs)
+    if all(x.dtype == np.uint16 for x in xs):
+        return xs + (1,)
+    return tuple(np.ascontiguousarray(x, dtype=np.float64) for x in xs) + (0,)
 
 
 def attention(q, k, v, causal=False, scale=None):
@@ -147,3 +156,62 @@ def attention_blocked(q, k, v, causal=False, scale=None, block_q=128, block_k=12
 def threads_used() -> int:
     """Number of threads the oracle's row loops run on (1 without OpenMP)."""
     return int(_load().oracle_num_threads())
+
+
+def attention_bwd(q, k, v, dout, causal=False, scale=None):
+    """Gradients of naive attention for the upstream gradient ``dout``
+    ([B,H,Nq,d]).  Returns (dq [B,H,Nq,d], dk, dv [B,H,Nk,d]) in float64."""
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    q, k, v, dout, is_bf16 = _inputs(q, k, v, dout)
+    dq = np.empty((B, H, Nq, d), np.float64)
+    dk = np.empty((B, H, Nk, d), np.float64)
+    dv = np.empty((B, H, Nk, d), np.float64)
+    rc = _load().oracle_attention_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), is_bf16, _ptr(dq),
+                                      _ptr(dk), _ptr(dv), B, H, Nq, Nk, d,
+                                      int(bool(causal)), float(scale))
+    if rc != 0:
+        raise ValueError("oracle_attention_bwd rejected its arguments")
+    return dq, dk, dv
+
+
+def attention_bwd_dq_rows(q, k, v, dout, rows, causal=False, scale=None):
+    """dQ on rows ``rows`` ([n, 2] of (bh, i)).  Returns (dq [n, d], D [n])
+    with D_i = sum_j P_ij dP_ij."""
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    q, k, v, dout, is_bf16 = _inputs(q, k, v, dout)
+    rows = np.ascontiguousarray(rows, dtype=np.int64).reshape(-1, 2)
+    n = rows.shape[0]
+    dq = np.empty((n, d), np.float64)
+    D = np.empty((n,), np.float64)
+    rc = _load().oracle_attention_bwd_dq_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), is_bf16,
+                                              _ptr(rows), n, _ptr(dq), _ptr(D), B, H, Nq, Nk, d,
+                                              int(bool(causal)), float(scale))
+    if rc != 0:
+        raise ValueError("oracle_attention_bwd_dq_rows rejected its arguments")
+    return dq, D
+
+
+def attention_bwd_dkdv_keys(q, k, v, dout, keys, causal=False, scale=None):
+    """dK and dV on key rows ``keys`` ([n, 2] of (bh, j)).  Returns (dk, dv),
+    each [n, d]."""
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    q, k, v, dout, is_bf16 = _inputs(q, k, v, dout)
+    keys = np.ascontiguousarray(keys, dtype=np.int64).reshape(-1, 2)
+    n = keys.shape[0]
+    dk = np.empty((n, d), np.float64)
+    dv = np.empty((n, d), np.float64)
+    rc = _load().oracle_attention_bwd_dkdv_keys(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), is_bf16,
+                                                _ptr(keys), n, _ptr(dk), _ptr(dv), B, H, Nq, Nk,
+                                                d, int(bool(causal)), float(scale))
+    if rc != 0:
+        raise ValueError("oracle_attention_bwd_dkdv_keys rejected its arguments")
+    return dk, dv

@@ -346,3 +346,255 @@ ORACLE_ABI int oracle_attention_blocked(const double *q, const double *k, const 
     free(S); free(m); free(l); free(acc);
     return 0;
 }
+
+/* ---- FlashAttention backward (CS336 Lecture 5 notes, section 8.4) ------ */
+
+/*
+ * Gradients of O = softmax(S) V with S = scale Q K^T (masked as in the
+ * forward), for a given upstream gradient dO = dL/dO:
+ *     P_ij  = softmax_j(S_i.)             dV_j = sum_i P_ij dO_i
+ *     dP_ij = dO_i . V_j                  D_i  = sum_j P_ij dP_ij
+ *     dS_ij = P_ij (dP_ij - D_i)          dQ_i = scale sum_j dS_ij K_j
+ *                                         dK_j = scale sum_i dS_ij Q_i
+ * D_i is written from its definition (the derivative of the softmax), not
+ * from the shortcut rowsum(dO_i * O_i) the notes prove equal in exercise 9,
+ * so the tests can check that identity against it.  Inputs q, k, v, dout as
+ * in the forward (binary64 or bfloat16 bits), dout: [B,H,Nq,d].  Outputs are
+ * binary64.
+ */
+
+/*
+ * Row i of head bh: P_i. (normalised, masked entries 0) into prow, dP_i. into
+ * dprow (Nk entries each, dP of masked keys left 0), D_i into *D_out, lse_i
+ * into *lse_out.  `o_row` is caller scratch of d doubles.
+ */
+static void backward_row(const void *q, const void *k, const void *v, const void *dout,
+                         int is_bf16, long Nq, long Nk, long d, long bh, long i, int causal,
+                         double scale, double *prow, double *dprow, double *o_row,
+                         double *D_out, double *lse_out)
+{
+    attention_row(q, k, v, is_bf16, Nq, Nk, d, bh, i, causal, scale, prow, o_row, lse_out);
+    const size_t dobase = ((size_t)bh * (size_t)Nq + (size_t)i) * (size_t)d;
+    const size_t kvbase = (size_t)bh * (size_t)Nk * (size_t)d;
+    double D = 0.0;
+    for (long j = 0; j < Nk; ++j) {
+        dprow[j] = 0.0;
+        if (prow[j] == 0.0)
+            continue; /* masked (or underflowed): contributes nothing */
+        double dp = 0.0;
+        for (long c = 0; c < d; ++c)
+            dp += load_elem(dout, dobase + (size_t)c, is_bf16) *
+                  load_elem(v, kvbase + (size_t)j * (size_t)d + (size_t)c, is_bf16);
+        dprow[j] = dp;
+        D += prow[j] * dp;
+    }
+    *D_out = D;
+}
+
+/*
+ * Full backward over all heads.  dq: [B,H,Nq,d], dk, dv: [B,H,Nk,d].
+ * Heads run in parallel; inside a head the rows run in order, so the result
+ * does not depend on the thread count.  Returns 0 or -1.
+ */
+ORACLE_ABI int oracle_attention_bwd(const void *q, const void *k, const void *v,
+                                    const void *dout, int is_bf16, double *dq, double *dk,
+                                    double *dv, long B, long H, long Nq, long Nk, long d,
+                                    int causal, double scale)
+{
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || d <= 0 || (causal && Nq > Nk))
+        return -1;
+    int err = 0;
+#pragma omp parallel
+    {
+        double *prow = (double *)malloc((size_t)Nk * sizeof(double));
+        double *dprow = (double *)malloc((size_t)Nk * sizeof(double));
+        double *o_row = (double *)malloc((size_t)d * sizeof(double));
+        if (!prow || !dprow || !o_row) {
+#pragma omp atomic write
+            err = -1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (long bh = 0; bh < B * H; ++bh) {
+                double *dkh = dk + (size_t)bh * (size_t)Nk * (size_t)d;
+                double *dvh = dv + (size_t)bh * (size_t)Nk * (size_t)d;
+                for (size_t x = 0; x < (size_t)Nk * (size_t)d; ++x) {
+                    dkh[x] = 0.0;
+                    dvh[x] = 0.0;
+                }
+                const size_t kvbase = (size_t)bh * (size_t)Nk * (size_t)d;
+                for (long i = 0; i < Nq; ++i) {
+                    double D, lse;
+                    backward_row(q, k, v, dout, is_bf16, Nq, Nk, d, bh, i, causal, scale, prow,
+                                 dprow, o_row, &D, &lse);
+                    const size_t rbase = ((size_t)bh * (size_t)Nq + (size_t)i) * (size_t)d;
+                    double *dqi = dq + rbase;
+                    for (long c = 0; c < d; ++c)
+                        dqi[c] = 0.0;
+                    for (long j = 0; j < Nk; ++j) {
+                        const double p = prow[j];
+                        if (p == 0.0)
+                            continue;
+                        const double ds = p * (dprow[j] - D);
+                        for (long c = 0; c < d; ++c) {
+                            const double kjc = load_elem(k, kvbase + (size_t)j * (size_t)d + (size_t)c, is_bf16);
+                            const double qic = load_elem(q, rbase + (size_t)c, is_bf16);
+                            const double doic = load_elem(dout, rbase + (size_t)c, is_bf16);
+                            dqi[c] += scale * ds * kjc;
+                            dkh[(size_t)j * (size_t)d + (size_t)c] += scale * ds * qic;
+                            dvh[(size_t)j * (size_t)d + (size_t)c] += p * doic;
+                        }
+                    }
+                }
+            }
+        }
+        free(prow);
+        free(dprow);
+        free(o_row);
+    }
+    return err;
+}
+
+/*
+ * dQ on a list of rows (rows[2t] = bh, rows[2t+1] = i); dq: [nrows, d].
+ * Optionally the per-row D_i (D may be NULL), for the exercise-9 check.
+ */
+ORACLE_ABI int oracle_attention_bwd_dq_rows(const void *q, const void *k, const void *v,
+                                            const void *dout, int is_bf16, const long *rows,
+                                            long nrows, double *dq, double *D, long B, long H,
+                                            long Nq, long Nk, long d, int causal, double scale)
+{
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || d <= 0 || nrows < 0 || (causal && Nq > Nk))
+        return -1;
+    for (long t = 0; t < nrows; ++t)
+        if (rows[2 * t] < 0 || rows[2 * t] >= B * H || rows[2 * t + 1] < 0 ||
+            rows[2 * t + 1] >= Nq)
+            return -1;
+    int err = 0;
+#pragma omp parallel
+    {
+        double *prow = (double *)malloc((size_t)Nk * sizeof(double));
+        double *dprow = (double *)malloc((size_t)Nk * sizeof(double));
+        double *o_row = (double *)malloc((size_t)d * sizeof(double));
+        if (!prow || !dprow || !o_row) {
+#pragma omp atomic write
+            err = -1;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (long t = 0; t < nrows; ++t) {
+                const long bh = rows[2 * t], i = rows[2 * t + 1];
+                double Di, lse;
+                backward_row(q, k, v, dout, is_bf16, Nq, Nk, d, bh, i, causal, scale, prow,
+                             dprow, o_row, &Di, &lse);
+                if (D)
+                    D[t] = Di;
+                const size_t kvbase = (size_t)bh * (size_t)Nk * (size_t)d;
+                double *dqi = dq + (size_t)t * (size_t)d;
+                for (long c = 0; c < d; ++c)
+                    dqi[c] = 0.0;
+                for (long j = 0; j < Nk; ++j) {
+                    if (prow[j] == 0.0)
+                        continue;
+                    const double ds = prow[j] * (dprow[j] - Di);
+                    for (long c = 0; c < d; ++c)
+                        dqi[c] += scale * ds * load_elem(k, kvbase + (size_t)j * (size_t)d + (size_t)c, is_bf16);
+                }
+            }
+        }
+        free(prow);
+        free(dprow);
+        free(o_row);
+    }
+    return err;
+}
+
+/*
+ * dK and dV on a list of keys (keys[2t] = bh, keys[2t+1] = j); dk, dv:
+ * [nkeys, d].  For each head that appears, every row's lse_i and D_i are
+ * computed first (rows in parallel); then each listed key sums over the rows
+ * with P_ij = e^{S_ij - lse_i} recomputed from the logsumexp, the form the
+ * notes use in the backward pass (section 8.4).  Returns 0 or -1.
+ */
+ORACLE_ABI int oracle_attention_bwd_dkdv_keys(const void *q, const void *k, const void *v,
+                                              const void *dout, int is_bf16, const long *keys,
+                                              long nkeys, double *dk, double *dv, long B,
+                                              long H, long Nq, long Nk, long d, int causal,
+                                              double scale)
+{
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || d <= 0 || nkeys < 0 || (causal && Nq > Nk))
+        return -1;
+    for (long t = 0; t < nkeys; ++t)
+        if (keys[2 * t] < 0 || keys[2 * t] >= B * H || keys[2 * t + 1] < 0 ||
+            keys[2 * t + 1] >= Nk)
+            return -1;
+    double *lse = (double *)malloc((size_t)Nq * sizeof(double));
+    double *Dr = (double *)malloc((size_t)Nq * sizeof(double));
+    char *done = (char *)calloc((size_t)(nkeys > 0 ? nkeys : 1), 1);
+    if (!lse || !Dr || !done) {
+        free(lse); free(Dr); free(done);
+        return -1;
+    }
+    int err = 0;
+    for (long t0 = 0; t0 < nkeys && !err; ++t0) {
+        if (done[t0])
+            continue;
+        const long bh = keys[2 * t0];
+        /* pass 1: lse_i and D_i of every row of this head */
+#pragma omp parallel
+        {
+            double *prow = (double *)malloc((size_t)Nk * sizeof(double));
+            double *dprow = (double *)malloc((size_t)Nk * sizeof(double));
+            double *o_row = (double *)malloc((size_t)d * sizeof(double));
+            if (!prow || !dprow || !o_row) {
+#pragma omp atomic write
+                err = -1;
+            } else {
+#pragma omp for schedule(dynamic, 8)
+                for (long i = 0; i < Nq; ++i)
+                    backward_row(q, k, v, dout, is_bf16, Nq, Nk, d, bh, i, causal, scale, prow,
+                                 dprow, o_row, &Dr[i], &lse[i]);
+            }
+            free(prow);
+            free(dprow);
+            free(o_row);
+        }
+        if (err)
+            break;
+        /* pass 2: every listed key of this head */
+        const size_t kvbase = (size_t)bh * (size_t)Nk * (size_t)d;
+        const size_t qbase = (size_t)bh * (size_t)Nq * (size_t)d;
+#pragma omp parallel for schedule(dynamic, 1)
+        for (long t = t0; t < nkeys; ++t) {
+            if (keys[2 * t] != bh)
+                continue;
+            done[t] = 1;
+            const long j = keys[2 * t + 1];
+            double *dkj = dk + (size_t)t * (size_t)d;
+            double *dvj = dv + (size_t)t * (size_t)d;
+            for (long c = 0; c < d; ++c) {
+                dkj[c] = 0.0;
+                dvj[c] = 0.0;
+            }
+            for (long i = 0; i < Nq; ++i) {
+                if (causal && j > i + (Nk - Nq))
+                    continue;
+                double s = 0.0, dp = 0.0;
+                for (long c = 0; c < d; ++c) {
+                    const double vjc = load_elem(v, kvbase + (size_t)j * (size_t)d + (size_t)c, is_bf16);
+                    s += load_elem(q, qbase + (size_t)i * (size_t)d + (size_t)c, is_bf16) *
+                         load_elem(k, kvbase + (size_t)j * (size_t)d + (size_t)c, is_bf16);
+                    dp += load_elem(dout, qbase + (size_t)i * (size_t)d + (size_t)c, is_bf16) * vjc;
+                }
+                const double p = exp(scale * s - lse[i]);
+                const double ds = p * (dp - Dr[i]);
+                for (long c = 0; c < d; ++c) {
+                    dkj[c] += scale * ds * load_elem(q, qbase + (size_t)i * (size_t)d + (size_t)c, is_bf16);
+                    dvj[c] += p * load_elem(dout, qbase + (size_t)i * (size_t)d + (size_t)c, is_bf16);
+                }
+            }
+        }
+    }
+    free(lse);
+    free(Dr);
+    free(done);
+    return err;
+}

@@ -302,6 +302,96 @@ def pin_rows_equal_full(orc):
         assert lrow[t] == lse.reshape(B * H, n)[bh, i]
 
 
+# -- backward (CS336 L5 section 8.4) ------------------------------------------
+
+def _bwd_case(seed, B=1, H=2, nq=9, nk=13, d=6):
+    return (_rand((B, H, nq, d), seed), _rand((B, H, nk, d), seed + 1),
+            _rand((B, H, nk, d), seed + 2), _rand((B, H, nq, d), seed + 3))
+
+
+def pin_bwd_finite_differences(orc):
+    """The gradients are those of L = sum(O * dO) with O from the (separately
+    pinned) forward: central differences on single entries of Q, K and V."""
+    q, k, v, do = _bwd_case(40)
+    h = 1e-5
+    for causal in (False, True):
+        dq, dk, dv = orc.attention_bwd(q, k, v, do, causal=causal, scale=0.45)
+
+        def loss(qq, kk, vv):
+            o, _ = orc.attention(qq, kk, vv, causal=causal, scale=0.45)
+            return float(np.sum(o * do))
+
+        rng = np.random.default_rng(41)
+        for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+            for _ in range(6):
+                idx = tuple(int(rng.integers(n)) for n in x.shape)
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += h
+                xm[idx] -= h
+                args_p = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+                args_m = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+                fd = (loss(*args_p) - loss(*args_m)) / (2 * h)
+                assert abs(fd - g[idx]) <= 1e-7 * max(1.0, abs(fd)), (name, causal, idx, fd, g[idx])
+
+
+def pin_bwd_torch_autograd(orc):
+    """CS336 L5 section 8.4, demo 3: agreement with torch autograd in float64
+    (the page reports differences of order 1e-15)."""
+    import torch
+    q, k, v, do = _bwd_case(44, B=2, H=2, nq=10, nk=17, d=8)
+    for causal in (False, True):
+        dq, dk, dv = orc.attention_bwd(q, k, v, do, causal=causal, scale=0.3)
+        tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+        s = (tq @ tk.transpose(-1, -2)) * 0.3
+        if causal:  # the newest 10 of 17 tokens: query i sees keys j <= i + 7
+            vis = torch.ones(10, 17, dtype=torch.bool).tril(7)
+            s = s.masked_fill(~vis, float("-inf"))
+        (torch.softmax(s, dim=-1) @ tv).backward(torch.tensor(do))
+        for got, ref in ((dq, tq.grad), (dk, tk.grad), (dv, tv.grad)):
+            assert np.max(np.abs(got - ref.numpy())) <= 1e-13, causal
+
+
+def pin_bwd_exercise9_identity(orc):
+    """CS336 L5 exercise 9: D_i = sum_j P_ij dP_ij equals sum_k dO_ik O_ik."""
+    q, k, v, do = _bwd_case(48, nq=11, nk=11)
+    for causal in (False, True):
+        o, _ = orc.attention(q, k, v, causal=causal)
+        rows = np.array([[bh, i] for bh in range(2) for i in range(11)])
+        _, D = orc.attention_bwd_dq_rows(q, k, v, do, rows, causal=causal)
+        ref = np.sum(do * o, axis=-1).reshape(-1)
+        assert np.max(np.abs(D - ref)) <= 1e-13, causal
+
+
+def pin_bwd_invariants(orc):
+    """Softmax rows sum to one, so sum_j dS_ij = 0: the key gradients of a head
+    sum to zero, the value gradients sum to the sum of dO, and with all keys
+    equal the query gradient vanishes."""
+    q, k, v, do = _bwd_case(52)
+    for causal in (False, True):
+        dq, dk, dv = orc.attention_bwd(q, k, v, do, causal=causal)
+        assert np.max(np.abs(dk.sum(axis=2))) <= 1e-12, causal
+        assert np.max(np.abs(dv.sum(axis=2) - do.sum(axis=2))) <= 1e-12, causal
+        keq = np.broadcast_to(k[:, :, :1], k.shape).copy()
+        dq0, _, _ = orc.attention_bwd(q, keq, v, do, causal=causal)
+        assert np.max(np.abs(dq0)) <= 1e-12, causal
+
+
+def pin_bwd_rows_and_keys_equal_full(orc):
+    """The sampled entry points give the full backward's rows and keys."""
+    q, k, v, do = _bwd_case(56, B=2, H=1, nq=8, nk=12)
+    for causal in (False, True):
+        dq, dk, dv = orc.attention_bwd(q, k, v, do, causal=causal)
+        rows = np.array([[0, 0], [1, 7], [0, 3]])
+        dqr, _ = orc.attention_bwd_dq_rows(q, k, v, do, rows, causal=causal)
+        keys = np.array([[1, 0], [0, 11], [1, 5], [0, 4]])
+        dkk, dvk = orc.attention_bwd_dkdv_keys(q, k, v, do, keys, causal=causal)
+        for t, (bh, i) in enumerate(rows):
+            assert np.max(np.abs(dqr[t] - dq.reshape(2, 8, -1)[bh, i])) <= 1e-13
+        for t, (bh, j) in enumerate(keys):
+            assert np.max(np.abs(dkk[t] - dk.reshape(2, 12, -1)[bh, j])) <= 1e-13
+            assert np.max(np.abs(dvk[t] - dv.reshape(2, 12, -1)[bh, j])) <= 1e-13
+
+
 ALL_PINS = [
     pin_exercise8_online_softmax,
     pin_memory_table,
@@ -319,4 +409,9 @@ ALL_PINS = [
     pin_torch_crosscheck,
     pin_bf16_widening,
     pin_rows_equal_full,
+    pin_bwd_finite_differences,
+    pin_bwd_torch_autograd,
+    pin_bwd_exercise9_identity,
+    pin_bwd_invariants,
+    pin_bwd_rows_and_keys_equal_full,
 ]

@@ -24,8 +24,9 @@ MUTANTS = [
      "const long pos = i + (Nq - Nk);"),
     ("lse_without_max", "*lse_out = m + log(l);", "*lse_out = log(l);"),
     ("lse_base2", "*lse_out = m + log(l);", "*lse_out = m + log2(l);"),
-    ("scores_use_v", "load_elem(k, kvbase + (size_t)j * (size_t)d + (size_t)c, is_bf16)",
-     "load_elem(v, kvbase + (size_t)j * (size_t)d + (size_t)c, is_bf16)"),
+    ("scores_use_v", "is_bf16) *\n                   load_elem(k, kvbase",
+     "is_bf16) *\n                   load_elem(v, kvbase"),
+    ("bwd_dq_uses_v", "dqi[c] += scale * ds * load_elem(k,", "dqi[c] += scale * ds * load_elem(v,"),
     ("output_uses_k", "o_row[c] += srow[j] * load_elem(v,", "o_row[c] += srow[j] * load_elem(k,"),
     ("online_no_rescale", "l * exp(m - m_new)) + s;", "l) + s;"),
     ("merge_sign_flipped", "exp(m1 - m);", "exp(m - m1);"),
@@ -37,6 +38,17 @@ MUTANTS = [
      "if (causal && j0 > i0 + br - 1)"),
     ("blocked_chunk_top_left", "if (!(causal && j > i + off)) {", "if (!(causal && j > i)) {"),
     ("bf16_widening_shift", "(uint32_t)bits << 16;", "(uint32_t)bits << 15;"),
+    ("bwd_D_dropped", "const double ds = p * (dprow[j] - D);", "const double ds = p * dprow[j];"),
+    ("bwd_dq_no_scale", "dqi[c] += scale * ds * kjc;", "dqi[c] += ds * kjc;"),
+    ("bwd_dk_uses_k", "+= scale * ds * qic;", "+= scale * ds * kjc;"),
+    ("bwd_dv_uses_ds", "+= p * doic;", "+= ds * doic;"),
+    ("bwd_dp_uses_k", "is_bf16) *\n                  load_elem(v, kvbase",
+     "is_bf16) *\n                  load_elem(k, kvbase"),
+    ("bwd_rows_D_dropped", "prow[j] * (dprow[j] - Di);", "prow[j] * dprow[j];"),
+    ("bwd_keys_lse_sign", "exp(scale * s - lse[i]);", "exp(scale * s + lse[i]);"),
+    ("bwd_keys_top_left", "if (causal && j > i + (Nk - Nq))\n                    continue;",
+     "if (causal && j > i)\n                    continue;"),
+    ("bwd_keys_dv_uses_q", "dvj[c] += p * load_elem(dout,", "dvj[c] += p * load_elem(q,"),
 ]
 
 
