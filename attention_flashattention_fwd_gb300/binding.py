@@ -44,6 +44,10 @@ def load():
         lib.attn_fwd_decode.restype = I
         lib.attn_fwd_from_host.argtypes = [P] * 10 + [I, I, I, I, I, I, F, P]
         lib.attn_fwd_from_host.restype = I
+        lib.attn_bwd_workspace_bytes.argtypes = [I, I, I, I, I]
+        lib.attn_bwd_workspace_bytes.restype = S
+        lib.attn_bwd.argtypes = [P] * 9 + [I, I, I, I, I, I, F, P, S, P]
+        lib.attn_bwd.restype = I
         lib.attn_status_string.argtypes = [I]
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_device_error.argtypes = []
@@ -163,6 +167,42 @@ def attn_fwd_from_host(q, k, v, o, lse, dq, dk, dv, do_, dlse, causal=False, sca
                                    int(bool(causal)), float(scale), _stream_ptr(stream))
     _check(st, "attn_fwd_from_host")
     return o, lse
+
+
+def bwd_workspace_bytes(B, H, Nq, Nk, d) -> int:
+    return int(load().attn_bwd_workspace_bytes(B, H, Nq, Nk, d))
+
+
+def attn_bwd(q, k, v, o, lse, dout, causal=False, scale=None, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    """The C entry point ``attn_bwd``: gradients (dq, dk, dv) of attn_fwd for
+    the upstream gradient ``dout``, given the forward's inputs and its
+    outputs ``o`` and ``lse``.  ``workspace`` (a CUDA uint8 tensor) is
+    allocated here when not given."""
+    B, H, Nq, Nk, d = _check_inputs(q, k, v)
+    for name, t, dt in (("o", o, torch.bfloat16), ("dout", dout, torch.bfloat16),
+                        ("lse", lse, torch.float32)):
+        if not t.is_cuda or t.dtype != dt or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {dt} CUDA tensor")
+    if o.shape != q.shape or dout.shape != q.shape or lse.shape != (B, H, Nq):
+        raise ValueError("o and dout must be [B, H, Nq, d] and lse [B, H, Nq]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if dq is None:
+        dq = torch.empty_like(q)
+    if dk is None:
+        dk = torch.empty_like(k)
+    if dv is None:
+        dv = torch.empty_like(v)
+    need = bwd_workspace_bytes(B, H, Nq, Nk, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                         _ptr(dk), _ptr(dv), B, H, Nq, Nk, d, int(bool(causal)), float(scale),
+                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+                         _stream_ptr(stream))
+    _check(st, "attn_bwd")
+    return dq, dk, dv
 
 
 def device_error() -> int:

@@ -1,0 +1,583 @@
+// backward_sm103.cu -- FlashAttention backward for sm_103a.
+//
+// What it computes is the backward pass of the CS336 Lecture 5 notes,
+// section 8.4 (the FlashAttention-2 form): the forward stores no P; it is
+// recomputed as P_ij = e^{S_ij - L_i} from the logsumexp L, and with
+// D_i = rowsum(dO_i * O_i) (exercise 9 of the same notes)
+//     dV_j += P_ij^T dO_i,   dP_ij = dO_i V_j^T,   dS_ij = P_ij * (dP_ij - D_i),
+//     dQ_i += scale dS_ij K_j,   dK_j += scale dS_ij^T Q_i.
+//
+// Three kernels, in stream order:
+//   * prep: D_i and L_i log2(e) for every query row, padded to whole 128-row
+//     tiles (padded rows get D = 0 and L = +inf, so their P is 0), and a
+//     zeroed fp32 dQ accumulator;
+//   * main: one CTA per (b, h, 128-key tile j), key/value-outer as in the
+//     notes' FlashAttention-2 form.  K_j and V_j stay in shared memory; for
+//     every query tile i that can see the key tile, TMA brings Q_i and dO_i
+//     (two-stage ring) and tcgen05.mma computes, with one thread per key row
+//     (= one Tensor Memory lane) in the softmax warpgroup:
+//         S^T = K_j Q_i^T,  dP^T = V_j dO_i^T            (into Tensor Memory)
+//         P^T = 2^{S^T c - L log2 e},  dS^T = P^T (dP^T - D)   (registers)
+//         dV_j += P^T dO_i,  dK_j += dS^T Q_i              (A operand in TMEM)
+//         dQ_i  = dS K_j                                   (A = dS in shared memory)
+//     and a second warpgroup adds dQ_i into the fp32 accumulator;
+//   * convert: dQ = scale * accumulator, rounded to bf16.
+// Working transposed (a thread owns a key row) keeps the dV and dK products'
+// A operands in Tensor Memory and makes the row statistics L_i and D_i
+// per-column values that every thread reads at the same address.
+#include <cuda_bf16.h>
+#include <cuda.h>
+
+#include "gbattn_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace gbattn {
+
+__device__ unsigned int g_bwd_error = 0;
+
+namespace {
+
+constexpr int kTile = 128;       // keys per CTA, queries per step
+constexpr int kThreads = 320;    // warps 0-3 key rows, 4-7 dQ rows, 8 MMA, 9 TMA
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+
+template <int D>
+struct BCfg {
+    static constexpr int kSub = D / 64;               // 128-byte swizzle atoms along d
+    static constexpr int kSubBytes = 128 * 128;       // one atom column: 128 rows x 128 B
+    static constexpr int kTileBytes = kTile * D * 2;  // a 128-row bf16 tile of K, V, Q or dO
+    static constexpr int kKOff = 0;
+    static constexpr int kVOff = kTileBytes;
+    static constexpr int kRingOff = 2 * kTileBytes;   // stage s: Q_i, then dO_i
+    static constexpr int kDsOff = kRingOff + 4 * kTileBytes;  // dS, 128 keys x 128 queries bf16
+    static constexpr int kBarOff = kDsOff + 2 * kSubBytes;
+    static constexpr int kNumBars = 10;
+    static constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
+    static constexpr int kAbortOff = kTmemSlotOff + 4;
+    static constexpr int kSmemBytes = kAbortOff + 4 + 1024;  // + alignment slack
+    // Tensor Memory columns.  S^T is overwritten by P^T (bf16 pairs, first 64
+    // columns) and, once the dV product has read P^T, by the dQ_i product.
+    static constexpr uint32_t kColS = 0;
+    static constexpr uint32_t kColDP = 128;  // dP^T, then dS^T (bf16 pairs, first 64 columns)
+    static constexpr uint32_t kColDV = 256;
+    static constexpr uint32_t kColDK = 256 + D;
+};
+static_assert(BCfg<128>::kSmemBytes <= 232448, "shared memory of one CTA");
+
+struct BBars {
+    uint32_t base;
+    __device__ uint32_t kv_full() const { return base; }
+    __device__ uint32_t q_full(int s) const { return base + 8u * (1 + s); }
+    __device__ uint32_t q_empty(int s) const { return base + 8u * (3 + s); }
+    __device__ uint32_t s_full() const { return base + 8u * 5; }
+    __device__ uint32_t p_ready() const { return base + 8u * 6; }
+    __device__ uint32_t dq_full() const { return base + 8u * 7; }
+    __device__ uint32_t dq_free() const { return base + 8u * 8; }
+    __device__ uint32_t done() const { return base + 8u * 9; }
+};
+
+__device__ __forceinline__ void flag_abort(volatile int* abort_flag) {
+    *abort_flag = 1;
+    atomicOr(&g_bwd_error, kErrTimeout);
+}
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
+                                              volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0u) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                flag_abort(abort_flag);
+                return false;
+            }
+        }
+    }
+}
+
+// Wait for this thread's Tensor Memory loads into `a` and `b`; the registers
+// are tied to the wait so no use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld_into(uint32_t (&a)[32], uint32_t (&b)[32]) {
+    asm volatile(
+        "tcgen05.wait::ld.sync.aligned;"
+        : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]),
+          "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]),
+          "+r"(a[13]), "+r"(a[14]), "+r"(a[15]), "+r"(a[16]), "+r"(a[17]), "+r"(a[18]),
+          "+r"(a[19]), "+r"(a[20]), "+r"(a[21]), "+r"(a[22]), "+r"(a[23]), "+r"(a[24]),
+          "+r"(a[25]), "+r"(a[26]), "+r"(a[27]), "+r"(a[28]), "+r"(a[29]), "+r"(a[30]),
+          "+r"(a[31]), "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]),
+          "+r"(b[6]), "+r"(b[7]), "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]),
+          "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15]), "+r"(b[16]), "+r"(b[17]),
+          "+r"(b[18]), "+r"(b[19]), "+r"(b[20]), "+r"(b[21]), "+r"(b[22]), "+r"(b[23]),
+          "+r"(b[24]), "+r"(b[25]), "+r"(b[26]), "+r"(b[27]), "+r"(b[28]), "+r"(b[29]),
+          "+r"(b[30]), "+r"(b[31])
+        :
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld_into(uint32_t (&a)[32]) {
+    asm volatile(
+        "tcgen05.wait::ld.sync.aligned;"
+        : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]),
+          "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]),
+          "+r"(a[13]), "+r"(a[14]), "+r"(a[15]), "+r"(a[16]), "+r"(a[17]), "+r"(a[18]),
+          "+r"(a[19]), "+r"(a[20]), "+r"(a[21]), "+r"(a[22]), "+r"(a[23]), "+r"(a[24]),
+          "+r"(a[25]), "+r"(a[26]), "+r"(a[27]), "+r"(a[28]), "+r"(a[29]), "+r"(a[30]),
+          "+r"(a[31])
+        :
+        : "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the
+// tensor core (async proxy).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Instruction descriptor with A in MN-major (transposed) layout as well.
+constexpr uint32_t idesc_bf16_a_mn(uint32_t M, uint32_t N) {
+    return umma_idesc_bf16(M, N, true) | (1u << 15);
+}
+
+__device__ __forceinline__ uint4 bf16x8(const float* x) {
+    return make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                      pack_bf16x2(x[6], x[7]));
+}
+
+}  // namespace
+
+// ----------------------------------------------------------------- prep kernel
+//
+// Row i of head bh (i < Nq_pad): D_i = sum_c dO_ic O_ic in fp32 and
+// L2_i = lse_i log2(e); rows i >= Nq get D = 0 and L2 = +inf.  The fp32 dQ
+// accumulator row is zeroed.  D / 8 consecutive threads share a row (16-byte
+// loads); the trip count is rounded up to whole warps so the row sum's
+// shuffles always see the full warp.
+template <int D>
+__global__ void __launch_bounds__(256) attn_bwd_prep_kernel(BwdPrepParams a) {
+    constexpr int kLanes = D / 8;
+    const long long total = a.rows * kLanes;
+    const long long padded = (total + 31) / 32 * 32;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < padded;
+         g += stride) {
+        const bool valid = g < total;
+        const long long row = g / kLanes;
+        const int c = static_cast<int>(g % kLanes);
+        const long long bh = row / a.Nq_pad;
+        const int i = static_cast<int>(row % a.Nq_pad);
+        float acc = 0.f;
+        if (valid && i < a.Nq) {
+            const size_t off = (static_cast<size_t>(bh) * a.Nq + i) * D + c * 8;
+            const uint4 ov = *reinterpret_cast<const uint4*>(a.o + off);
+            const uint4 dv = *reinterpret_cast<const uint4*>(a.dout + off);
+            const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+            const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const float2 of = __bfloat1622float2(o2[t]);
+                const float2 df = __bfloat1622float2(d2[t]);
+                acc = fmaf(of.x, df.x, acc);
+                acc = fmaf(of.y, df.y, acc);
+            }
+        }
+#pragma unroll
+        for (int sh = kLanes / 2; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
+        if (valid) {
+            float4* z = reinterpret_cast<float4*>(a.dq_acc + row * D + c * 8);
+            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (c == 0) {
+                a.Dd[row] = acc;
+                a.lse2[row] = i < a.Nq
+                                  ? a.lse[static_cast<size_t>(bh) * a.Nq + i] * 1.4426950408889634f
+                                  : INFINITY;
+            }
+        }
+    }
+}
+
+// ----------------------------------------------------------------- main kernel
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_do, BwdParams p) {
+    using C = BCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle pattern
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t sK = sbase + C::kKOff;
+    const uint32_t sV = sbase + C::kVOff;
+    const uint32_t sRing = sbase + C::kRingOff;
+    const uint32_t sDs = sbase + C::kDsOff;
+    const BBars bars{sbase + C::kBarOff};
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kTmemSlotOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // Work item: key tile j of head bh, most query tiles (lowest j under a
+    // causal mask) first.  Key tile j is seen by query q iff some key k of
+    // it has k <= q + causal_off, i.e. from query tile (kj0 - off) / 128 on.
+    const int j = static_cast<int>(blockIdx.x) / p.BH;
+    const int bh = static_cast<int>(blockIdx.x) % p.BH;
+    const int kj0 = j * kTile;
+    const int n_qt = p.Nq_pad / kTile;
+    int i_first = 0;
+    if (p.causal) {
+        const int f = kj0 - p.causal_off;
+        i_first = f > 0 ? f / kTile : 0;
+    }
+    const int n_iter = n_qt - i_first;  // >= 1: the last query sees every key
+
+    // ---- set-up: barriers (one thread), Tensor Memory (warp 0)
+    if (threadIdx.x == kLoadWarp * 32) {
+        mbar_init(bars.kv_full(), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bars.q_full(s), 1);
+            mbar_init(bars.q_empty(s), 1);
+        }
+        mbar_init(bars.s_full(), 1);
+        mbar_init(bars.p_ready(), 4);  // one arrival per key-row warp
+        mbar_init(bars.dq_full(), 1);
+        mbar_init(bars.dq_free(), 4);  // one arrival per dQ warp
+        mbar_init(bars.done(), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) tmem_alloc<kTmemCols>(smem_addr(tmem_slot));
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kLoadWarp) {
+        // ===================================================== TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            prefetch_tmap(&tm_do);
+            mbar_arrive_expect_tx(bars.kv_full(), 2 * C::kTileBytes);
+            for (int s = 0; s < C::kSub; ++s) {
+                tma_load_3d(sK + s * C::kSubBytes, &tm_k, bars.kv_full(), s * 64, kj0, bh);
+                tma_load_3d(sV + s * C::kSubBytes, &tm_v, bars.kv_full(), s * 64, kj0, bh);
+            }
+            bool ok = true;
+            int issued = 0;
+            for (int it = 0; it < n_iter; ++it) {
+                const int s = it & 1;
+                // the stage's previous tiles (step it - 2) have been read by their last product
+                if (it >= 2 &&
+                    !(ok = wait_or_abort(bars.q_empty(s), ((it >> 1) - 1) & 1, abort_flag)))
+                    break;
+                mbar_arrive_expect_tx(bars.q_full(s), 2 * C::kTileBytes);
+                const uint32_t dst = sRing + s * 2 * C::kTileBytes;
+                const int y = (i_first + it) * kTile;
+                for (int sub = 0; sub < C::kSub; ++sub) {
+                    tma_load_3d(dst + sub * C::kSubBytes, &tm_q, bars.q_full(s), sub * 64, y, bh);
+                    tma_load_3d(dst + C::kTileBytes + sub * C::kSubBytes, &tm_do, bars.q_full(s),
+                                sub * 64, y, bh);
+                }
+                ++issued;
+            }
+            if (!ok) {
+                // drain: every copy in flight must land before the CTA exits
+                mbar_wait(bars.kv_full(), 0);
+                for (int it = max(0, issued - 2); it < issued; ++it)
+                    mbar_wait(bars.q_full(it & 1), (it >> 1) & 1);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // ===================================================== MMA issuer
+        // Per step i (stage s):  S^T, dP^T -> s_full;  wait P^T, dS^T;
+        // dV += P^T dO_i, dK += dS^T Q_i -> q_empty(s);  dQ_i = dS K_j -> dq_full.
+        // dQ_i lands in the S^T columns after the dV product has read P^T from
+        // them (one thread's MMAs run in issue order), so the next step's S^T
+        // waits until the dQ warpgroup has read dQ_i (dq_free).
+        if (lane == 0) {
+            const uint32_t id_s = umma_idesc_bf16(kTile, kTile, false);  // both K-major
+            const uint32_t id_acc = umma_idesc_bf16(kTile, D, true);     // B MN-major
+            const uint32_t id_dq = idesc_bf16_a_mn(kTile, D);            // A and B MN-major
+            const uint64_t dk_k = umma_desc_sw128(sK, 16, 1024);
+            const uint64_t dv_k = umma_desc_sw128(sV, 16, 1024);
+            const uint64_t dk_mn = umma_desc_sw128(sK, C::kSubBytes, 1024);
+            const uint64_t dds_mn = umma_desc_sw128(sDs, C::kSubBytes, 1024);
+            bool ok = wait_or_abort(bars.kv_full(), 0, abort_flag);
+            for (int it = 0; it < n_iter && ok; ++it) {
+                const int s = it & 1;
+                if (!(ok = wait_or_abort(bars.q_full(s), (it >> 1) & 1, abort_flag))) break;
+                if (it > 0 && !(ok = wait_or_abort(bars.dq_free(), (it - 1) & 1, abort_flag)))
+                    break;
+                tc_fence_after();
+                const uint32_t sq = sRing + s * 2 * C::kTileBytes;
+                const uint32_t sdo = sq + C::kTileBytes;
+                const uint64_t dq_k = umma_desc_sw128(sq, 16, 1024);
+                const uint64_t ddo_k = umma_desc_sw128(sdo, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {  // K = d in steps of 16
+                    const uint32_t off = ((kk >> 2) * C::kSubBytes + (kk & 3) * 32) >> 4;
+                    umma_ss(tmem + C::kColS, dk_k + off, dq_k + off, id_s, kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk >> 2) * C::kSubBytes + (kk & 3) * 32) >> 4;
+                    umma_ss(tmem + C::kColDP, dv_k + off, ddo_k + off, id_s, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(bars.s_full());
+                if (!(ok = wait_or_abort(bars.p_ready(), it & 1, abort_flag))) break;
+                tc_fence_after();
+                const uint64_t dq_mn = umma_desc_sw128(sq, C::kSubBytes, 1024);
+                const uint64_t ddo_mn = umma_desc_sw128(sdo, C::kSubBytes, 1024);
+                // K = 128 queries in steps of 16: 8 packed P / dS columns, 16 rows of 128 B
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    umma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8, ddo_mn + ((kk * 2048) >> 4),
+                            id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    umma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8, dq_mn + ((kk * 2048) >> 4),
+                            id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(bars.q_empty(s));
+                // K = 128 keys in steps of 16 rows of the dS and K_j tiles
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    umma_ss(tmem + C::kColS, dds_mn + ((kk * 2048) >> 4), dk_mn + ((kk * 2048) >> 4),
+                            id_dq, kk > 0 ? 1u : 0u);
+                umma_commit(bars.dq_full());
+            }
+            // every MMA this thread issued has completed once `done` flips
+            umma_commit(bars.done());
+            mbar_wait(bars.done(), 0);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ===================================================== key rows: P^T, dS^T
+        const int r = warp * 32 + lane;  // key row within the tile = TMEM lane
+        const int key = kj0 + r;
+        const bool key_ok = key < p.Nk;
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t tS = tmem + lane_off + C::kColS;
+        const uint32_t tDP = tmem + lane_off + C::kColDP;
+        const float cl2 = p.scale_log2;
+        const float* lse2_h = p.lse2 + static_cast<size_t>(bh) * p.Nq_pad;
+        const float* D_h = p.Dd + static_cast<size_t>(bh) * p.Nq_pad;
+        const int first_vis = key - p.causal_off;  // causal: query q sees this key iff q >= first_vis
+        bool ok = true;
+        for (int it = 0; it < n_iter; ++it) {
+            // S^T(it) was issued after dQ_{it-1} had been read, so the dS tile in
+            // shared memory (read by that product) is free as well
+            ok = wait_or_abort(bars.s_full(), it & 1, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const int i0 = (i_first + it) * kTile;
+            const bool diag = p.causal && (kj0 + kTile - 1 > i0 + p.causal_off);
+#pragma unroll 1
+            for (int ch = 0; ch < 4; ++ch) {  // 32 queries at a time
+                uint32_t sr[32], dr[32];
+                tmem_ld32(tS + ch * 32, sr);
+                tmem_ld32(tDP + ch * 32, dr);
+                // L2 and D of these 32 queries: the same address in every lane
+                float lq[32], dq[32];
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    const float4 l4 = __ldg(reinterpret_cast<const float4*>(lse2_h + i0 + ch * 32) + x);
+                    const float4 d4 = __ldg(reinterpret_cast<const float4*>(D_h + i0 + ch * 32) + x);
+                    lq[4 * x] = l4.x; lq[4 * x + 1] = l4.y; lq[4 * x + 2] = l4.z; lq[4 * x + 3] = l4.w;
+                    dq[4 * x] = d4.x; dq[4 * x + 1] = d4.y; dq[4 * x + 2] = d4.z; dq[4 * x + 3] = d4.w;
+                }
+                tmem_wait_ld_into(sr, dr);
+                uint32_t pk[16], dk[16];
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    float pv[2], dsv[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int q = i0 + ch * 32 + c + e;
+                        float pe = ex2_approx(fmaf(__uint_as_float(sr[c + e]), cl2, -lq[c + e]));
+                        if (!key_ok || (diag && q < first_vis)) pe = 0.f;
+                        pv[e] = pe;
+                        dsv[e] = pe * (__uint_as_float(dr[c + e]) - dq[c + e]);
+                    }
+                    pk[c / 2] = pack_bf16x2(pv[0], pv[1]);
+                    dk[c / 2] = pack_bf16x2(dsv[0], dsv[1]);
+                }
+                // P^T and dS^T over the first 64 columns of S^T and dP^T: packed
+                // column ch*16.. lies below the fp32 columns still to be read
+                tmem_st16(tS + ch * 16, pk);
+                tmem_st16(tDP + ch * 16, dk);
+                // dS as the MN-major A operand of dQ_i = dS K_j: row r of 128
+                // queries, two 64-query halves 16 KB apart, 16-byte chunks
+                // permuted by the 128-byte swizzle (chunk ^ (row % 8))
+                uint8_t* row = smem + C::kDsOff + (ch >> 1) * C::kSubBytes + r * 128;
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const int chunk = ((ch & 1) * 4 + x) ^ (r & 7);
+                    *reinterpret_cast<uint4*>(row + chunk * 16) =
+                        make_uint4(dk[4 * x], dk[4 * x + 1], dk[4 * x + 2], dk[4 * x + 3]);
+                }
+            }
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.p_ready());
+        }
+        // ---- epilogue: dV_j and dK_j rows (dK scaled), bf16
+        if (ok) {
+            ok = wait_or_abort(bars.done(), 0, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok) {
+            tc_fence_after();
+            const size_t row_off = (static_cast<size_t>(bh) * p.Nk + key) * D;
+#pragma unroll 1
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t col = which ? C::kColDK : C::kColDV;
+                const float mul = which ? p.scale : 1.f;
+                __nv_bfloat16* out = (which ? p.dk : p.dv) + row_off;
+#pragma unroll 1
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_off + col + ch * 32, v);
+                    tmem_wait_ld_into(v);
+                    if (key_ok) {
+                        float f[32];
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) f[c] = __uint_as_float(v[c]) * mul;
+                        uint4* dst = reinterpret_cast<uint4*>(out + ch * 32);
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) dst[x] = bf16x8(f + 8 * x);
+                    }
+                }
+            }
+        }
+    } else if (warp < 8) {
+        // ===================================================== query rows: dQ_i
+        const int wq = warp - 4;
+        const int r = wq * 32 + lane;  // query row within the tile = TMEM lane
+        const uint32_t tQ = tmem + (static_cast<uint32_t>(wq * 32) << 16) + C::kColS;
+        bool ok = true;
+        for (int it = 0; it < n_iter; ++it) {
+            ok = wait_or_abort(bars.dq_full(), it & 1, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const int q = (i_first + it) * kTile + r;
+            float* dst = p.dq_acc + (static_cast<size_t>(bh) * p.Nq_pad + q) * D;
+#pragma unroll 1
+            for (int ch = 0; ch < D / 32; ++ch) {
+                uint32_t v[32];
+                tmem_ld32(tQ + ch * 32, v);
+                tmem_wait_ld_into(v);
+                if (q < p.Nq) {
+                    float4* d4 = reinterpret_cast<float4*>(dst + ch * 32);
+#pragma unroll
+                    for (int x = 0; x < 8; ++x)
+                        atomicAdd(d4 + x, make_float4(__uint_as_float(v[4 * x]),
+                                                      __uint_as_float(v[4 * x + 1]),
+                                                      __uint_as_float(v[4 * x + 2]),
+                                                      __uint_as_float(v[4 * x + 3])));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.dq_free());
+        }
+    }
+
+    // ---- teardown: all Tensor Memory traffic is complete; free the columns
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc<kTmemCols>(tmem);
+}
+
+// ----------------------------------------------------------------- convert kernel
+//
+// dQ = scale * accumulator, rounded to bf16; eight elements per thread.
+template <int D>
+__global__ void __launch_bounds__(256) attn_bwd_dq_kernel(const float* __restrict__ dq_acc,
+                                                          __nv_bfloat16* __restrict__ dq,
+                                                          float scale, int Nq, int Nq_pad,
+                                                          long long n8) {
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < n8;
+         g += stride) {
+        const long long e = g * 8;
+        const long long row = e / D;  // b*H*Nq + ... in the unpadded layout
+        const int col = static_cast<int>(e % D);
+        const long long bh = row / Nq;
+        const int i = static_cast<int>(row % Nq);
+        const float4* src =
+            reinterpret_cast<const float4*>(dq_acc + (static_cast<size_t>(bh) * Nq_pad + i) * D + col);
+        const float4 a = src[0], b = src[1];
+        const float f[8] = {a.x * scale, a.y * scale, a.z * scale, a.w * scale,
+                            b.x * scale, b.y * scale, b.z * scale, b.w * scale};
+        *reinterpret_cast<uint4*>(dq + e) = bf16x8(f);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+int bwd_set_attributes() {
+    if (cudaFuncSetAttribute(attn_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             BCfg<128>::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             BCfg<64>::kSmemBytes) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+size_t bwd_workspace_bytes(long long BH, int Nq, int d) {
+    const long long nq_pad = (static_cast<long long>(Nq) + kTile - 1) / kTile * kTile;
+    return static_cast<size_t>(BH * nq_pad) * static_cast<size_t>(d + 2) * sizeof(float);
+}
+
+template <int D>
+static int launch_backward_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const CUtensorMap& tdo, const BwdPrepParams& a, const BwdParams& p,
+                             __nv_bfloat16* dq, int num_sms, cudaStream_t stream) {
+    const long long prep_threads = (a.rows * (D / 8) + 31) / 32 * 32;
+    long long prep_blocks = (prep_threads + 255) / 256;
+    if (prep_blocks > 8LL * num_sms) prep_blocks = 8LL * num_sms;
+    attn_bwd_prep_kernel<D><<<static_cast<unsigned>(prep_blocks), 256, 0, stream>>>(a);
+    const long long grid = static_cast<long long>(p.n_kt) * p.BH;
+    attn_bwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, BCfg<D>::kSmemBytes, stream>>>(
+        tq, tk, tv, tdo, p);
+    const long long n8 = static_cast<long long>(p.BH) * p.Nq * D / 8;
+    long long cblocks = (n8 + 255) / 256;
+    if (cblocks > 8LL * num_sms) cblocks = 8LL * num_sms;
+    attn_bwd_dq_kernel<D><<<static_cast<unsigned>(cblocks), 256, 0, stream>>>(
+        p.dq_acc, dq, p.scale, p.Nq, p.Nq_pad, n8);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int launch_backward(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                    const CUtensorMap& tdo, const BwdPrepParams& a, const BwdParams& p,
+                    __nv_bfloat16* dq, int num_sms, cudaStream_t stream) {
+    return d == 128 ? launch_backward_d<128>(tq, tk, tv, tdo, a, p, dq, num_sms, stream)
+                    : launch_backward_d<64>(tq, tk, tv, tdo, a, p, dq, num_sms, stream);
+}
+
+unsigned read_and_clear_bwd_error() {
+    unsigned v = 0, zero = 0;
+    cudaMemcpyFromSymbol(&v, g_bwd_error, sizeof v);
+    cudaMemcpyToSymbol(g_bwd_error, &zero, sizeof zero);
+    return v;
+}
+
+}  // namespace gbattn

@@ -52,6 +52,7 @@ void init_once() {
     }
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     g_init_status = prefill_set_attributes();
+    if (g_init_status == ATTN_OK) g_init_status = bwd_set_attributes();
 }
 
 int ensure_init() {
@@ -119,6 +120,50 @@ int enqueue_fwd(const void* q, const void* k, const void* v, void* o, float* lse
     p.causal_off = causal ? Nk - Nq : 0;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
     return launch_prefill(d, tq, tk, tv, p, num_sms, stream);
+}
+
+int enqueue_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                const float* lse, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk,
+                int d, int causal, float scale, void* workspace, cudaStream_t stream) {
+    int st = ensure_init();
+    if (st != ATTN_OK) return st;
+    int num_sms = 0;
+    if ((st = current_sm_count(&num_sms)) != ATTN_OK) return st;
+    const long long BH = static_cast<long long>(B) * H;
+    CUtensorMap tq, tk, tv, tdo;
+    if ((st = encode_bhnd(&tq, q, BH, Nq, d)) != ATTN_OK) return st;
+    if ((st = encode_bhnd(&tk, k, BH, Nk, d)) != ATTN_OK) return st;
+    if ((st = encode_bhnd(&tv, v, BH, Nk, d)) != ATTN_OK) return st;
+    if ((st = encode_bhnd(&tdo, dout, BH, Nq, d)) != ATTN_OK) return st;
+    const int nq_pad = (Nq + 127) / 128 * 128;
+    float* ws = static_cast<float*>(workspace);
+    BwdPrepParams a;
+    a.o = static_cast<const __nv_bfloat16*>(o);
+    a.dout = static_cast<const __nv_bfloat16*>(dout);
+    a.lse = lse;
+    a.dq_acc = ws;
+    a.lse2 = ws + BH * nq_pad * d;
+    a.Dd = a.lse2 + BH * nq_pad;
+    a.rows = BH * nq_pad;
+    a.Nq = Nq;
+    a.Nq_pad = nq_pad;
+    BwdParams p;
+    p.dk = static_cast<__nv_bfloat16*>(dk);
+    p.dv = static_cast<__nv_bfloat16*>(dv);
+    p.dq_acc = a.dq_acc;
+    p.lse2 = a.lse2;
+    p.Dd = a.Dd;
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.Nq_pad = nq_pad;
+    p.BH = static_cast<int>(BH);
+    p.n_kt = (Nk + 127) / 128;
+    p.causal = causal;
+    p.causal_off = causal ? Nk - Nq : 0;
+    p.scale = scale;
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    return launch_backward(d, tq, tk, tv, tdo, a, p, static_cast<__nv_bfloat16*>(dq), num_sms,
+                           stream);
 }
 
 }  // namespace
@@ -195,6 +240,28 @@ int attn_fwd_from_host(const void* q, const void* k, const void* v, void* o, flo
     return ATTN_OK;
 }
 
+size_t attn_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || (d != 64 && d != 128)) return 0;
+    return bwd_workspace_bytes(static_cast<long long>(B) * H, Nq, d);
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+             int causal, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+    int st = validate_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale);
+    if (st != ATTN_OK) return st;
+    if (!dout || !dq || !dk || !dv || !workspace) return ATTN_ERR_INVALID_ARG;
+    const long long BH = static_cast<long long>(B) * H;
+    if (BH * ((static_cast<long long>(Nk) + 127) / 128) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    if (workspace_bytes < bwd_workspace_bytes(BH, Nq, d)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+        !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+        !aligned16(workspace))
+        return ATTN_ERR_MISALIGNED;
+    return enqueue_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, Nq, Nk, d, causal, scale,
+                       workspace, static_cast<cudaStream_t>(stream));
+}
+
 const char* attn_status_string(int status) {
     switch (status) {
         case ATTN_OK: return "ATTN_OK";
@@ -209,7 +276,7 @@ const char* attn_status_string(int status) {
 
 int attn_device_error(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
-    const unsigned e = read_and_clear_prefill_error();
+    const unsigned e = read_and_clear_prefill_error() | read_and_clear_bwd_error();
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     return e ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }

@@ -36,6 +36,31 @@ struct DecodeParams {
     float scale_log2;
 };
 
+// Arguments of the backward preprocessing kernel.
+struct BwdPrepParams {
+    const __nv_bfloat16* o;     // [BH, Nq, d]
+    const __nv_bfloat16* dout;  // [BH, Nq, d]
+    const float* lse;           // [BH, Nq], natural log
+    float* lse2;                // [BH, Nq_pad] lse * log2(e); +inf on padded rows
+    float* Dd;                  // [BH, Nq_pad] rowsum(dO * O); 0 on padded rows
+    float* dq_acc;              // [BH, Nq_pad, d], zeroed
+    long long rows;             // BH * Nq_pad
+    int Nq, Nq_pad;
+};
+
+// Arguments of the backward main kernel besides the four TMA descriptors.
+struct BwdParams {
+    __nv_bfloat16* dk;   // [BH, Nk, d]
+    __nv_bfloat16* dv;   // [BH, Nk, d]
+    float* dq_acc;       // [BH, Nq_pad, d]
+    const float* lse2;   // [BH, Nq_pad]
+    const float* Dd;     // [BH, Nq_pad]
+    int Nq, Nk, Nq_pad, BH;
+    int n_kt;            // key tiles per head: ceil(Nk / 128)
+    int causal, causal_off;
+    float scale, scale_log2;
+};
+
 // prefill_sm103.cu
 int prefill_set_attributes();
 // Persistent launch: min(work items, num_sms) CTAs, one per SM.
@@ -48,5 +73,14 @@ unsigned read_and_clear_prefill_error();
 void decode_split_plan(long long BH, int Nk, int* splits, int* keys_per_split);
 size_t decode_workspace_bytes(long long BH, int Nk, int d);
 int launch_decode(int d, const DecodeParams& p, cudaStream_t stream);
+
+// backward_sm103.cu
+int bwd_set_attributes();
+size_t bwd_workspace_bytes(long long BH, int Nq, int d);
+// prep, main (one CTA per key tile and head) and dQ convert kernels, in order
+int launch_backward(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                    const CUtensorMap& tdo, const BwdPrepParams& a, const BwdParams& p,
+                    __nv_bfloat16* dq, int num_sms, cudaStream_t stream);
+unsigned read_and_clear_bwd_error();
 
 }  // namespace gbattn

@@ -159,6 +159,50 @@ int attn_fwd_from_host(const void *q, const void *k, const void *v, void *o, flo
 int attn_fwd_decode_no_alloc(const void *q, const void *k, const void *v, void *o, float *lse,
                              int B, int H, int Nk, int d, float scale, void *stream);
 
+/*
+ * attn_bwd_workspace_bytes -- bytes of device workspace attn_bwd needs:
+ * an fp32 dQ accumulator plus two fp32 values per query row, over whole
+ * 128-row query tiles: B*H*ceil(Nq/128)*128*(d + 2)*4.  Pure host
+ * arithmetic; returns 0 for invalid sizes.
+ */
+size_t attn_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d);
+
+/*
+ * attn_bwd -- backward pass of attn_fwd: dQ, dK, dV for an upstream
+ * gradient dO = dL/dO.
+ *
+ * The FlashAttention-2 backward of the CS336 Lecture 5 notes, section 8.4:
+ * P is not stored but recomputed from the forward's logsumexp,
+ * P_ij = e^{s_ij - lse_i}; with D_i = rowsum(dO_i * O_i) (exercise 9 there)
+ *   dV_j = sum_i P_ij dO_i,           dP_ij = dO_i . v_j,
+ *   dS_ij = P_ij (dP_ij - D_i),       dQ_i = scale sum_j dS_ij k_j,
+ *   dK_j = scale sum_i dS_ij q_i,
+ * with s and the causal mask exactly as in attn_fwd.
+ *
+ *   q, k, v     device, bf16, the forward's inputs; read only.
+ *   o, lse      device, the forward's outputs for these inputs (bf16
+ *               [B,H,Nq,d], fp32 [B,H,Nq]) from attn_fwd; read only.
+ *   dout        device, bf16 [B,H,Nq,d], dL/dO; read only.
+ *   dq          device, bf16 [B,H,Nq,d]; written.
+ *   dk, dv      device, bf16 [B,H,Nk,d]; written.
+ *   B .. scale  as attn_fwd (causal needs Nq <= Nk).
+ *   workspace   device, at least attn_bwd_workspace_bytes(B, H, Nq, Nk, d)
+ *               bytes, 16-byte aligned; owned by the caller, overwritten,
+ *               need not be initialised.  Calls that overlap on the GPU must
+ *               not share a workspace.
+ *   stream      cudaStream_t.
+ * Internal arithmetic: S and dP in fp32 on the tensor cores, P and dS
+ * rounded to bf16 for the dV, dK and dQ products, fp32 accumulation of dK
+ * and dV in Tensor Memory and of dQ in the workspace (atomic adds, so the
+ * last bits of dQ may differ from run to run).
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG (also for a missing or too-small
+ * workspace), ATTN_ERR_UNSUPPORTED, ATTN_ERR_MISALIGNED or ATTN_ERR_CUDA.
+ */
+int attn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+             const float *lse, void *dq, void *dk, void *dv, int B, int H, int Nq, int Nk,
+             int d, int causal, float scale, void *workspace, size_t workspace_bytes,
+             void *stream);
+
 /* attn_status_string -- a static, human-readable name for a status code. */
 const char *attn_status_string(int status);
 

@@ -107,3 +107,38 @@ def test_from_host_rejects_before_launch(lib):
     assert lib.attn_fwd_from_host(*args, 1, 1, 128, 128, 64, 0, 0.125, P(0)) == MISALIGNED
     args = [P(FAKE)] * 10
     assert lib.attn_fwd_from_host(*args, 1, 1, 128, 128, 72, 0, 0.125, P(0)) == UNSUPPORTED
+
+
+def test_bwd_workspace_bytes_is_host_arithmetic(lib):
+    lib.attn_bwd_workspace_bytes.argtypes = [ctypes.c_int] * 5
+    lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+    # dQ accumulator (d floats) plus two floats per row, rows padded to 128
+    assert lib.attn_bwd_workspace_bytes(2, 16, 4096, 4096, 128) == 32 * 4096 * 130 * 4
+    assert lib.attn_bwd_workspace_bytes(1, 1, 77, 77, 64) == 128 * 66 * 4
+    assert lib.attn_bwd_workspace_bytes(1, 1, 77, 77, 96) == 0
+    assert lib.attn_bwd_workspace_bytes(1, 0, 77, 77, 64) == 0
+
+
+def test_bwd_rejects_before_launch(lib):
+    P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.attn_bwd.argtypes = [P] * 9 + [I, I, I, I, I, I, F, P, S, P]
+    lib.attn_bwd.restype = I
+    need = 128 * 66 * 4
+
+    def bwd(ptrs=None, Nq=128, Nk=128, d=64, causal=0, scale=0.125, ws=FAKE, ws_bytes=need):
+        p = [FAKE] * 9 if ptrs is None else ptrs
+        return lib.attn_bwd(*[P(x) for x in p], 1, 1, Nq, Nk, d, causal, scale, P(ws), ws_bytes,
+                            P(0))
+
+    for i in range(9):  # q, k, v, o, dout, lse, dq, dk, dv
+        ptrs = [FAKE] * 9
+        ptrs[i] = 0
+        assert bwd(ptrs) == INVALID, i
+        ptrs[i] = FAKE + 8
+        assert bwd(ptrs) == MISALIGNED, i
+    assert bwd(ws=0) == INVALID
+    assert bwd(ws_bytes=need - 1) == INVALID
+    assert bwd(ws=FAKE + 4) == MISALIGNED
+    assert bwd(d=80) == UNSUPPORTED
+    assert bwd(causal=1, Nq=256, Nk=128, ws_bytes=1 << 20) == UNSUPPORTED
+    assert bwd(scale=float("nan")) == INVALID
