@@ -20,7 +20,8 @@
 //         P^T = 2^{S^T c - L log2 e},  dS^T = P^T (dP^T - D)   (registers)
 //         dV_j += P^T dO_i,  dK_j += dS^T Q_i              (A operand in TMEM)
 //         dQ_i  = dS K_j                                   (A = dS in shared memory)
-//     and a second warpgroup adds dQ_i into the fp32 accumulator;
+//     and a second warpgroup adds dQ_i into the fp32 accumulator with TMA
+//     bulk reduce-adds, staged through the dS tile once dQ_i has read it;
 //   * convert: dQ = scale * accumulator, rounded to bf16.
 // Working transposed (a thread owns a key row) keeps the dV and dK products'
 // A operands in Tensor Memory and makes the row statistics L_i and D_i
@@ -35,10 +36,18 @@ namespace gbattn {
 
 __device__ unsigned int g_bwd_error = 0;
 
+// Error bit of the backward kernel: its shared-memory layout did not fit.
+constexpr unsigned kErrLayout = 2u;
+
 namespace {
 
 constexpr int kTile = 128;       // keys per CTA, queries per step
-constexpr int kThreads = 320;    // warps 0-3 key rows, 4-7 dQ rows, 8 MMA, 9 TMA
+constexpr int kThreads = 384;    // warps 0-3 key rows, 4-7 dQ rows, 8 MMA, 9 TMA, 10-11 idle
+// Register split.  The launch gives each thread 168 registers (65536 / 384,
+// rounded down to 8); the key-row warpgroup takes more from the other two:
+// 128 x 240 + 128 x 96 + 128 x 96 = 55296 <= 384 x 168 = 64512.
+constexpr uint32_t kKeyRowRegs = 240;
+constexpr uint32_t kOtherRegs = 96;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr uint32_t kTmemCols = 512;
@@ -52,19 +61,28 @@ struct BCfg {
     static constexpr int kVOff = kTileBytes;
     static constexpr int kRingOff = 2 * kTileBytes;   // stage s: Q_i, then dO_i
     static constexpr int kDsOff = kRingOff + 4 * kTileBytes;  // dS, 128 keys x 128 queries bf16
-    static constexpr int kBarOff = kDsOff + 2 * kSubBytes;
+    // stage s: L log2(e) and D of the stage's 128 queries (fp32, 512 B each)
+    static constexpr int kLdOff = kDsOff + 2 * kSubBytes;
+    static constexpr int kTilesBytes = kLdOff + 2 * 1024;
+    // Barriers, the TMEM address slot and the abort flag (96 bytes) go into the
+    // gap below the 1024-byte aligned tiles when it has room, else after them.
+    // The dynamic shared memory base is 16-byte aligned, so the gap is at most
+    // 1008 bytes: the allocation covers both cases.
     static constexpr int kNumBars = 10;
-    static constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
-    static constexpr int kAbortOff = kTmemSlotOff + 4;
-    static constexpr int kSmemBytes = kAbortOff + 4 + 1024;  // + alignment slack
+    static constexpr int kSmallBytes = 96;
+    static constexpr int kSmemBytes =
+        kTilesBytes + (1008 > kSmallBytes + 80 ? 1008 : kSmallBytes + 80);
     // Tensor Memory columns.  S^T is overwritten by P^T (bf16 pairs, first 64
-    // columns) and, once the dV product has read P^T, by the dQ_i product.
+    // columns); dP^T by dS^T (bf16 pairs, first 64 columns) and, once the dK
+    // product has read dS^T, by the dQ_i product.
     static constexpr uint32_t kColS = 0;
-    static constexpr uint32_t kColDP = 128;  // dP^T, then dS^T (bf16 pairs, first 64 columns)
+    static constexpr uint32_t kColDP = 128;
+    static constexpr uint32_t kColDQ = 128;
     static constexpr uint32_t kColDV = 256;
     static constexpr uint32_t kColDK = 256 + D;
 };
 static_assert(BCfg<128>::kSmemBytes <= 232448, "shared memory of one CTA");
+static_assert(BCfg<128>::kNumBars * 8 + 8 <= BCfg<128>::kSmallBytes, "small objects");
 
 struct BBars {
     uint32_t base;
@@ -139,8 +157,79 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// 1-D bulk copy global -> shared completing `bar`'s transaction count
+// (addresses 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Ties registers to the preceding tcgen05.wait::ld without emitting code, so
+// no use of them is scheduled above that wait.
+__device__ __forceinline__ void after_wait_ld(uint32_t (&a)[32], uint32_t (&b)[32]) {
+    asm volatile(""
+                 : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]),
+                   "+r"(a[6]), "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]),
+                   "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15]), "+r"(a[16]), "+r"(a[17]),
+                   "+r"(a[18]), "+r"(a[19]), "+r"(a[20]), "+r"(a[21]), "+r"(a[22]), "+r"(a[23]),
+                   "+r"(a[24]), "+r"(a[25]), "+r"(a[26]), "+r"(a[27]), "+r"(a[28]), "+r"(a[29]),
+                   "+r"(a[30]), "+r"(a[31]), "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]),
+                   "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7]), "+r"(b[8]), "+r"(b[9]),
+                   "+r"(b[10]), "+r"(b[11]), "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15]),
+                   "+r"(b[16]), "+r"(b[17]), "+r"(b[18]), "+r"(b[19]), "+r"(b[20]), "+r"(b[21]),
+                   "+r"(b[22]), "+r"(b[23]), "+r"(b[24]), "+r"(b[25]), "+r"(b[26]), "+r"(b[27]),
+                   "+r"(b[28]), "+r"(b[29]), "+r"(b[30]), "+r"(b[31])
+                 :
+                 : "memory");
+}
+
+// Barrier 1 among the 128 threads of the dQ warpgroup (barrier 0 is
+// __syncthreads).
+__device__ __forceinline__ void dq_group_sync() {
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// AND of `ok` over the 128 threads of the dQ warpgroup (barrier 1 with a
+// reduction): every warp of the group takes the same branch after a bounded
+// wait, so none can be left alone at a later `bar.sync 1`.
+__device__ __forceinline__ bool dq_group_all(bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, 1, 128, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(ok))
+        : "memory");
+    return r != 0;
+}
+
+// Element-wise add of a shared-memory box into global memory through the
+// tensor map (TMA reduce), tracked by this thread's bulk async-group.
+__device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, uint32_t src, int x, int y,
+                                                  int z) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+        " [%0, {%2, %3, %4}], [%1];" ::"l"(tmap),
+        "r"(src), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// The shared-memory sources of this thread's committed bulk copies have been read.
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// This thread's committed bulk copies have completed.
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Instruction descriptor with A in MN-major (transposed) layout as well.
-constexpr uint32_t idesc_bf16_a_mn(uint32_t M, uint32_t N) {
+__host__ __device__ constexpr uint32_t idesc_bf16_a_mn(uint32_t M, uint32_t N) {
     return umma_idesc_bf16(M, N, true) | (1u << 15);
 }
 
@@ -209,20 +298,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
-                    const __grid_constant__ CUtensorMap tm_do, BwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_dqacc, BwdParams p) {
     using C = BCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle pattern
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int gap = static_cast<int>(smem - smem_raw);
+    uint8_t* small = gap >= C::kSmallBytes ? smem - C::kSmallBytes : smem + C::kTilesBytes;
+    if (gap + C::kTilesBytes + (gap >= C::kSmallBytes ? 0 : C::kSmallBytes) > C::kSmemBytes) {
+        // the base was less aligned than assumed: report and do nothing
+        if (threadIdx.x == 0) atomicOr(&g_bwd_error, kErrLayout);
+        return;
+    }
     const uint32_t sbase = smem_addr(smem);
     const uint32_t sK = sbase + C::kKOff;
     const uint32_t sV = sbase + C::kVOff;
     const uint32_t sRing = sbase + C::kRingOff;
     const uint32_t sDs = sbase + C::kDsOff;
-    const BBars bars{sbase + C::kBarOff};
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kTmemSlotOff);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
+    const uint32_t sLd = sbase + C::kLdOff;
+    const BBars bars{smem_addr(small)};
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(small + C::kNumBars * 8);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(small + C::kNumBars * 8 + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -262,6 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    if (warp >= 8) {
+    // ====================================================== control warpgroup
+    setmaxnreg_dec<kOtherRegs>();
     if (warp == kLoadWarp) {
         // ===================================================== TMA producer
         if (lane == 0) {
@@ -282,9 +383,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (it >= 2 &&
                     !(ok = wait_or_abort(bars.q_empty(s), ((it >> 1) - 1) & 1, abort_flag)))
                     break;
-                mbar_arrive_expect_tx(bars.q_full(s), 2 * C::kTileBytes);
+                mbar_arrive_expect_tx(bars.q_full(s), 2 * C::kTileBytes + 1024);
                 const uint32_t dst = sRing + s * 2 * C::kTileBytes;
                 const int y = (i_first + it) * kTile;
+                const size_t row0 = static_cast<size_t>(bh) * p.Nq_pad + y;
+                bulk_load(sLd + s * 1024, p.lse2 + row0, 512, bars.q_full(s));
+                bulk_load(sLd + s * 1024 + 512, p.Dd + row0, 512, bars.q_full(s));
                 for (int sub = 0; sub < C::kSub; ++sub) {
                     tma_load_3d(dst + sub * C::kSubBytes, &tm_q, bars.q_full(s), sub * 64, y, bh);
                     tma_load_3d(dst + C::kTileBytes + sub * C::kSubBytes, &tm_do, bars.q_full(s),
@@ -302,11 +406,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ===================================================== MMA issuer
-        // Per step i (stage s):  S^T, dP^T -> s_full;  wait P^T, dS^T;
-        // dV += P^T dO_i, dK += dS^T Q_i -> q_empty(s);  dQ_i = dS K_j -> dq_full.
-        // dQ_i lands in the S^T columns after the dV product has read P^T from
-        // them (one thread's MMAs run in issue order), so the next step's S^T
-        // waits until the dQ warpgroup has read dQ_i (dq_free).
+        // Per step i (stage s):  dP^T -> s_full (S^T was issued at the end of
+        // the previous step);  wait P^T, dS^T;  dV += P^T dO_i, dK += dS^T Q_i
+        // -> q_empty(s);  dQ_i = dS K_j -> dq_full;  S^T of step i + 1.
+        // dQ_i lands in the dP^T columns after the dK product has read dS^T from
+        // them and S^T(i+1) in the S^T columns after the dV product has read P^T
+        // (one thread's MMAs run in issue order), so only dP^T(i+1) waits for
+        // the dQ warpgroup to have taken dQ_i (dq_free).
         if (lane == 0) {
             const uint32_t id_s = umma_idesc_bf16(kTile, kTile, false);  // both K-major
             const uint32_t id_acc = umma_idesc_bf16(kTile, D, true);     // B MN-major
@@ -315,24 +421,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dv_k = umma_desc_sw128(sV, 16, 1024);
             const uint64_t dk_mn = umma_desc_sw128(sK, C::kSubBytes, 1024);
             const uint64_t dds_mn = umma_desc_sw128(sDs, C::kSubBytes, 1024);
-            bool ok = wait_or_abort(bars.kv_full(), 0, abort_flag);
+            auto issue_s = [&](int it) {  // S^T = K_j Q_i^T, K = d in steps of 16
+                const uint64_t dq_k = umma_desc_sw128(sRing + (it & 1) * 2 * C::kTileBytes, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk >> 2) * C::kSubBytes + (kk & 3) * 32) >> 4;
+                    umma_ss(tmem + C::kColS, dk_k + off, dq_k + off, id_s, kk > 0 ? 1u : 0u);
+                }
+            };
+            bool ok = wait_or_abort(bars.kv_full(), 0, abort_flag) &&
+                      wait_or_abort(bars.q_full(0), 0, abort_flag);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+            }
             for (int it = 0; it < n_iter && ok; ++it) {
                 const int s = it & 1;
-                if (!(ok = wait_or_abort(bars.q_full(s), (it >> 1) & 1, abort_flag))) break;
                 if (it > 0 && !(ok = wait_or_abort(bars.dq_free(), (it - 1) & 1, abort_flag)))
                     break;
                 tc_fence_after();
                 const uint32_t sq = sRing + s * 2 * C::kTileBytes;
                 const uint32_t sdo = sq + C::kTileBytes;
-                const uint64_t dq_k = umma_desc_sw128(sq, 16, 1024);
                 const uint64_t ddo_k = umma_desc_sw128(sdo, 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {  // K = d in steps of 16
-                    const uint32_t off = ((kk >> 2) * C::kSubBytes + (kk & 3) * 32) >> 4;
-                    umma_ss(tmem + C::kColS, dk_k + off, dq_k + off, id_s, kk > 0 ? 1u : 0u);
-                }
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
+                for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V_j dO_i^T
                     const uint32_t off = ((kk >> 2) * C::kSubBytes + (kk & 3) * 32) >> 4;
                     umma_ss(tmem + C::kColDP, dv_k + off, ddo_k + off, id_s, kk > 0 ? 1u : 0u);
                 }
@@ -354,16 +466,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // K = 128 keys in steps of 16 rows of the dS and K_j tiles
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)
-                    umma_ss(tmem + C::kColS, dds_mn + ((kk * 2048) >> 4), dk_mn + ((kk * 2048) >> 4),
+                    umma_ss(tmem + C::kColDQ, dds_mn + ((kk * 2048) >> 4), dk_mn + ((kk * 2048) >> 4),
                             id_dq, kk > 0 ? 1u : 0u);
                 umma_commit(bars.dq_full());
+                if (it + 1 < n_iter) {
+                    if (!(ok = wait_or_abort(bars.q_full((it + 1) & 1), ((it + 1) >> 1) & 1,
+                                             abort_flag)))
+                        break;
+                    tc_fence_after();
+                    issue_s(it + 1);
+                }
             }
             // every MMA this thread issued has completed once `done` flips
             umma_commit(bars.done());
             mbar_wait(bars.done(), 0);
         }
         __syncwarp();
+    }  // warps 10 and 11 have no role
     } else if (warp < 4) {
+        setmaxnreg_inc<kKeyRowRegs>();
         // ===================================================== key rows: P^T, dS^T
         const int r = warp * 32 + lane;  // key row within the tile = TMEM lane
         const int key = kj0 + r;
@@ -372,63 +493,68 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tS = tmem + lane_off + C::kColS;
         const uint32_t tDP = tmem + lane_off + C::kColDP;
         const float cl2 = p.scale_log2;
-        const float* lse2_h = p.lse2 + static_cast<size_t>(bh) * p.Nq_pad;
-        const float* D_h = p.Dd + static_cast<size_t>(bh) * p.Nq_pad;
         const int first_vis = key - p.causal_off;  // causal: query q sees this key iff q >= first_vis
         bool ok = true;
         for (int it = 0; it < n_iter; ++it) {
-            // S^T(it) was issued after dQ_{it-1} had been read, so the dS tile in
-            // shared memory (read by that product) is free as well
-            ok = wait_or_abort(bars.s_full(), it & 1, abort_flag);
+            // dP^T(it) was issued after the dQ warpgroup had taken dQ_{it-1} out of
+            // the dS tile, so the tile in shared memory is free as well.  The
+            // stage's L and D arrived with its Q and dO tiles (q_full).
+            ok = wait_or_abort(bars.s_full(), it & 1, abort_flag) &&
+                 wait_or_abort(bars.q_full(it & 1), (it >> 1) & 1, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
             const int i0 = (i_first + it) * kTile;
             const bool diag = p.causal && (kj0 + kTile - 1 > i0 + p.causal_off);
+            const float4* L4 = reinterpret_cast<const float4*>(smem + C::kLdOff + (it & 1) * 1024);
+            const float4* D4 = L4 + 32;
 #pragma unroll 1
-            for (int ch = 0; ch < 4; ++ch) {  // 32 queries at a time
-                uint32_t sr[32], dr[32];
-                tmem_ld32(tS + ch * 32, sr);
-                tmem_ld32(tDP + ch * 32, dr);
-                // L2 and D of these 32 queries: the same address in every lane
-                float lq[32], dq[32];
+            for (int hf = 0; hf < 2; ++hf) {  // 64 queries at a time
+                uint32_t s0[32], s1[32], d0[32], d1[32];
+                tmem_ld32(tS + hf * 64, s0);
+                tmem_ld32(tS + hf * 64 + 32, s1);
+                tmem_ld32(tDP + hf * 64, d0);
+                tmem_ld32(tDP + hf * 64 + 32, d1);
+                tmem_wait_ld_into(s0, s1);
+                after_wait_ld(d0, d1);
+                uint32_t pk[32], dk[32];
 #pragma unroll
-                for (int x = 0; x < 8; ++x) {
-                    const float4 l4 = __ldg(reinterpret_cast<const float4*>(lse2_h + i0 + ch * 32) + x);
-                    const float4 d4 = __ldg(reinterpret_cast<const float4*>(D_h + i0 + ch * 32) + x);
-                    lq[4 * x] = l4.x; lq[4 * x + 1] = l4.y; lq[4 * x + 2] = l4.z; lq[4 * x + 3] = l4.w;
-                    dq[4 * x] = d4.x; dq[4 * x + 1] = d4.y; dq[4 * x + 2] = d4.z; dq[4 * x + 3] = d4.w;
-                }
-                tmem_wait_ld_into(sr, dr);
-                uint32_t pk[16], dk[16];
+                for (int c4 = 0; c4 < 16; ++c4) {  // four queries per shared-memory read
+                    // L and D of these queries: the same address in every lane
+                    const float4 l4 = L4[hf * 16 + c4];
+                    const float4 dd4 = D4[hf * 16 + c4];
+                    const float lq[4] = {l4.x, l4.y, l4.z, l4.w};
+                    const float dq[4] = {dd4.x, dd4.y, dd4.z, dd4.w};
+                    float pv[4], dsv[4];
 #pragma unroll
-                for (int c = 0; c < 32; c += 2) {
-                    float pv[2], dsv[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int q = i0 + ch * 32 + c + e;
-                        float pe = ex2_approx(fmaf(__uint_as_float(sr[c + e]), cl2, -lq[c + e]));
-                        if (!key_ok || (diag && q < first_vis)) pe = 0.f;
+                    for (int e = 0; e < 4; ++e) {
+                        const int c = c4 * 4 + e;  // column within the 64
+                        const uint32_t sv = c < 32 ? s0[c] : s1[c - 32];
+                        const uint32_t dv = c < 32 ? d0[c] : d1[c - 32];
+                        float pe = ex2_approx(fmaf(__uint_as_float(sv), cl2, -lq[e]));
+                        if (!key_ok || (diag && i0 + hf * 64 + c < first_vis)) pe = 0.f;
                         pv[e] = pe;
-                        dsv[e] = pe * (__uint_as_float(dr[c + e]) - dq[c + e]);
+                        dsv[e] = pe * (__uint_as_float(dv) - dq[e]);
                     }
-                    pk[c / 2] = pack_bf16x2(pv[0], pv[1]);
-                    dk[c / 2] = pack_bf16x2(dsv[0], dsv[1]);
+                    pk[2 * c4] = pack_bf16x2(pv[0], pv[1]);
+                    pk[2 * c4 + 1] = pack_bf16x2(pv[2], pv[3]);
+                    dk[2 * c4] = pack_bf16x2(dsv[0], dsv[1]);
+                    dk[2 * c4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
                 }
                 // P^T and dS^T over the first 64 columns of S^T and dP^T: packed
-                // column ch*16.. lies below the fp32 columns still to be read
-                tmem_st16(tS + ch * 16, pk);
-                tmem_st16(tDP + ch * 16, dk);
-                // dS as the MN-major A operand of dQ_i = dS K_j: row r of 128
-                // queries, two 64-query halves 16 KB apart, 16-byte chunks
-                // permuted by the 128-byte swizzle (chunk ^ (row % 8))
-                uint8_t* row = smem + C::kDsOff + (ch >> 1) * C::kSubBytes + r * 128;
+                // columns hf*32.. lie below the fp32 columns still to be read
+                tmem_st16(tS + hf * 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+                tmem_st16(tS + hf * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+                tmem_st16(tDP + hf * 32, *reinterpret_cast<uint32_t(*)[16]>(&dk[0]));
+                tmem_st16(tDP + hf * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&dk[16]));
+                // dS as the MN-major A operand of dQ_i = dS K_j: row r holds 64
+                // queries per 16 KB half, its 16-byte chunks permuted by the
+                // 128-byte swizzle (chunk ^ (row % 8))
+                uint8_t* row = smem + C::kDsOff + hf * C::kSubBytes + r * 128;
 #pragma unroll
-                for (int x = 0; x < 4; ++x) {
-                    const int chunk = ((ch & 1) * 4 + x) ^ (r & 7);
-                    *reinterpret_cast<uint4*>(row + chunk * 16) =
+                for (int x = 0; x < 8; ++x)
+                    *reinterpret_cast<uint4*>(row + ((x ^ (r & 7)) * 16)) =
                         make_uint4(dk[4 * x], dk[4 * x + 1], dk[4 * x + 2], dk[4 * x + 3]);
-                }
             }
             tmem_wait_st();
             fence_proxy_async_smem();
@@ -465,38 +591,61 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (warp < 8) {
+    } else {
+        setmaxnreg_dec<kOtherRegs>();
         // ===================================================== query rows: dQ_i
+        // dQ_i leaves Tensor Memory through the dS tile (free once the dQ product
+        // has read it): 32-column fp32 boxes of 128 rows in the 128-byte swizzle
+        // layout, two at a time, each added to the accumulator by one TMA
+        // reduce-add.
         const int wq = warp - 4;
         const int r = wq * 32 + lane;  // query row within the tile = TMEM lane
-        const uint32_t tQ = tmem + (static_cast<uint32_t>(wq * 32) << 16) + C::kColS;
+        const uint32_t tQ = tmem + (static_cast<uint32_t>(wq * 32) << 16) + C::kColDQ;
+        const bool leader = threadIdx.x == 4 * 32;
+        constexpr int kBoxBytes = 128 * 128;         // 128 rows x 32 fp32
+        constexpr int kBoxes = D / 32;
+        constexpr int kBoxesPerRound = 2;            // the dS tile holds two boxes
         bool ok = true;
         for (int it = 0; it < n_iter; ++it) {
-            ok = wait_or_abort(bars.dq_full(), it & 1, abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
+            ok = dq_group_all(wait_or_abort(bars.dq_full(), it & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
-            const int q = (i_first + it) * kTile + r;
-            float* dst = p.dq_acc + (static_cast<size_t>(bh) * p.Nq_pad + q) * D;
+            const int q0 = (i_first + it) * kTile;
 #pragma unroll 1
-            for (int ch = 0; ch < D / 32; ++ch) {
-                uint32_t v[32];
-                tmem_ld32(tQ + ch * 32, v);
-                tmem_wait_ld_into(v);
-                if (q < p.Nq) {
-                    float4* d4 = reinterpret_cast<float4*>(dst + ch * 32);
+            for (int b0 = 0; b0 < kBoxes; b0 += kBoxesPerRound) {
+                if (b0 > 0) {
+                    // the previous round's boxes have been read out of shared memory
+                    if (leader) bulk_wait_read_all();
+                    dq_group_sync();
+                }
+#pragma unroll
+                for (int bb = 0; bb < kBoxesPerRound; ++bb) {
+                    uint32_t v[32];
+                    tmem_ld32(tQ + (b0 + bb) * 32, v);
+                    tmem_wait_ld_into(v);
+                    uint8_t* row = smem + C::kDsOff + bb * kBoxBytes + r * 128;
 #pragma unroll
                     for (int x = 0; x < 8; ++x)
-                        atomicAdd(d4 + x, make_float4(__uint_as_float(v[4 * x]),
-                                                      __uint_as_float(v[4 * x + 1]),
-                                                      __uint_as_float(v[4 * x + 2]),
-                                                      __uint_as_float(v[4 * x + 3])));
+                        *reinterpret_cast<uint4*>(row + ((x ^ (r & 7)) * 16)) =
+                            make_uint4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+                }
+                fence_proxy_async_smem();
+                dq_group_sync();
+                if (leader) {
+                    for (int bb = 0; bb < kBoxesPerRound; ++bb)
+                        tma_reduce_add_3d(&tm_dqacc, sDs + bb * kBoxBytes, (b0 + bb) * 32, q0, bh);
+                    bulk_commit();
                 }
             }
+            // dQ_i has left Tensor Memory; the dS tile is free once the last
+            // round's boxes have been read
+            if (leader) bulk_wait_read_all();
+            dq_group_sync();
             tc_fence_before();
-            __syncwarp();
             if (lane == 0) mbar_arrive(bars.dq_free());
         }
+        // the reduce-adds must be complete before the CTA exits
+        if (leader) bulk_wait_all();
     }
 
     // ---- teardown: all Tensor Memory traffic is complete; free the columns
@@ -549,15 +698,16 @@ size_t bwd_workspace_bytes(long long BH, int Nq, int d) {
 
 template <int D>
 static int launch_backward_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                             const CUtensorMap& tdo, const BwdPrepParams& a, const BwdParams& p,
-                             __nv_bfloat16* dq, int num_sms, cudaStream_t stream) {
+                             const CUtensorMap& tdo, const CUtensorMap& tdqacc,
+                             const BwdPrepParams& a, const BwdParams& p, __nv_bfloat16* dq,
+                             int num_sms, cudaStream_t stream) {
     const long long prep_threads = (a.rows * (D / 8) + 31) / 32 * 32;
     long long prep_blocks = (prep_threads + 255) / 256;
     if (prep_blocks > 8LL * num_sms) prep_blocks = 8LL * num_sms;
     attn_bwd_prep_kernel<D><<<static_cast<unsigned>(prep_blocks), 256, 0, stream>>>(a);
     const long long grid = static_cast<long long>(p.n_kt) * p.BH;
     attn_bwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, BCfg<D>::kSmemBytes, stream>>>(
-        tq, tk, tv, tdo, p);
+        tq, tk, tv, tdo, tdqacc, p);
     const long long n8 = static_cast<long long>(p.BH) * p.Nq * D / 8;
     long long cblocks = (n8 + 255) / 256;
     if (cblocks > 8LL * num_sms) cblocks = 8LL * num_sms;
@@ -567,10 +717,10 @@ static int launch_backward_d(const CUtensorMap& tq, const CUtensorMap& tk, const
 }
 
 int launch_backward(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                    const CUtensorMap& tdo, const BwdPrepParams& a, const BwdParams& p,
-                    __nv_bfloat16* dq, int num_sms, cudaStream_t stream) {
-    return d == 128 ? launch_backward_d<128>(tq, tk, tv, tdo, a, p, dq, num_sms, stream)
-                    : launch_backward_d<64>(tq, tk, tv, tdo, a, p, dq, num_sms, stream);
+                    const CUtensorMap& tdo, const CUtensorMap& tdqacc, const BwdPrepParams& a,
+                    const BwdParams& p, __nv_bfloat16* dq, int num_sms, cudaStream_t stream) {
+    return d == 128 ? launch_backward_d<128>(tq, tk, tv, tdo, tdqacc, a, p, dq, num_sms, stream)
+                    : launch_backward_d<64>(tq, tk, tv, tdo, tdqacc, a, p, dq, num_sms, stream);
 }
 
 unsigned read_and_clear_bwd_error() {

@@ -98,6 +98,23 @@ int encode_bhnd(CUtensorMap* m, const void* base, long long BH, int N, int d) {
     return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// The fp32 dQ accumulator [BH, Nq_pad, d] of the backward as a 3-D tensor
+// {d, Nq_pad, BH} in boxes of 32 x 128 x 1 with the 128-byte swizzle (the
+// target of the backward's TMA reduce-adds).
+int encode_dq_acc(CUtensorMap* m, void* base, long long BH, int nq_pad, int d) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(nq_pad),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                             static_cast<cuuint64_t>(nq_pad) * static_cast<cuuint64_t>(d) * 4};
+    cuuint32_t box[3] = {32, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 int enqueue_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                 int Nq, int Nk, int d, int causal, float scale, cudaStream_t stream) {
     int st = ensure_init();
@@ -137,6 +154,8 @@ int enqueue_bwd(const void* q, const void* k, const void* v, const void* o, cons
     if ((st = encode_bhnd(&tdo, dout, BH, Nq, d)) != ATTN_OK) return st;
     const int nq_pad = (Nq + 127) / 128 * 128;
     float* ws = static_cast<float*>(workspace);
+    CUtensorMap tdqacc;
+    if ((st = encode_dq_acc(&tdqacc, ws, BH, nq_pad, d)) != ATTN_OK) return st;
     BwdPrepParams a;
     a.o = static_cast<const __nv_bfloat16*>(o);
     a.dout = static_cast<const __nv_bfloat16*>(dout);
@@ -162,8 +181,8 @@ int enqueue_bwd(const void* q, const void* k, const void* v, const void* o, cons
     p.causal_off = causal ? Nk - Nq : 0;
     p.scale = scale;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
-    return launch_backward(d, tq, tk, tv, tdo, a, p, static_cast<__nv_bfloat16*>(dq), num_sms,
-                           stream);
+    return launch_backward(d, tq, tk, tv, tdo, tdqacc, a, p, static_cast<__nv_bfloat16*>(dq),
+                           num_sms, stream);
 }
 
 }  // namespace

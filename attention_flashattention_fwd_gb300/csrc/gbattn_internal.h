@@ -77,10 +77,12 @@ int launch_decode(int d, const DecodeParams& p, cudaStream_t stream);
 // backward_sm103.cu
 int bwd_set_attributes();
 size_t bwd_workspace_bytes(long long BH, int Nq, int d);
-// prep, main (one CTA per key tile and head) and dQ convert kernels, in order
+// prep, main (one CTA per key tile and head) and dQ convert kernels, in order.
+// tdqacc: the fp32 dQ accumulator [BH, Nq_pad, d] as 32 x 128 x 1 boxes with
+// the 128-byte swizzle.
 int launch_backward(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                    const CUtensorMap& tdo, const BwdPrepParams& a, const BwdParams& p,
-                    __nv_bfloat16* dq, int num_sms, cudaStream_t stream);
+                    const CUtensorMap& tdo, const CUtensorMap& tdqacc, const BwdPrepParams& a,
+                    const BwdParams& p, __nv_bfloat16* dq, int num_sms, cudaStream_t stream);
 unsigned read_and_clear_bwd_error();
 
 }  // namespace gbattn
