@@ -44,10 +44,12 @@ namespace {
 constexpr int kTile = 128;       // keys per CTA, queries per step
 constexpr int kThreads = 384;    // warps 0-3 key rows, 4-7 dQ rows, 8 MMA, 9 TMA, 10-11 idle
 // Register split.  The launch gives each thread 168 registers (65536 / 384,
-// rounded down to 8); the key-row warpgroup takes more from the other two:
-// 128 x 240 + 128 x 96 + 128 x 96 = 55296 <= 384 x 168 = 64512.
+// rounded down to 8); the key-row warpgroup (P and dS) and the dQ warpgroup
+// (all of dQ_i in registers) take more from the control warpgroup:
+// 128 x 240 + 128 x 152 + 128 x 96 = 62464 <= 384 x 168 = 64512.
 constexpr uint32_t kKeyRowRegs = 240;
-constexpr uint32_t kOtherRegs = 96;
+constexpr uint32_t kDqRegs = 152;
+constexpr uint32_t kCtrlRegs = 96;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr uint32_t kTmemCols = 512;
@@ -64,12 +66,12 @@ struct BCfg {
     // stage s: L log2(e) and D of the stage's 128 queries (fp32, 512 B each)
     static constexpr int kLdOff = kDsOff + 2 * kSubBytes;
     static constexpr int kTilesBytes = kLdOff + 2 * 1024;
-    // Barriers, the TMEM address slot and the abort flag (96 bytes) go into the
-    // gap below the 1024-byte aligned tiles when it has room, else after them.
-    // The dynamic shared memory base is 16-byte aligned, so the gap is at most
-    // 1008 bytes: the allocation covers both cases.
-    static constexpr int kNumBars = 10;
-    static constexpr int kSmallBytes = 96;
+    // Barriers, the TMEM address slot and the abort flag (112 bytes) go into
+    // the gap below the 1024-byte aligned tiles when it has room, else after
+    // them.  The dynamic shared memory base is 16-byte aligned, so the gap is
+    // at most 1008 bytes: the allocation covers both cases.
+    static constexpr int kNumBars = 13;
+    static constexpr int kSmallBytes = 112;
     static constexpr int kSmemBytes =
         kTilesBytes + (1008 > kSmallBytes + 80 ? 1008 : kSmallBytes + 80);
     // Tensor Memory columns.  S^T is overwritten by P^T (bf16 pairs, first 64
@@ -89,11 +91,14 @@ struct BBars {
     __device__ uint32_t kv_full() const { return base; }
     __device__ uint32_t q_full(int s) const { return base + 8u * (1 + s); }
     __device__ uint32_t q_empty(int s) const { return base + 8u * (3 + s); }
-    __device__ uint32_t s_full() const { return base + 8u * 5; }
-    __device__ uint32_t p_ready() const { return base + 8u * 6; }
-    __device__ uint32_t dq_full() const { return base + 8u * 7; }
-    __device__ uint32_t dq_free() const { return base + 8u * 8; }
-    __device__ uint32_t done() const { return base + 8u * 9; }
+    __device__ uint32_t s_full() const { return base + 8u * 5; }    // S^T in TMEM
+    __device__ uint32_t dp_full() const { return base + 8u * 6; }   // dP^T in TMEM
+    __device__ uint32_t pa_ready() const { return base + 8u * 7; }  // P^T written
+    __device__ uint32_t pb_ready() const { return base + 8u * 8; }  // dS^T and dS written
+    __device__ uint32_t dq_full() const { return base + 8u * 9; }   // dQ_i in TMEM
+    __device__ uint32_t dq_free() const { return base + 8u * 10; }  // dQ_i out of TMEM
+    __device__ uint32_t ds_free() const { return base + 8u * 11; }  // dS tile free again
+    __device__ uint32_t done() const { return base + 8u * 12; }
 };
 
 __device__ __forceinline__ void flag_abort(volatile int* abort_flag) {
@@ -347,9 +352,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bars.q_empty(s), 1);
         }
         mbar_init(bars.s_full(), 1);
-        mbar_init(bars.p_ready(), 4);  // one arrival per key-row warp
+        mbar_init(bars.dp_full(), 1);
+        mbar_init(bars.pa_ready(), 4);  // one arrival per key-row warp
+        mbar_init(bars.pb_ready(), 4);
         mbar_init(bars.dq_full(), 1);
-        mbar_init(bars.dq_free(), 4);  // one arrival per dQ warp
+        mbar_init(bars.dq_free(), 4);   // one arrival per dQ warp
+        mbar_init(bars.ds_free(), 1);   // the dQ warpgroup's TMA thread
         mbar_init(bars.done(), 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -362,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp >= 8) {
     // ====================================================== control warpgroup
-    setmaxnreg_dec<kOtherRegs>();
+    setmaxnreg_dec<kCtrlRegs>();
     if (warp == kLoadWarp) {
         // ===================================================== TMA producer
         if (lane == 0) {
@@ -406,13 +414,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ===================================================== MMA issuer
-        // Per step i (stage s):  dP^T -> s_full (S^T was issued at the end of
-        // the previous step);  wait P^T, dS^T;  dV += P^T dO_i, dK += dS^T Q_i
-        // -> q_empty(s);  dQ_i = dS K_j -> dq_full;  S^T of step i + 1.
+        // Per step i (stage s), with S^T(i) issued at the end of step i - 1:
+        //   [dQ_{i-1} out of TMEM]  dP^T -> dp_full
+        //   [P^T written]           dV += P^T dO_i
+        //   [dS^T, dS written]      dK += dS^T Q_i -> q_empty(s);  dQ_i = dS K_j -> dq_full
+        //   [Q_{i+1} loaded]        S^T(i+1) -> s_full
         // dQ_i lands in the dP^T columns after the dK product has read dS^T from
-        // them and S^T(i+1) in the S^T columns after the dV product has read P^T
-        // (one thread's MMAs run in issue order), so only dP^T(i+1) waits for
-        // the dQ warpgroup to have taken dQ_i (dq_free).
+        // them, S^T(i+1) in the S^T columns after the dV product has read P^T
+        // (one thread's MMAs run in issue order); only dP^T(i+1) waits for the
+        // dQ warpgroup to have taken dQ_i.
         if (lane == 0) {
             const uint32_t id_s = umma_idesc_bf16(kTile, kTile, false);  // both K-major
             const uint32_t id_acc = umma_idesc_bf16(kTile, D, true);     // B MN-major
@@ -428,6 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t off = ((kk >> 2) * C::kSubBytes + (kk & 3) * 32) >> 4;
                     umma_ss(tmem + C::kColS, dk_k + off, dq_k + off, id_s, kk > 0 ? 1u : 0u);
                 }
+                umma_commit(bars.s_full());
             };
             bool ok = wait_or_abort(bars.kv_full(), 0, abort_flag) &&
                       wait_or_abort(bars.q_full(0), 0, abort_flag);
@@ -448,16 +459,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t off = ((kk >> 2) * C::kSubBytes + (kk & 3) * 32) >> 4;
                     umma_ss(tmem + C::kColDP, dv_k + off, ddo_k + off, id_s, kk > 0 ? 1u : 0u);
                 }
-                umma_commit(bars.s_full());
-                if (!(ok = wait_or_abort(bars.p_ready(), it & 1, abort_flag))) break;
-                tc_fence_after();
+                umma_commit(bars.dp_full());
                 const uint64_t dq_mn = umma_desc_sw128(sq, C::kSubBytes, 1024);
                 const uint64_t ddo_mn = umma_desc_sw128(sdo, C::kSubBytes, 1024);
                 // K = 128 queries in steps of 16: 8 packed P / dS columns, 16 rows of 128 B
+                if (!(ok = wait_or_abort(bars.pa_ready(), it & 1, abort_flag))) break;
+                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)
                     umma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8, ddo_mn + ((kk * 2048) >> 4),
                             id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+                if (!(ok = wait_or_abort(bars.pb_ready(), it & 1, abort_flag))) break;
+                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)
                     umma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8, dq_mn + ((kk * 2048) >> 4),
@@ -486,6 +499,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp < 4) {
         setmaxnreg_inc<kKeyRowRegs>();
         // ===================================================== key rows: P^T, dS^T
+        // Phase A (S^T in TMEM): P^T = 2^{S^T c - L}, kept as bf16 pairs in
+        // registers and written over the first 64 columns of S^T (the dV
+        // product's A operand).  Phase B (dP^T in TMEM): dS^T = P^T (dP^T - D)
+        // from the bf16 P, written over the first 64 columns of dP^T (the dK
+        // product's A operand) and as the dS tile in shared memory (the dQ
+        // product's A operand).
         const int r = warp * 32 + lane;  // key row within the tile = TMEM lane
         const int key = kj0 + r;
         const bool key_ok = key < p.Nk;
@@ -496,9 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int first_vis = key - p.causal_off;  // causal: query q sees this key iff q >= first_vis
         bool ok = true;
         for (int it = 0; it < n_iter; ++it) {
-            // dP^T(it) was issued after the dQ warpgroup had taken dQ_{it-1} out of
-            // the dS tile, so the tile in shared memory is free as well.  The
-            // stage's L and D arrived with its Q and dO tiles (q_full).
+            // the stage's L and D arrived with its Q and dO tiles (q_full)
             ok = wait_or_abort(bars.s_full(), it & 1, abort_flag) &&
                  wait_or_abort(bars.q_full(it & 1), (it >> 1) & 1, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
@@ -508,45 +525,74 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool diag = p.causal && (kj0 + kTile - 1 > i0 + p.causal_off);
             const float4* L4 = reinterpret_cast<const float4*>(smem + C::kLdOff + (it & 1) * 1024);
             const float4* D4 = L4 + 32;
-#pragma unroll 1
+            uint32_t pk[64];  // P^T row as bf16 pairs, 128 queries
+            // ---- phase A
+#pragma unroll
             for (int hf = 0; hf < 2; ++hf) {  // 64 queries at a time
-                uint32_t s0[32], s1[32], d0[32], d1[32];
+                uint32_t s0[32], s1[32];
                 tmem_ld32(tS + hf * 64, s0);
                 tmem_ld32(tS + hf * 64 + 32, s1);
-                tmem_ld32(tDP + hf * 64, d0);
-                tmem_ld32(tDP + hf * 64 + 32, d1);
                 tmem_wait_ld_into(s0, s1);
-                after_wait_ld(d0, d1);
-                uint32_t pk[32], dk[32];
 #pragma unroll
-                for (int c4 = 0; c4 < 16; ++c4) {  // four queries per shared-memory read
-                    // L and D of these queries: the same address in every lane
-                    const float4 l4 = L4[hf * 16 + c4];
-                    const float4 dd4 = D4[hf * 16 + c4];
+                for (int c4 = 0; c4 < 16; ++c4) {
+                    const float4 l4 = L4[hf * 16 + c4];  // same address in every lane
                     const float lq[4] = {l4.x, l4.y, l4.z, l4.w};
-                    const float dq[4] = {dd4.x, dd4.y, dd4.z, dd4.w};
-                    float pv[4], dsv[4];
+                    float pv[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int c = c4 * 4 + e;  // column within the 64
                         const uint32_t sv = c < 32 ? s0[c] : s1[c - 32];
-                        const uint32_t dv = c < 32 ? d0[c] : d1[c - 32];
                         float pe = ex2_approx(fmaf(__uint_as_float(sv), cl2, -lq[e]));
                         if (!key_ok || (diag && i0 + hf * 64 + c < first_vis)) pe = 0.f;
                         pv[e] = pe;
+                    }
+                    pk[hf * 32 + 2 * c4] = pack_bf16x2(pv[0], pv[1]);
+                    pk[hf * 32 + 2 * c4 + 1] = pack_bf16x2(pv[2], pv[3]);
+                }
+                // packed columns hf*32.. lie below the fp32 columns still to be read
+                tmem_st16(tS + hf * 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[hf * 32]));
+                tmem_st16(tS + hf * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[hf * 32 + 16]));
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.pa_ready());
+            // ---- phase B
+            ok = wait_or_abort(bars.dp_full(), it & 1, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t d0[32], d1[32];
+                tmem_ld32(tDP + hf * 64, d0);
+                tmem_ld32(tDP + hf * 64 + 32, d1);
+                tmem_wait_ld_into(d0, d1);
+                uint32_t dk[32];
+#pragma unroll
+                for (int c4 = 0; c4 < 16; ++c4) {
+                    const float4 dd4 = D4[hf * 16 + c4];  // same address in every lane
+                    const float dq[4] = {dd4.x, dd4.y, dd4.z, dd4.w};
+                    float dsv[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int c = c4 * 4 + e;
+                        const uint32_t dv = c < 32 ? d0[c] : d1[c - 32];
+                        const uint32_t pp = pk[hf * 32 + (c >> 1)];
+                        const float pe = __uint_as_float((c & 1) ? (pp & 0xffff0000u) : (pp << 16));
                         dsv[e] = pe * (__uint_as_float(dv) - dq[e]);
                     }
-                    pk[2 * c4] = pack_bf16x2(pv[0], pv[1]);
-                    pk[2 * c4 + 1] = pack_bf16x2(pv[2], pv[3]);
                     dk[2 * c4] = pack_bf16x2(dsv[0], dsv[1]);
                     dk[2 * c4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
                 }
-                // P^T and dS^T over the first 64 columns of S^T and dP^T: packed
-                // columns hf*32.. lie below the fp32 columns still to be read
-                tmem_st16(tS + hf * 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-                tmem_st16(tS + hf * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
                 tmem_st16(tDP + hf * 32, *reinterpret_cast<uint32_t(*)[16]>(&dk[0]));
                 tmem_st16(tDP + hf * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&dk[16]));
+                // the dS tile: the dQ warpgroup has added dQ_{i-1} out of it
+                if (hf == 0 && it > 0) {
+                    ok = wait_or_abort(bars.ds_free(), (it - 1) & 1, abort_flag);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                }
                 // dS as the MN-major A operand of dQ_i = dS K_j: row r holds 64
                 // queries per 16 KB half, its 16-byte chunks permuted by the
                 // 128-byte swizzle (chunk ^ (row % 8))
@@ -556,11 +602,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<uint4*>(row + ((x ^ (r & 7)) * 16)) =
                         make_uint4(dk[4 * x], dk[4 * x + 1], dk[4 * x + 2], dk[4 * x + 3]);
             }
+            if (!ok) break;
             tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bars.p_ready());
+            if (lane == 0) mbar_arrive(bars.pb_ready());
         }
         // ---- epilogue: dV_j and dK_j rows (dK scaled), bf16
         if (ok) {
@@ -592,57 +639,66 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        setmaxnreg_dec<kOtherRegs>();
+        setmaxnreg_dec<kDqRegs>();
         // ===================================================== query rows: dQ_i
-        // dQ_i leaves Tensor Memory through the dS tile (free once the dQ product
-        // has read it): 32-column fp32 boxes of 128 rows in the 128-byte swizzle
-        // layout, two at a time, each added to the accumulator by one TMA
-        // reduce-add.
+        // All of dQ_i comes out of Tensor Memory into registers at once (its
+        // columns are then free for the next dP^T); it is then added to the
+        // accumulator through the dS tile (free once the dQ product has read
+        // it): 32-column fp32 boxes of 128 rows in the 128-byte swizzle layout,
+        // two at a time, each added by one TMA reduce-add.
         const int wq = warp - 4;
         const int r = wq * 32 + lane;  // query row within the tile = TMEM lane
         const uint32_t tQ = tmem + (static_cast<uint32_t>(wq * 32) << 16) + C::kColDQ;
         const bool leader = threadIdx.x == 4 * 32;
-        constexpr int kBoxBytes = 128 * 128;         // 128 rows x 32 fp32
+        constexpr int kBoxBytes = 128 * 128;  // 128 rows x 32 fp32
         constexpr int kBoxes = D / 32;
-        constexpr int kBoxesPerRound = 2;            // the dS tile holds two boxes
         bool ok = true;
         for (int it = 0; it < n_iter; ++it) {
             ok = dq_group_all(wait_or_abort(bars.dq_full(), it & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
+            uint32_t v[kBoxes][32];
+#pragma unroll
+            for (int bx = 0; bx < kBoxes; ++bx) tmem_ld32(tQ + bx * 32, v[bx]);
+            if constexpr (kBoxes == 4) {
+                tmem_wait_ld_into(v[0], v[1]);
+                after_wait_ld(v[2], v[3]);
+            } else {
+                tmem_wait_ld_into(v[0], v[1]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.dq_free());
             const int q0 = (i_first + it) * kTile;
-#pragma unroll 1
-            for (int b0 = 0; b0 < kBoxes; b0 += kBoxesPerRound) {
+#pragma unroll
+            for (int b0 = 0; b0 < kBoxes; b0 += 2) {
                 if (b0 > 0) {
                     // the previous round's boxes have been read out of shared memory
                     if (leader) bulk_wait_read_all();
                     dq_group_sync();
                 }
 #pragma unroll
-                for (int bb = 0; bb < kBoxesPerRound; ++bb) {
-                    uint32_t v[32];
-                    tmem_ld32(tQ + (b0 + bb) * 32, v);
-                    tmem_wait_ld_into(v);
+                for (int bb = 0; bb < 2; ++bb) {
                     uint8_t* row = smem + C::kDsOff + bb * kBoxBytes + r * 128;
 #pragma unroll
                     for (int x = 0; x < 8; ++x)
                         *reinterpret_cast<uint4*>(row + ((x ^ (r & 7)) * 16)) =
-                            make_uint4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+                            make_uint4(v[b0 + bb][4 * x], v[b0 + bb][4 * x + 1],
+                                       v[b0 + bb][4 * x + 2], v[b0 + bb][4 * x + 3]);
                 }
                 fence_proxy_async_smem();
                 dq_group_sync();
                 if (leader) {
-                    for (int bb = 0; bb < kBoxesPerRound; ++bb)
+                    for (int bb = 0; bb < 2; ++bb)
                         tma_reduce_add_3d(&tm_dqacc, sDs + bb * kBoxBytes, (b0 + bb) * 32, q0, bh);
                     bulk_commit();
                 }
             }
-            // dQ_i has left Tensor Memory; the dS tile is free once the last
-            // round's boxes have been read
-            if (leader) bulk_wait_read_all();
-            dq_group_sync();
-            tc_fence_before();
-            if (lane == 0) mbar_arrive(bars.dq_free());
+            // the dS tile is free once the last boxes have been read
+            if (leader) {
+                bulk_wait_read_all();
+                mbar_arrive(bars.ds_free());
+            }
         }
         // the reduce-adds must be complete before the CTA exits
         if (leader) bulk_wait_all();
