@@ -8,9 +8,10 @@
 //     dQ_i += scale dS_ij K_j,   dK_j += scale dS_ij^T Q_i.
 //
 // Three kernels, in stream order:
-//   * prep: D_i and L_i log2(e) for every query row, padded to whole 128-row
-//     tiles (padded rows get D = 0 and L = +inf, so their P is 0), and a
-//     zeroed fp32 dQ accumulator;
+//   * prep: -D_i and -L_i log2(e) for every query row (negated for the fused
+//     multiply-adds that use them), padded to whole 128-row tiles (padded rows
+//     get D = 0 and L = +inf, so their P is 0), and a zeroed fp32 dQ
+//     accumulator;
 //   * main: one CTA per (b, h, 128-key tile j), key/value-outer as in the
 //     notes' FlashAttention-2 form.  K_j and V_j stay in shared memory; for
 //     every query tile i that can see the key tile, TMA brings Q_i and dO_i
@@ -63,15 +64,15 @@ struct BCfg {
     static constexpr int kVOff = kTileBytes;
     static constexpr int kRingOff = 2 * kTileBytes;   // stage s: Q_i, then dO_i
     static constexpr int kDsOff = kRingOff + 4 * kTileBytes;  // dS, 128 keys x 128 queries bf16
-    // stage s: L log2(e) and D of the stage's 128 queries (fp32, 512 B each)
+    // stage s: -L log2(e) and -D of the stage's 128 queries (fp32, 512 B each)
     static constexpr int kLdOff = kDsOff + 2 * kSubBytes;
     static constexpr int kTilesBytes = kLdOff + 2 * 1024;
-    // Barriers, the TMEM address slot and the abort flag (112 bytes) go into
+    // Barriers, the TMEM address slot and the abort flag (128 bytes) go into
     // the gap below the 1024-byte aligned tiles when it has room, else after
     // them.  The dynamic shared memory base is 16-byte aligned, so the gap is
     // at most 1008 bytes: the allocation covers both cases.
-    static constexpr int kNumBars = 13;
-    static constexpr int kSmallBytes = 112;
+    static constexpr int kNumBars = 14;
+    static constexpr int kSmallBytes = 128;
     static constexpr int kSmemBytes =
         kTilesBytes + (1008 > kSmallBytes + 80 ? 1008 : kSmallBytes + 80);
     // Tensor Memory columns.  S^T is overwritten by P^T (bf16 pairs, first 64
@@ -94,11 +95,12 @@ struct BBars {
     __device__ uint32_t s_full() const { return base + 8u * 5; }    // S^T in TMEM
     __device__ uint32_t dp_full() const { return base + 8u * 6; }   // dP^T in TMEM
     __device__ uint32_t pa_ready() const { return base + 8u * 7; }  // P^T written
-    __device__ uint32_t pb_ready() const { return base + 8u * 8; }  // dS^T and dS written
-    __device__ uint32_t dq_full() const { return base + 8u * 9; }   // dQ_i in TMEM
-    __device__ uint32_t dq_free() const { return base + 8u * 10; }  // dQ_i out of TMEM
-    __device__ uint32_t ds_free() const { return base + 8u * 11; }  // dS tile free again
-    __device__ uint32_t done() const { return base + 8u * 12; }
+    __device__ uint32_t pb_tmem() const { return base + 8u * 8; }   // dS^T written (TMEM)
+    __device__ uint32_t pb_smem() const { return base + 8u * 9; }   // dS tile written (smem)
+    __device__ uint32_t dq_full() const { return base + 8u * 10; }  // dQ_i in TMEM
+    __device__ uint32_t dq_free() const { return base + 8u * 11; }  // dQ_i out of TMEM
+    __device__ uint32_t ds_free() const { return base + 8u * 12; }  // dS tile free again
+    __device__ uint32_t done() const { return base + 8u * 13; }
 };
 
 __device__ __forceinline__ void flag_abort(volatile int* abort_flag) {
@@ -191,6 +193,17 @@ __device__ __forceinline__ void after_wait_ld(uint32_t (&a)[32], uint32_t (&b)[3
                  : "memory");
 }
 
+// Element-wise product of fp32 pairs (one packed instruction).
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    float2 r;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
 // Barrier 1 among the 128 threads of the dQ warpgroup (barrier 0 is
 // __syncthreads).
 __device__ __forceinline__ void dq_group_sync() {
@@ -228,6 +241,11 @@ __device__ __forceinline__ void bulk_commit() {
 __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// All but the most recent of this thread's committed bulk copies have read
+// their shared-memory sources.
+__device__ __forceinline__ void bulk_wait_read_but_one() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 // This thread's committed bulk copies have completed.
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -247,8 +265,8 @@ __device__ __forceinline__ uint4 bf16x8(const float* x) {
 
 // ----------------------------------------------------------------- prep kernel
 //
-// Row i of head bh (i < Nq_pad): D_i = sum_c dO_ic O_ic in fp32 and
-// L2_i = lse_i log2(e); rows i >= Nq get D = 0 and L2 = +inf.  The fp32 dQ
+// Row i of head bh (i < Nq_pad): -D_i with D_i = sum_c dO_ic O_ic in fp32 and
+// -lse_i log2(e); rows i >= Nq get 0 and -inf.  The fp32 dQ
 // accumulator row is zeroed.  D / 8 consecutive threads share a row (16-byte
 // loads); the trip count is rounded up to whole warps so the row sum's
 // shuffles always see the full warp.
@@ -287,10 +305,10 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(BwdPrepParams a) {
             z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
             z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (c == 0) {
-                a.Dd[row] = acc;
-                a.lse2[row] = i < a.Nq
-                                  ? a.lse[static_cast<size_t>(bh) * a.Nq + i] * 1.4426950408889634f
-                                  : INFINITY;
+                a.nD[row] = -acc;
+                a.nl2[row] = i < a.Nq
+                                 ? a.lse[static_cast<size_t>(bh) * a.Nq + i] * -1.4426950408889634f
+                                 : -INFINITY;
             }
         }
     }
@@ -354,7 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bars.s_full(), 1);
         mbar_init(bars.dp_full(), 1);
         mbar_init(bars.pa_ready(), 4);  // one arrival per key-row warp
-        mbar_init(bars.pb_ready(), 4);
+        mbar_init(bars.pb_tmem(), 4);
+        mbar_init(bars.pb_smem(), 4);
         mbar_init(bars.dq_full(), 1);
         mbar_init(bars.dq_free(), 4);   // one arrival per dQ warp
         mbar_init(bars.ds_free(), 1);   // the dQ warpgroup's TMA thread
@@ -395,8 +414,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t dst = sRing + s * 2 * C::kTileBytes;
                 const int y = (i_first + it) * kTile;
                 const size_t row0 = static_cast<size_t>(bh) * p.Nq_pad + y;
-                bulk_load(sLd + s * 1024, p.lse2 + row0, 512, bars.q_full(s));
-                bulk_load(sLd + s * 1024 + 512, p.Dd + row0, 512, bars.q_full(s));
+                bulk_load(sLd + s * 1024, p.nl2 + row0, 512, bars.q_full(s));
+                bulk_load(sLd + s * 1024 + 512, p.nD + row0, 512, bars.q_full(s));
                 for (int sub = 0; sub < C::kSub; ++sub) {
                     tma_load_3d(dst + sub * C::kSubBytes, &tm_q, bars.q_full(s), sub * 64, y, bh);
                     tma_load_3d(dst + C::kTileBytes + sub * C::kSubBytes, &tm_do, bars.q_full(s),
@@ -414,11 +433,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ===================================================== MMA issuer
-        // Per step i (stage s), with S^T(i) issued at the end of step i - 1:
+        // Per step i (stage s), with S^T(i) issued during step i - 1:
         //   [dQ_{i-1} out of TMEM]  dP^T -> dp_full
         //   [P^T written]           dV += P^T dO_i
-        //   [dS^T, dS written]      dK += dS^T Q_i -> q_empty(s);  dQ_i = dS K_j -> dq_full
         //   [Q_{i+1} loaded]        S^T(i+1) -> s_full
+        //   [dS^T written]          dK += dS^T Q_i -> q_empty(s)
+        //   [dS tile written]       dQ_i = dS K_j -> dq_full
         // dQ_i lands in the dP^T columns after the dK product has read dS^T from
         // them, S^T(i+1) in the S^T columns after the dV product has read P^T
         // (one thread's MMAs run in issue order); only dP^T(i+1) waits for the
@@ -469,19 +489,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < kTile / 16; ++kk)
                     umma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8, ddo_mn + ((kk * 2048) >> 4),
                             id_acc, (it > 0 || kk > 0) ? 1u : 0u);
-                if (!(ok = wait_or_abort(bars.pb_ready(), it & 1, abort_flag))) break;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)
-                    umma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8, dq_mn + ((kk * 2048) >> 4),
-                            id_acc, (it > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(bars.q_empty(s));
-                // K = 128 keys in steps of 16 rows of the dS and K_j tiles
-#pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)
-                    umma_ss(tmem + C::kColDQ, dds_mn + ((kk * 2048) >> 4), dk_mn + ((kk * 2048) >> 4),
-                            id_dq, kk > 0 ? 1u : 0u);
-                umma_commit(bars.dq_full());
+                // S^T(i+1) right behind the dV product that read P^T(i): the key-row
+                // warps start on it as soon as they are done with dS(i)
                 if (it + 1 < n_iter) {
                     if (!(ok = wait_or_abort(bars.q_full((it + 1) & 1), ((it + 1) >> 1) & 1,
                                              abort_flag)))
@@ -489,6 +498,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     issue_s(it + 1);
                 }
+                if (!(ok = wait_or_abort(bars.pb_tmem(), it & 1, abort_flag))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    umma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8, dq_mn + ((kk * 2048) >> 4),
+                            id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(bars.q_empty(s));
+                if (!(ok = wait_or_abort(bars.pb_smem(), it & 1, abort_flag))) break;
+                tc_fence_after();
+                // K = 128 keys in steps of 16 rows of the dS and K_j tiles
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    umma_ss(tmem + C::kColDQ, dds_mn + ((kk * 2048) >> 4), dk_mn + ((kk * 2048) >> 4),
+                            id_dq, kk > 0 ? 1u : 0u);
+                umma_commit(bars.dq_full());
             }
             // every MMA this thread issued has completed once `done` flips
             umma_commit(bars.done());
@@ -526,7 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float4* L4 = reinterpret_cast<const float4*>(smem + C::kLdOff + (it & 1) * 1024);
             const float4* D4 = L4 + 32;
             uint32_t pk[64];  // P^T row as bf16 pairs, 128 queries
-            // ---- phase A
+            // ---- phase A: p = 2^{s c - L log2 e}, pairs of columns per instruction
+            const float2 c2 = make_float2(cl2, cl2);
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {  // 64 queries at a time
                 uint32_t s0[32], s1[32];
@@ -536,18 +561,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c4 = 0; c4 < 16; ++c4) {
                     const float4 l4 = L4[hf * 16 + c4];  // same address in every lane
-                    const float lq[4] = {l4.x, l4.y, l4.z, l4.w};
-                    float pv[4];
+                    const int c = c4 * 4;                 // column within the 64
+                    auto sv = [&](int e) { return __uint_as_float(c < 32 ? s0[c + e] : s1[c - 32 + e]); };
+                    const float2 x0 = ffma2(make_float2(sv(0), sv(1)), c2, make_float2(l4.x, l4.y));
+                    const float2 x1 = ffma2(make_float2(sv(2), sv(3)), c2, make_float2(l4.z, l4.w));
+                    float pv[4] = {ex2_approx(x0.x), ex2_approx(x0.y), ex2_approx(x1.x),
+                                   ex2_approx(x1.y)};
+                    if (diag) {  // tiles that straddle the causal boundary
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int c = c4 * 4 + e;  // column within the 64
-                        const uint32_t sv = c < 32 ? s0[c] : s1[c - 32];
-                        float pe = ex2_approx(fmaf(__uint_as_float(sv), cl2, -lq[e]));
-                        if (!key_ok || (diag && i0 + hf * 64 + c < first_vis)) pe = 0.f;
-                        pv[e] = pe;
+                        for (int e = 0; e < 4; ++e)
+                            if (i0 + hf * 64 + c + e < first_vis) pv[e] = 0.f;
                     }
                     pk[hf * 32 + 2 * c4] = pack_bf16x2(pv[0], pv[1]);
                     pk[hf * 32 + 2 * c4 + 1] = pack_bf16x2(pv[2], pv[3]);
+                }
+                if (!key_ok) {  // rows past the last key
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) pk[hf * 32 + x] = 0u;
                 }
                 // packed columns hf*32.. lie below the fp32 columns still to be read
                 tmem_st16(tS + hf * 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[hf * 32]));
@@ -562,52 +592,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
+            uint32_t dk[64];  // dS^T row as bf16 pairs, 128 queries
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 uint32_t d0[32], d1[32];
                 tmem_ld32(tDP + hf * 64, d0);
                 tmem_ld32(tDP + hf * 64 + 32, d1);
                 tmem_wait_ld_into(d0, d1);
-                uint32_t dk[32];
 #pragma unroll
-                for (int c4 = 0; c4 < 16; ++c4) {
-                    const float4 dd4 = D4[hf * 16 + c4];  // same address in every lane
-                    const float dq[4] = {dd4.x, dd4.y, dd4.z, dd4.w};
-                    float dsv[4];
+                for (int c2i = 0; c2i < 32; ++c2i) {  // pairs of columns
+                    const float2 nd = reinterpret_cast<const float2*>(D4)[hf * 32 + c2i];  // -D, broadcast
+                    const int c = 2 * c2i;
+                    auto dv = [&](int e) { return __uint_as_float(c < 32 ? d0[c + e] : d1[c - 32 + e]); };
+                    const uint32_t pp = pk[hf * 32 + c2i];
+                    const float2 pe = make_float2(__uint_as_float(pp << 16),
+                                                  __uint_as_float(pp & 0xffff0000u));
+                    const float2 t = fadd2(make_float2(dv(0), dv(1)), nd);
+                    const float2 ds = fmul2(pe, t);
+                    dk[hf * 32 + c2i] = pack_bf16x2(ds.x, ds.y);
+                }
+                tmem_st16(tDP + hf * 32, *reinterpret_cast<uint32_t(*)[16]>(&dk[hf * 32]));
+                tmem_st16(tDP + hf * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&dk[hf * 32 + 16]));
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.pb_tmem());
+            // the dS tile, once the dQ warpgroup has added dQ_{i-1} out of it: the
+            // MN-major A operand of dQ_i = dS K_j; row r holds 64 queries per 16 KB
+            // half, its 16-byte chunks permuted by the 128-byte swizzle (chunk ^ (row % 8))
+            if (it > 0) {
+                ok = wait_or_abort(bars.ds_free(), (it - 1) & 1, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+            }
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int c = c4 * 4 + e;
-                        const uint32_t dv = c < 32 ? d0[c] : d1[c - 32];
-                        const uint32_t pp = pk[hf * 32 + (c >> 1)];
-                        const float pe = __uint_as_float((c & 1) ? (pp & 0xffff0000u) : (pp << 16));
-                        dsv[e] = pe * (__uint_as_float(dv) - dq[e]);
-                    }
-                    dk[2 * c4] = pack_bf16x2(dsv[0], dsv[1]);
-                    dk[2 * c4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
-                }
-                tmem_st16(tDP + hf * 32, *reinterpret_cast<uint32_t(*)[16]>(&dk[0]));
-                tmem_st16(tDP + hf * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&dk[16]));
-                // the dS tile: the dQ warpgroup has added dQ_{i-1} out of it
-                if (hf == 0 && it > 0) {
-                    ok = wait_or_abort(bars.ds_free(), (it - 1) & 1, abort_flag);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                }
-                // dS as the MN-major A operand of dQ_i = dS K_j: row r holds 64
-                // queries per 16 KB half, its 16-byte chunks permuted by the
-                // 128-byte swizzle (chunk ^ (row % 8))
+            for (int hf = 0; hf < 2; ++hf) {
                 uint8_t* row = smem + C::kDsOff + hf * C::kSubBytes + r * 128;
 #pragma unroll
                 for (int x = 0; x < 8; ++x)
                     *reinterpret_cast<uint4*>(row + ((x ^ (r & 7)) * 16)) =
-                        make_uint4(dk[4 * x], dk[4 * x + 1], dk[4 * x + 2], dk[4 * x + 3]);
+                        make_uint4(dk[hf * 32 + 4 * x], dk[hf * 32 + 4 * x + 1],
+                                   dk[hf * 32 + 4 * x + 2], dk[hf * 32 + 4 * x + 3]);
             }
-            if (!ok) break;
-            tmem_wait_st();
             fence_proxy_async_smem();
-            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bars.pb_ready());
+            if (lane == 0) mbar_arrive(bars.pb_smem());
         }
         // ---- epilogue: dV_j and dK_j rows (dK scaled), bf16
         if (ok) {
@@ -645,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // columns are then free for the next dP^T); it is then added to the
         // accumulator through the dS tile (free once the dQ product has read
         // it): 32-column fp32 boxes of 128 rows in the 128-byte swizzle layout,
-        // two at a time, each added by one TMA reduce-add.
+        // each added by one TMA reduce-add, two in flight.
         const int wq = warp - 4;
         const int r = wq * 32 + lane;  // query row within the tile = TMEM lane
         const uint32_t tQ = tmem + (static_cast<uint32_t>(wq * 32) << 16) + C::kColDQ;
@@ -670,27 +700,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bars.dq_free());
             const int q0 = (i_first + it) * kTile;
+            // box bx goes through slot bx % 2 of the dS tile; a slot is rewritten
+            // once the box before the previous one has been read out of it
 #pragma unroll
-            for (int b0 = 0; b0 < kBoxes; b0 += 2) {
-                if (b0 > 0) {
-                    // the previous round's boxes have been read out of shared memory
-                    if (leader) bulk_wait_read_all();
+            for (int bx = 0; bx < kBoxes; ++bx) {
+                if (bx >= 2) {
+                    if (leader) bulk_wait_read_but_one();
                     dq_group_sync();
                 }
+                uint8_t* row = smem + C::kDsOff + (bx & 1) * kBoxBytes + r * 128;
 #pragma unroll
-                for (int bb = 0; bb < 2; ++bb) {
-                    uint8_t* row = smem + C::kDsOff + bb * kBoxBytes + r * 128;
-#pragma unroll
-                    for (int x = 0; x < 8; ++x)
-                        *reinterpret_cast<uint4*>(row + ((x ^ (r & 7)) * 16)) =
-                            make_uint4(v[b0 + bb][4 * x], v[b0 + bb][4 * x + 1],
-                                       v[b0 + bb][4 * x + 2], v[b0 + bb][4 * x + 3]);
-                }
+                for (int x = 0; x < 8; ++x)
+                    *reinterpret_cast<uint4*>(row + ((x ^ (r & 7)) * 16)) =
+                        make_uint4(v[bx][4 * x], v[bx][4 * x + 1], v[bx][4 * x + 2], v[bx][4 * x + 3]);
                 fence_proxy_async_smem();
                 dq_group_sync();
                 if (leader) {
-                    for (int bb = 0; bb < 2; ++bb)
-                        tma_reduce_add_3d(&tm_dqacc, sDs + bb * kBoxBytes, (b0 + bb) * 32, q0, bh);
+                    tma_reduce_add_3d(&tm_dqacc, sDs + (bx & 1) * kBoxBytes, bx * 32, q0, bh);
                     bulk_commit();
                 }
             }

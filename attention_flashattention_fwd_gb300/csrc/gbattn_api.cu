@@ -161,8 +161,8 @@ int enqueue_bwd(const void* q, const void* k, const void* v, const void* o, cons
     a.dout = static_cast<const __nv_bfloat16*>(dout);
     a.lse = lse;
     a.dq_acc = ws;
-    a.lse2 = ws + BH * nq_pad * d;
-    a.Dd = a.lse2 + BH * nq_pad;
+    a.nl2 = ws + BH * nq_pad * d;
+    a.nD = a.nl2 + BH * nq_pad;
     a.rows = BH * nq_pad;
     a.Nq = Nq;
     a.Nq_pad = nq_pad;
@@ -170,8 +170,8 @@ int enqueue_bwd(const void* q, const void* k, const void* v, const void* o, cons
     p.dk = static_cast<__nv_bfloat16*>(dk);
     p.dv = static_cast<__nv_bfloat16*>(dv);
     p.dq_acc = a.dq_acc;
-    p.lse2 = a.lse2;
-    p.Dd = a.Dd;
+    p.nl2 = a.nl2;
+    p.nD = a.nD;
     p.Nq = Nq;
     p.Nk = Nk;
     p.Nq_pad = nq_pad;

@@ -41,8 +41,8 @@ struct BwdPrepParams {
     const __nv_bfloat16* o;     // [BH, Nq, d]
     const __nv_bfloat16* dout;  // [BH, Nq, d]
     const float* lse;           // [BH, Nq], natural log
-    float* lse2;                // [BH, Nq_pad] lse * log2(e); +inf on padded rows
-    float* Dd;                  // [BH, Nq_pad] rowsum(dO * O); 0 on padded rows
+    float* nl2;                 // [BH, Nq_pad] -lse * log2(e); -inf on padded rows
+    float* nD;                  // [BH, Nq_pad] -rowsum(dO * O); 0 on padded rows
     float* dq_acc;              // [BH, Nq_pad, d], zeroed
     long long rows;             // BH * Nq_pad
     int Nq, Nq_pad;
@@ -53,8 +53,8 @@ struct BwdParams {
     __nv_bfloat16* dk;   // [BH, Nk, d]
     __nv_bfloat16* dv;   // [BH, Nk, d]
     float* dq_acc;       // [BH, Nq_pad, d]
-    const float* lse2;   // [BH, Nq_pad]
-    const float* Dd;     // [BH, Nq_pad]
+    const float* nl2;    // [BH, Nq_pad] -lse * log2(e)
+    const float* nD;     // [BH, Nq_pad] -D
     int Nq, Nk, Nq_pad, BH;
     int n_kt;            // key tiles per head: ceil(Nk / 128)
     int causal, causal_off;
