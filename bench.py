@@ -55,6 +55,8 @@ def parse_args():
                     help="run only this workload's kernel(s) (profiling runs); prints its time")
     ap.add_argument("--shape", default=None,
                     help="with --case custom: B,H,Nq,Nk,d,causal of a profiling workload")
+    ap.add_argument("--pass", dest="which", choices=["fwd", "bwd"], default="fwd",
+                    help="with --case: time the forward (default) or the backward call")
     a = ap.parse_args()
     a.warmup = max(3, a.warmup)
     a.steps = max(1, a.steps)
@@ -81,6 +83,10 @@ def _sources_sha(names):
 
 PREFILL_SOURCES = ["prefill_sm103.cu", "sm103_ptx.cuh"]
 DECODE_SOURCES = ["decode_sm103.cu", "sm103_ptx.cuh"]
+BACKWARD_SOURCES = ["backward_sm103.cu", "sm103_ptx.cuh"]
+# FLOPs of the backward: five products of the forward's size (S and dP
+# recomputed, dV, dK, dQ) against the forward's two.
+BWD_FLOP_RATIO = 2.5
 
 
 def profiled_traffic(profile_name, sources):
@@ -311,6 +317,22 @@ def run_case(args):
         else:
             binding.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)
 
+    flop_ratio = 1.0
+    if args.which == "bwd":
+        if w.decode:
+            raise SystemExit("--pass bwd needs a prefill workload")
+        launch()  # o, lse of these inputs
+        g = torch.Generator(device=dev).manual_seed(w.seed + 7)
+        dout = torch.randn(q.shape, generator=g, device=dev).to(torch.bfloat16)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        bws = torch.empty(binding.bwd_workspace_bytes(w.B, w.H, w.Nq, w.Nk, w.d),
+                          dtype=torch.uint8, device=dev)
+        flop_ratio = BWD_FLOP_RATIO
+
+        def launch():  # noqa: F811  (the timed call is the backward)
+            binding.attn_bwd(q, k, v, o, lse, dout, causal=w.causal, scale=w.scale, dq=dq, dk=dk,
+                             dv=dv, workspace=bws)
+
     for _ in range(args.warmup):
         launch()
     torch.cuda.synchronize()
@@ -324,10 +346,11 @@ def run_case(args):
     ms = e0.elapsed_time(e1) / args.steps
     if binding.device_error() != 0:
         raise RuntimeError("a kernel reported a device-side error")
-    val = (w.algorithmic_bytes() / ms / 1e6, "GB/s") if w.decode else (w.flops() / ms / 1e9,
-                                                                         "TFLOP/s")
-    print(json.dumps({"case": w.name, "ms_per_launch": ms, "value": val[0], "unit": val[1],
-                      "steps": args.steps, "warmup": args.warmup, "l2": "not flushed"}))
+    val = (w.algorithmic_bytes() / ms / 1e6, "GB/s") if w.decode else (
+        flop_ratio * w.flops() / ms / 1e9, "TFLOP/s")
+    print(json.dumps({"case": w.name, "pass": args.which, "ms_per_launch": ms, "value": val[0],
+                      "unit": val[1], "steps": args.steps, "warmup": args.warmup,
+                      "l2": "not flushed"}))
 
 
 def run_gpu(args):
@@ -456,6 +479,50 @@ def run_gpu(args):
            "ms_per_step": e2e_ms / e2e_steps,
            "path": "attn_fwd_from_host (pinned host q,k,v -> device -> kernel -> host o,lse)"}
 
+    # ---- the backward pass (next-row widening; not part of the timed step):
+    # attn_bwd on the headline workload with the step's own o and lse, timed
+    # call by call with CUDA events after an L2 flush
+    g = torch.Generator(device=dev).manual_seed(w3.seed + 7)
+    dout3 = torch.randn(q3.shape, generator=g, device=dev).to(torch.bfloat16)
+    dq3, dk3, dv3 = torch.empty_like(q3), torch.empty_like(k3), torch.empty_like(v3)
+    bws = torch.empty(binding.bwd_workspace_bytes(w3.B, w3.H, w3.Nq, w3.Nk, w3.d),
+                      dtype=torch.uint8, device=dev)
+    binding.attn_fwd(q3, k3, v3, causal=True, scale=w3.scale, out=o3, lse=l3, stream=stream)
+
+    def bwd_call():
+        binding.attn_bwd(q3, k3, v3, o3, l3, dout3, causal=True, scale=w3.scale, dq=dq3, dk=dk3,
+                         dv=dv3, workspace=bws, stream=stream)
+
+    for _ in range(3):
+        bwd_call()
+    torch.cuda.synchronize()
+    bwd_reps = min(K, 20)
+    bwd_ms = 0.0
+    for _ in range(bwd_reps):
+        flush.zero_()
+        torch.cuda._sleep(LAUNCH_COVER_CYCLES)
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        bwd_call()
+        b1.record(stream)
+        torch.cuda.synchronize()
+        bwd_ms += b0.elapsed_time(b1)
+    if binding.device_error() != 0:
+        raise RuntimeError("a kernel reported a device-side error in the backward")
+    (bwd_ms,) = max_over_ranks([bwd_ms], world, device=dev)
+    bwd_per = bwd_ms / bwd_reps
+    bwd_flops = BWD_FLOP_RATIO * w3.flops()
+    bwd_tf = bwd_flops / (bwd_per * 1e-3) / 1e12
+    backward = {
+        "workload": w3.name, "value": world * bwd_tf, "unit": "TFLOP/s", "ms_per_call": bwd_per,
+        "calls": bwd_reps, "flops_per_call": bwd_flops,
+        "timed": "attn_bwd call: prep + main + dQ convert kernels, L2 flushed before each call",
+        "roofline": {"bound": "tensor", "achieved": bwd_tf, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": bwd_tf / peaks["bf16_tflops"],
+                     "traffic": profiled_traffic("ncu_backward_" + HEADLINE, BACKWARD_SOURCES),
+                     "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)"},
+    }
+
     line = {
         "metric": METRIC, "value": p3["value"], "unit": "TFLOP/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": total_ms / K,
@@ -468,6 +535,7 @@ def run_gpu(args):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": p3["roofline"],
         "parts": {HEADLINE: p3, LONG: p4, DECODE: p5},
+        "backward": backward,
         "e2e": e2e,
         "clocks": clocks,
         "gpu_launches": launches_per_step * K,
