@@ -48,6 +48,8 @@ def load():
         lib.attn_bwd_workspace_bytes.restype = S
         lib.attn_bwd.argtypes = [P] * 9 + [I, I, I, I, I, I, F, P, S, P]
         lib.attn_bwd.restype = I
+        lib.attn_merge.argtypes = [P, P, I, P, P, I, I, I, I, P]
+        lib.attn_merge.restype = I
         lib.attn_status_string.argtypes = [I]
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_device_error.argtypes = []
@@ -167,6 +169,26 @@ def attn_fwd_from_host(q, k, v, o, lse, dq, dk, dv, do_, dlse, causal=False, sca
                                    int(bool(causal)), float(scale), _stream_ptr(stream))
     _check(st, "attn_fwd_from_host")
     return o, lse
+
+
+def attn_merge(o_parts, lse_parts, out=None, lse=None, stream=None):
+    """The C entry point ``attn_merge``: attention over all keys from the
+    results over disjoint key sets.  o_parts bf16 [S, B, H, Nq, d] and
+    lse_parts fp32 [S, B, H, Nq], CUDA, contiguous.  Returns (o, lse)."""
+    if o_parts.dim() != 5 or lse_parts.shape != o_parts.shape[:4]:
+        raise ValueError("o_parts must be [S, B, H, Nq, d] and lse_parts [S, B, H, Nq]")
+    for name, t, dt in (("o_parts", o_parts, torch.bfloat16), ("lse_parts", lse_parts, torch.float32)):
+        if not t.is_cuda or t.dtype != dt or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {dt} CUDA tensor")
+    S, B, H, Nq, d = o_parts.shape
+    if out is None:
+        out = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=o_parts.device)
+    st = load().attn_merge(_ptr(o_parts), _ptr(lse_parts), S, _ptr(out), _ptr(lse), B, H, Nq, d,
+                           _stream_ptr(stream))
+    _check(st, "attn_merge")
+    return out, lse
 
 
 def bwd_workspace_bytes(B, H, Nq, Nk, d) -> int:

@@ -259,6 +259,28 @@ int attn_fwd_from_host(const void* q, const void* k, const void* v, void* o, flo
     return ATTN_OK;
 }
 
+int attn_merge(const void* o_parts, const float* lse_parts, int n_parts, void* o, float* lse,
+               int B, int H, int Nq, int d, void* stream) {
+    if (!o_parts || !lse_parts || !o || !lse) return ATTN_ERR_INVALID_ARG;
+    if (n_parts <= 0 || B <= 0 || H <= 0 || Nq <= 0) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    const long long rows = static_cast<long long>(B) * H * Nq;
+    if (rows > (1LL << 40) / n_parts) return ATTN_ERR_UNSUPPORTED;  // index range
+    if (!aligned16(o_parts) || !aligned16(lse_parts) || !aligned16(o) || !aligned16(lse))
+        return ATTN_ERR_MISALIGNED;
+    int num_sms = 0;
+    const int st = current_sm_count(&num_sms);
+    if (st != ATTN_OK) return st;
+    MergeParams p;
+    p.o_parts = static_cast<const __nv_bfloat16*>(o_parts);
+    p.lse_parts = lse_parts;
+    p.o = static_cast<__nv_bfloat16*>(o);
+    p.lse = lse;
+    p.rows = rows;
+    p.n_parts = n_parts;
+    return launch_merge(d, p, num_sms, static_cast<cudaStream_t>(stream));
+}
+
 size_t attn_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
     if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || (d != 64 && d != 128)) return 0;
     return bwd_workspace_bytes(static_cast<long long>(B) * H, Nq, d);

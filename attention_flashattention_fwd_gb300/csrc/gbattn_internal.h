@@ -61,6 +61,16 @@ struct BwdParams {
     float scale, scale_log2;
 };
 
+// Arguments of the merge kernel.
+struct MergeParams {
+    const __nv_bfloat16* o_parts;  // [n_parts, rows, d]
+    const float* lse_parts;        // [n_parts, rows], natural log
+    __nv_bfloat16* o;              // [rows, d]
+    float* lse;                    // [rows]
+    long long rows;                // B * H * Nq
+    int n_parts;
+};
+
 // prefill_sm103.cu
 int prefill_set_attributes();
 // Persistent launch: min(work items, num_sms) CTAs, one per SM.
@@ -73,6 +83,9 @@ unsigned read_and_clear_prefill_error();
 void decode_split_plan(long long BH, int Nk, int* splits, int* keys_per_split);
 size_t decode_workspace_bytes(long long BH, int Nk, int d);
 int launch_decode(int d, const DecodeParams& p, cudaStream_t stream);
+
+// merge_sm103.cu
+int launch_merge(int d, const MergeParams& p, int num_sms, cudaStream_t stream);
 
 // backward_sm103.cu
 int bwd_set_attributes();

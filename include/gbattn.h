@@ -160,6 +160,34 @@ int attn_fwd_decode_no_alloc(const void *q, const void *k, const void *v, void *
                              int B, int H, int Nk, int d, float scale, void *stream);
 
 /*
+ * attn_merge -- attention over all keys from results over disjoint key sets.
+ *
+ * For every row (b, h, i), part s holds o_s = attention of query i over the
+ * keys of part s and its logsumexp lse_s (e.g. attn_fwd or attn_fwd_decode
+ * on one shard of k and v).  The merge is the two-block rule of the CS149
+ * Lecture 9 notes, concept 9 (m = max, l = sum of e^{m_s - m} l_s), applied
+ * to all parts:
+ *   lse = log sum_s e^{lse_s},    o = sum_s e^{lse_s - lse} o_s
+ * which is the attention over the union of the parts' keys.  This is the
+ * one exchange step of key- (context-) parallel attention: each rank attends
+ * to its shard of the keys, the (o_s, lse_s) are gathered, and this call
+ * merges them.  A part with lse_s = -inf (no visible key) has weight 0; a row
+ * whose parts are all -inf gets o = 0 and lse = -inf.
+ *
+ *   o_parts    device, bf16 [n_parts, B, H, Nq, d], contiguous; read only.
+ *   lse_parts  device, fp32 [n_parts, B, H, Nq] (natural log); read only.
+ *   o          device, bf16 [B, H, Nq, d]; written.
+ *   lse        device, fp32 [B, H, Nq]; written.
+ *   n_parts, B, H, Nq >= 1;  d in {64, 128};  stream cudaStream_t.
+ * Arithmetic in fp32, o rounded to bf16 (round-to-nearest-even).  Memory
+ * bound: reads n_parts * (2 d + 4) and writes 2 d + 4 bytes per row.
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED,
+ * ATTN_ERR_MISALIGNED or ATTN_ERR_CUDA.
+ */
+int attn_merge(const void *o_parts, const float *lse_parts, int n_parts, void *o, float *lse,
+               int B, int H, int Nq, int d, void *stream);
+
+/*
  * attn_bwd_workspace_bytes -- bytes of device workspace attn_bwd needs:
  * an fp32 dQ accumulator plus two fp32 values per query row, over whole
  * 128-row query tiles: B*H*ceil(Nq/128)*128*(d + 2)*4.  Pure host

@@ -142,3 +142,17 @@ def test_bwd_rejects_before_launch(lib):
     assert bwd(d=80) == UNSUPPORTED
     assert bwd(causal=1, Nq=256, Nk=128, ws_bytes=1 << 20) == UNSUPPORTED
     assert bwd(scale=float("nan")) == INVALID
+
+
+def test_merge_rejects_before_launch(lib):
+    P, I = ctypes.c_void_p, ctypes.c_int
+    lib.attn_merge.argtypes = [P, P, I, P, P, I, I, I, I, P]
+    lib.attn_merge.restype = I
+
+    def merge(op=FAKE, lp=FAKE, n=2, o=FAKE, lse=FAKE, B=1, H=1, Nq=4, d=64):
+        return lib.attn_merge(P(op), P(lp), n, P(o), P(lse), B, H, Nq, d, P(0))
+
+    assert merge(op=0) == INVALID and merge(lp=0) == INVALID and merge(o=0) == INVALID
+    assert merge(lse=0) == INVALID and merge(n=0) == INVALID and merge(Nq=0) == INVALID
+    assert merge(d=96) == UNSUPPORTED
+    assert merge(op=FAKE + 8) == MISALIGNED and merge(lse=FAKE + 4) == MISALIGNED

@@ -1,0 +1,62 @@
+"""attn_merge (the exchange step of key-sharded attention) against the fp64
+oracle: the keys of each head are split into uneven shards, each shard goes
+through the prefill or decode kernel, and the merged result must match
+attention over all keys within the forward's tolerances."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_flashattention_fwd_gb300 import binding
+from attention_flashattention_fwd_gb300.inputs import bf16_bits, make_qkv
+
+pytestmark = pytest.mark.gpu
+
+O_MAX, O_MEAN, LSE_MAX = 2e-2, 1e-3, 2e-3
+
+
+def _check(o, lse, ro, rl, what):
+    o = o.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    e, el = np.abs(o - ro), np.abs(lse - rl)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse)), what
+    assert e.max() <= O_MAX and e.mean() <= O_MEAN and el.max() <= LSE_MAX, (
+        f"{what}: O max {e.max():.3g} mean {e.mean():.3g} lse {el.max():.3g}")
+
+
+@pytest.mark.parametrize("B,H,Nq,split,d", [
+    (1, 2, 300, (128, 300, 77), 128),
+    (2, 3, 1, (700, 1000, 300, 48), 128),     # decode-shaped shards
+    (1, 4, 256, (512, 512), 64),
+    (1, 1, 77, (5,), 64),                     # one part: the identity
+])
+def test_sharded_attention_merges_to_full(B, H, Nq, split, d):
+    Nk = sum(split)
+    q, k, v = make_qkv(B, H, Nq, Nk, d, seed=61 + Nk, device="cuda")
+    o_parts, lse_parts = [], []
+    k0 = 0
+    for n in split:
+        ks, vs = k[:, :, k0:k0 + n].contiguous(), v[:, :, k0:k0 + n].contiguous()
+        o_s, l_s = binding.attention(q, ks, vs)
+        o_parts.append(o_s)
+        lse_parts.append(l_s)
+        k0 += n
+    o, lse = binding.attn_merge(torch.stack(o_parts), torch.stack(lse_parts))
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v))
+    _check(o, lse, ro, rl, f"{(B, H, Nq, split, d)}")
+
+
+def test_empty_parts_have_no_weight():
+    q, k, v = make_qkv(1, 2, 128, 256, 128, seed=67, device="cuda")
+    o1, l1 = binding.attn_fwd(q, k, v)
+    junk = torch.full_like(o1, 7.0)
+    ninf = torch.full_like(l1, float("-inf"))
+    o, lse = binding.attn_merge(torch.stack([junk, o1, junk]), torch.stack([ninf, l1, ninf]))
+    torch.cuda.synchronize()
+    assert torch.equal(lse, l1)
+    assert (o.float() - o1.float()).abs().max().item() <= 2 ** -8 * o1.float().abs().max().item()
+    # every part empty: o = 0, lse = -inf
+    o, lse = binding.attn_merge(torch.stack([junk, junk]), torch.stack([ninf, ninf]))
+    torch.cuda.synchronize()
+    assert (o.float() == 0).all() and torch.isinf(lse).all() and (lse < 0).all()
