@@ -84,6 +84,7 @@ def _sources_sha(names):
 PREFILL_SOURCES = ["prefill_sm103.cu", "sm103_ptx.cuh"]
 DECODE_SOURCES = ["decode_sm103.cu", "sm103_ptx.cuh"]
 BACKWARD_SOURCES = ["backward_sm103.cu", "sm103_ptx.cuh"]
+MERGE_PARTS = 4  # key shards merged by attn_merge in the context-parallel measurement
 # FLOPs of the backward: five products of the forward's size (S and dP
 # recomputed, dV, dK, dQ) against the forward's two.
 BWD_FLOP_RATIO = 2.5
@@ -523,6 +524,36 @@ def run_gpu(args):
                      "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)"},
     }
 
+    # ---- the exchange step of key-sharded attention (not part of the timed step):
+    # attn_merge of MERGE_PARTS shard results of the headline shape
+    o_parts = torch.stack([o3] * MERGE_PARTS).contiguous()
+    l_parts = torch.stack([l3 - float(s) for s in range(MERGE_PARTS)]).contiguous()
+    om, lm = torch.empty_like(o3), torch.empty_like(l3)
+    for _ in range(3):
+        binding.attn_merge(o_parts, l_parts, out=om, lse=lm, stream=stream)
+    torch.cuda.synchronize()
+    m_ms = 0.0
+    for _ in range(bwd_reps):
+        flush.zero_()
+        torch.cuda._sleep(LAUNCH_COVER_CYCLES)
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        binding.attn_merge(o_parts, l_parts, out=om, lse=lm, stream=stream)
+        b1.record(stream)
+        torch.cuda.synchronize()
+        m_ms += b0.elapsed_time(b1)
+    (m_ms,) = max_over_ranks([m_ms], world, device=dev)
+    m_per = m_ms / bwd_reps
+    m_bytes = (MERGE_PARTS + 1) * (o3.nbytes + l3.nbytes)
+    m_gbs = m_bytes / (m_per * 1e-3) / 1e9
+    merge = {
+        "workload": f"{MERGE_PARTS} shard results of {w3.name}", "value": world * m_gbs,
+        "unit": "GB/s", "ms_per_call": m_per, "calls": bwd_reps, "bytes_per_call": m_bytes,
+        "roofline": {"bound": "hbm", "achieved": m_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": m_gbs / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": f"{peak_src} HBM copy (MEASURED_PEAKS.json)"},
+    }
+
     line = {
         "metric": METRIC, "value": p3["value"], "unit": "TFLOP/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": total_ms / K,
@@ -536,6 +567,7 @@ def run_gpu(args):
         "roofline": p3["roofline"],
         "parts": {HEADLINE: p3, LONG: p4, DECODE: p5},
         "backward": backward,
+        "merge": merge,
         "e2e": e2e,
         "clocks": clocks,
         "gpu_launches": launches_per_step * K,
