@@ -48,6 +48,10 @@ def load():
         lib.attn_bwd_workspace_bytes.restype = S
         lib.attn_bwd.argtypes = [P] * 9 + [I, I, I, I, I, I, F, P, S, P]
         lib.attn_bwd.restype = I
+        lib.attn_fwd_ragged.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, P]
+        lib.attn_fwd_ragged.restype = I
+        lib.attn_fwd_decode_ragged.argtypes = [P, P, P, P, P, P, I, I, I, I, F, P, S, P]
+        lib.attn_fwd_decode_ragged.restype = I
         lib.attn_merge.argtypes = [P, P, I, P, P, I, I, I, I, P]
         lib.attn_merge.restype = I
         lib.attn_status_string.argtypes = [I]
@@ -169,6 +173,59 @@ def attn_fwd_from_host(q, k, v, o, lse, dq, dk, dv, do_, dlse, causal=False, sca
                                    int(bool(causal)), float(scale), _stream_ptr(stream))
     _check(st, "attn_fwd_from_host")
     return o, lse
+
+
+def _seqlens_ptr(t, B, name):
+    if t is None:
+        return ctypes.c_void_p(0)
+    if not t.is_cuda or t.dtype != torch.int32 or t.shape != (B,) or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous int32 CUDA tensor of shape [B]")
+    return _ptr(t)
+
+
+def attn_fwd_ragged(q, k, v, seqlens_q=None, seqlens_k=None, causal=False, scale=None,
+                    out=None, lse=None, stream=None):
+    """``attn_fwd_ragged``: sequence b uses its first seqlens_q[b] queries and
+    seqlens_k[b] keys of the padded tensors (int32 CUDA tensors [B] or None).
+    Rows past seqlens_q[b] of the outputs are not written."""
+    B, H, Nq, Nk, d = _check_inputs(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    st = load().attn_fwd_ragged(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                _seqlens_ptr(seqlens_q, B, "seqlens_q"),
+                                _seqlens_ptr(seqlens_k, B, "seqlens_k"), B, H, Nq, Nk, d,
+                                int(bool(causal)), float(scale), _stream_ptr(stream))
+    _check(st, "attn_fwd_ragged")
+    return out, lse
+
+
+def attn_fwd_decode_ragged(q, k, v, seqlens_k=None, scale=None, out=None, lse=None,
+                           workspace=None, stream=None):
+    """``attn_fwd_decode_ragged``: one query per (b, h) over the first
+    seqlens_k[b] keys of the padded k and v."""
+    B, H, Nq, Nk, d = _check_inputs(q, k, v)
+    if Nq != 1:
+        raise ValueError("attn_fwd_decode_ragged takes a single query row (Nq = 1)")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, 1, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, 1), dtype=torch.float32, device=q.device)
+    need = decode_workspace_bytes(B, H, Nk, d)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = _ptr(workspace) if workspace is not None else ctypes.c_void_p(0)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().attn_fwd_decode_ragged(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                       _seqlens_ptr(seqlens_k, B, "seqlens_k"), B, H, Nk, d,
+                                       float(scale), ws_ptr, ws_bytes, _stream_ptr(stream))
+    _check(st, "attn_fwd_decode_ragged")
+    return out, lse
 
 
 def attn_merge(o_parts, lse_parts, out=None, lse=None, stream=None):

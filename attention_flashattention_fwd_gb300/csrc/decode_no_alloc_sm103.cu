@@ -86,5 +86,7 @@ extern "C" int attn_fwd_decode_no_alloc(const void* q, const void* k, const void
     p.splits = splits;
     p.keys_per_split = kps;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    p.H = H;
+    p.seqlens_k = nullptr;  // every sequence has all Nk keys
     return gbattn::launch_decode(d, p, static_cast<cudaStream_t>(stream));
 }

@@ -24,6 +24,8 @@
 
 namespace gbattn {
 
+__device__ unsigned int g_decode_error = 0;
+
 namespace {
 
 constexpr int kDecThreads = 256;   // 8 warps
@@ -86,8 +88,18 @@ __global__ void __launch_bounds__(kDecThreads)
     const int g = warp * kGroupsPerWarp + lane / kLanesPerRow;
     const int sub = lane % kLanesPerRow;  // which 8-element slice of the row
 
+    // keys of this (b, h): all Nk, or the sequence's own count (a count out
+    // of range is reported and gives the sequence no keys: o = 0, lse = -inf)
+    int nk = p.Nk;
+    if (p.seqlens_k) {
+        nk = p.seqlens_k[bh / p.H];
+        if (nk < 1 || nk > p.Nk) {
+            if (threadIdx.x == 0) atomicOr(&g_decode_error, kErrBitLengths);
+            nk = 0;
+        }
+    }
     const int ks = split * p.keys_per_split;
-    const int ke = min(p.Nk, ks + p.keys_per_split);
+    const int ke = min(nk, ks + p.keys_per_split);
 
     float q[8];
     {
@@ -172,7 +184,7 @@ __global__ void __launch_bounds__(kDecThreads)
         const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
         if (p.splits == 1) {
             p.o[static_cast<size_t>(bh) * D + c] = __float2bfloat16_rn(O * inv);
-            if (c == 0) p.lse[bh] = (M + log2f(Lsum)) * kLn2;
+            if (c == 0) p.lse[bh] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
         } else {
             const size_t ps = static_cast<size_t>(bh) * p.splits + split;
             p.part_o[ps * D + c] = O * inv;
@@ -201,7 +213,7 @@ __global__ void __launch_bounds__(D) attn_fwd_decode_combine_kernel(DecodeParams
         }
     }
     p.o[static_cast<size_t>(bh) * D + c] = __float2bfloat16_rn(Lsum > 0.f ? O / Lsum : 0.f);
-    if (c == 0) p.lse[bh] = (M + log2f(Lsum)) * kLn2;
+    if (c == 0) p.lse[bh] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
 }
 
 // ------------------------------------------------------------------ host side
@@ -243,6 +255,13 @@ int launch_decode(int d, const DecodeParams& p, cudaStream_t stream) {
             attn_fwd_decode_combine_kernel<64><<<p.BH, 64, 0, stream>>>(p);
     }
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+unsigned read_and_clear_decode_error() {
+    unsigned v = 0, zero = 0;
+    cudaMemcpyFromSymbol(&v, g_decode_error, sizeof v);
+    cudaMemcpyToSymbol(g_decode_error, &zero, sizeof zero);
+    return v;
 }
 
 }  // namespace gbattn

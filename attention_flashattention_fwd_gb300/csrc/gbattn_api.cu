@@ -116,7 +116,8 @@ int encode_dq_acc(CUtensorMap* m, void* base, long long BH, int nq_pad, int d) {
 }
 
 int enqueue_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                int Nq, int Nk, int d, int causal, float scale, cudaStream_t stream) {
+                int Nq, int Nk, int d, int causal, float scale, cudaStream_t stream,
+                const int* seqlens_q = nullptr, const int* seqlens_k = nullptr) {
     int st = ensure_init();
     if (st != ATTN_OK) return st;
     int num_sms = 0;
@@ -134,8 +135,10 @@ int enqueue_fwd(const void* q, const void* k, const void* v, void* o, float* lse
     p.BH = static_cast<int>(BH);
     p.num_pairs = (Nq + 255) / 256;
     p.causal = causal;
-    p.causal_off = causal ? Nk - Nq : 0;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    p.H = H;
+    p.seqlens_q = seqlens_q;
+    p.seqlens_k = seqlens_k;
     return launch_prefill(d, tq, tk, tv, p, num_sms, stream);
 }
 
@@ -204,9 +207,13 @@ size_t attn_fwd_decode_workspace_bytes(int B, int H, int Nk, int d) {
     return decode_workspace_bytes(static_cast<long long>(B) * H, Nk, d);
 }
 
-int attn_fwd_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                    int H, int Nk, int d, float scale, void* workspace, size_t workspace_bytes,
-                    void* stream) {
+}  // extern "C"
+
+namespace {
+
+int decode_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int Nk, int d, float scale, void* workspace, size_t workspace_bytes,
+                const int* seqlens_k, void* stream) {
     if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
     if (B <= 0 || H <= 0 || Nk <= 0) return ATTN_ERR_INVALID_ARG;
     if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
@@ -233,7 +240,40 @@ int attn_fwd_decode(const void* q, const void* k, const void* v, void* o, float*
     p.splits = splits;
     p.keys_per_split = kps;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    p.H = H;
+    p.seqlens_k = seqlens_k;
     return launch_decode(d, p, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                    int H, int Nk, int d, float scale, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+    return decode_impl(q, k, v, o, lse, B, H, Nk, d, scale, workspace, workspace_bytes, nullptr,
+                       stream);
+}
+
+int attn_fwd_decode_ragged(const void* q, const void* k, const void* v, void* o, float* lse,
+                           const int* seqlens_k, int B, int H, int Nk, int d, float scale,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+    if (seqlens_k && (reinterpret_cast<uintptr_t>(seqlens_k) & 3u)) return ATTN_ERR_MISALIGNED;
+    return decode_impl(q, k, v, o, lse, B, H, Nk, d, scale, workspace, workspace_bytes,
+                       seqlens_k, stream);
+}
+
+int attn_fwd_ragged(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int* seqlens_q, const int* seqlens_k, int B, int H, int Nq, int Nk,
+                    int d, int causal, float scale, void* stream) {
+    int st = validate_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale);
+    if (st != ATTN_OK) return st;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+        (reinterpret_cast<uintptr_t>(seqlens_q) & 3u) || (reinterpret_cast<uintptr_t>(seqlens_k) & 3u))
+        return ATTN_ERR_MISALIGNED;
+    return enqueue_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale,
+                       static_cast<cudaStream_t>(stream), seqlens_q, seqlens_k);
 }
 
 int attn_fwd_from_host(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -317,9 +357,11 @@ const char* attn_status_string(int status) {
 
 int attn_device_error(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
-    const unsigned e = read_and_clear_prefill_error() | read_and_clear_bwd_error();
+    const unsigned e = read_and_clear_prefill_error() | read_and_clear_bwd_error() |
+                       read_and_clear_decode_error();
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-    return e ? ATTN_ERR_TIMEOUT : ATTN_OK;
+    if (e & kErrBitTimeout) return ATTN_ERR_TIMEOUT;
+    return e ? ATTN_ERR_INVALID_ARG : ATTN_OK;
 }
 
 int attn_version(void) { return kVersion; }

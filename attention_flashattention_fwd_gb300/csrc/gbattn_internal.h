@@ -18,9 +18,11 @@ struct PrefillParams {
     float* lse;         // [BH, Nq]
     int Nq, Nk, BH;
     int num_pairs;      // query-tile pairs per head: ceil(Nq / 256)
-    int causal;
-    int causal_off;     // Nk - Nq when causal: query i sees keys j <= i + causal_off
+    int causal;         // query i sees keys j <= i + (nk - nq) of its sequence
     float scale_log2;   // scale * log2(e)
+    int H;
+    const int* seqlens_q;  // [B] per-sequence query counts, or null (all Nq)
+    const int* seqlens_k;  // [B] per-sequence key counts, or null (all Nk)
 };
 
 // Arguments of the split-K decode kernels.
@@ -34,6 +36,8 @@ struct DecodeParams {
     float* part_lse;         // [BH, splits]      (workspace), log2 units
     int BH, Nk, splits, keys_per_split;
     float scale_log2;
+    int H;
+    const int* seqlens_k;    // [B] per-sequence key counts, or null (all Nk)
 };
 
 // Arguments of the backward preprocessing kernel.
@@ -78,11 +82,15 @@ int launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CU
                    const PrefillParams& p, int num_sms, cudaStream_t stream);
 int prefill_smem_bytes(int d);
 unsigned read_and_clear_prefill_error();
+// Device error bits (shared by the kernels' error words)
+constexpr unsigned kErrBitTimeout = 1u;  // a bounded barrier wait ran out
+constexpr unsigned kErrBitLengths = 4u;  // a per-sequence length was out of range
 
 // decode_sm103.cu
 void decode_split_plan(long long BH, int Nk, int* splits, int* keys_per_split);
 size_t decode_workspace_bytes(long long BH, int Nk, int d);
 int launch_decode(int d, const DecodeParams& p, cudaStream_t stream);
+unsigned read_and_clear_decode_error();
 
 // merge_sm103.cu
 int launch_merge(int d, const MergeParams& p, int num_sms, cudaStream_t stream);

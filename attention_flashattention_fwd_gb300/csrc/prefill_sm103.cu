@@ -93,13 +93,18 @@ struct Bars {
     __device__ uint32_t o_free(int t) const { return tile0 + 8u * (6 * t + 5); }
 };
 
-// Geometry of work item `idx` (0 <= idx < num_pairs * BH).
+// Geometry of work item `idx` (0 <= idx < num_pairs * BH).  With per-sequence
+// lengths, nq / nk are sequence b's; an item whose rows all lie past nq is
+// empty and every role skips it.
 struct Item {
     int bh, row0, n_kv0, n_kv1;
+    int nq, nk, off;  // query and key count of the sequence; causal offset nk - nq
+    bool empty;
     __device__ int n_kv(int t) const { return t ? n_kv1 : n_kv0; }
     __device__ int n_kv_max() const { return max(n_kv0, n_kv1); }
 };
 
+template <bool kRagged>
 __device__ __forceinline__ Item item_at(const PrefillParams& p, int idx) {
     Item it;
     int pair;
@@ -111,11 +116,25 @@ __device__ __forceinline__ Item item_at(const PrefillParams& p, int idx) {
         it.bh = idx / p.num_pairs;
     }
     it.row0 = pair * 2 * kBM;
-    const int n_kv_all = (p.Nk + kBN - 1) / kBN;
+    it.nq = p.Nq;
+    it.nk = p.Nk;
+    if constexpr (kRagged) {
+        const int b = it.bh / p.H;
+        if (p.seqlens_q) it.nq = p.seqlens_q[b];
+        if (p.seqlens_k) it.nk = p.seqlens_k[b];
+        if (it.nq < 1 || it.nq > p.Nq || it.nk < 1 || it.nk > p.Nk || (p.causal && it.nq > it.nk)) {
+            atomicOr(&g_prefill_error, kErrBitLengths);  // the sequence is skipped
+            it.nq = 0;  // skip the sequence
+            it.nk = 1;
+        }
+    }
+    it.empty = it.row0 >= it.nq;
+    it.off = p.causal ? it.nk - it.nq : 0;
+    const int n_kv_all = (it.nk + kBN - 1) / kBN;
     // key tiles each query tile visits (causal: up to the tile holding the last
-    // key its last row sees, key row0 + 127 + causal_off for tile 0); tile 1
-    // visits every tile tile 0 does, and at most one more
-    const int last0 = it.row0 + kBM - 1 + p.causal_off;
+    // key its last row sees, key row0 + 127 + off for tile 0); tile 1 visits
+    // every tile tile 0 does, and at most one more
+    const int last0 = it.row0 + kBM - 1 + it.off;
     it.n_kv0 = p.causal ? min(n_kv_all, last0 / kBN + 1) : n_kv_all;
     it.n_kv1 = p.causal ? min(n_kv_all, (last0 + kBM) / kBN + 1) : n_kv_all;
     return it;
@@ -153,7 +172,9 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
 
 }  // namespace
 
-template <int D>
+// kRagged: per-sequence lengths (seqlens_q / seqlens_k) are read; the
+// instantiation without them is the plain [B, H, Nq, Nk] problem.
+template <int D, bool kRagged>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                             const __grid_constant__ CUtensorMap tm_k,
@@ -213,9 +234,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_v);
             int issued = 0;  // ring uses (K or V tiles) issued so far
             bool ok = true;
-            auto load_q = [&](int k, int t, const Item& it) {
+            auto load_q = [&](int kp, int t, const Item& it) {
                 // the previous item's last Q_t K^T product has finished
-                if (k > 0 && !(ok = wait_or_abort(bars.q_empty(t), (k - 1) & 1, abort_flag)))
+                if (kp > 0 && !(ok = wait_or_abort(bars.q_empty(t), (kp - 1) & 1, abort_flag)))
                     return;
                 mbar_arrive_expect_tx(bars.q_full(t), C::kTileBytes);
                 for (int s = 0; s < C::kSub; ++s)
@@ -235,19 +256,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 bars.full(slot), s * 64, j * kBN, it.bh);
                 ++issued;
             };
+            int kp = 0;  // items processed (empty items are skipped by every role)
             for (int k = 0; ok; ++k) {
                 const int idx = item_index(k, n_items);
                 if (idx < 0) break;
-                const Item it = item_at(p, idx);
+                const Item it = item_at<kRagged>(p, idx);
+                if (it.empty) continue;
                 // in the order the MMA warp needs them: Q_0, K_0, Q_1, V_0, K_1, V_1, ...
-                load_q(k, 0, it);
+                load_q(kp, 0, it);
                 if (ok) load_kv(0, 0, it);
-                if (ok) load_q(k, 1, it);
+                if (ok) load_q(kp, 1, it);
                 if (ok) load_kv(1, 0, it);
                 // warm L2 with the next item's query tiles (read once, from DRAM)
                 const int nidx = item_index(k + 1, n_items);
                 if (ok && nidx >= 0) {
-                    const Item nx = item_at(p, nidx);
+                    const Item nx = item_at<kRagged>(p, nidx);
                     for (int t = 0; t < 2; ++t)
                         for (int s = 0; s < C::kSub; ++s)
                             tma_prefetch_l2_3d(&tm_q, s * 64, nx.row0 + t * kBM, nx.bh);
@@ -256,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     load_kv(0, j, it);
                     if (ok) load_kv(1, j, it);
                 }
+                ++kp;
             }
             if (!ok) {
                 // drain: every slot's most recent copy must land before exit
@@ -315,14 +339,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             bool ok = true;
+            int kp = 0;  // items processed
             for (int k = 0; ok; ++k) {
                 const int idx = item_index(k, n_items);
                 if (idx < 0) break;
-                const Item it = item_at(p, idx);
+                const Item it = item_at<kRagged>(p, idx);
+                if (it.empty) continue;
                 const int nmax = it.n_kv_max();
                 // prologue of the item: S_0(0) once Q_0 and K_0 are in, then S_1(0)
                 for (int t = 0; t < 2 && ok; ++t) {
-                    ok = wait_or_abort(bars.q_full(t), k & 1, abort_flag) && (t == 1 || wait_use(u));
+                    ok = wait_or_abort(bars.q_full(t), kp & 1, abort_flag) && (t == 1 || wait_use(u));
                     if (!ok) break;
                     tc_fence_after();
                     issue_s(t, u);  // n_kv0, n_kv1 >= 1
@@ -338,8 +364,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!(ok = wait_or_abort(bars.p_ready(t), iter[t] & 1, abort_flag)))
                             break;
                         // O_t of the previous item has been read by its epilogue
-                        if (j == 0 && k > 0 &&
-                            !(ok = wait_or_abort(bars.o_free(t), (k - 1) & 1, abort_flag)))
+                        if (j == 0 && kp > 0 &&
+                            !(ok = wait_or_abort(bars.o_free(t), (kp - 1) & 1, abort_flag)))
                             break;
                         tc_fence_after();
                         issue_pv(t, uv, j == 0);
@@ -358,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     u += 2;
                 }
+                ++kp;
             }
             // every MMA this thread issued has completed once `fin` flips
             umma_commit(bars.fin);
@@ -376,11 +403,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem + lane_off + C::col_o(t);
         const float cl2 = p.scale_log2;
         int iter = 0;  // key tiles processed by this tile over all items
+        int kp = 0;    // items processed
         bool ok = true;
         for (int k = 0; ok; ++k) {
             const int idx = item_index(k, n_items);
             if (idx < 0) break;
-            const Item it = item_at(p, idx);
+            const Item it = item_at<kRagged>(p, idx);
+            if (it.empty) continue;
             const int row = it.row0 + t * kBM + r;
             const int nkv = it.n_kv(t);
             float m_ref = -INFINITY;  // running reference max, log2 units
@@ -407,12 +436,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_ld();
                 float* s = reinterpret_cast<float*>(sr);
                 const int key0 = j * kBN;
-                const bool ragged = key0 + kBN > p.Nk;
-                const bool diag =
-                    p.causal && (key0 + kBN - 1 > it.row0 + t * kBM + p.causal_off);
+                const bool ragged = key0 + kBN > it.nk;
+                const bool diag = p.causal && (key0 + kBN - 1 > it.row0 + t * kBM + it.off);
                 if (ragged || diag) {
                     // last visible key of this row
-                    const int lim = p.causal ? min(p.Nk - 1, row + p.causal_off) : p.Nk - 1;
+                    const int lim = p.causal ? min(it.nk - 1, row + it.off) : it.nk - 1;
 #pragma unroll
                     for (int c = 0; c < kBN; ++c)
                         if (key0 + c > lim) s[c] = -INFINITY;
@@ -491,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             // ---- epilogue of the item: O / l and the logsumexp
-            ok = wait_or_abort(bars.pv_done(t), k & 1, abort_flag);  // one phase per item
+            ok = wait_or_abort(bars.pv_done(t), kp & 1, abort_flag);  // one phase per item
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
@@ -505,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t o[32];
                 tmem_ld32(tO + ch * 32, o);
                 tmem_wait_ld();
-                if (row < p.Nq) {
+                if (row < it.nq) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int c = 0; c < 16; ++c)
@@ -522,9 +550,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bars.o_free(t));
-            if (row < p.Nq)
+            if (row < it.nq)
                 p.lse[static_cast<size_t>(it.bh) * p.Nq + row] =
                     (m_ref + log2f(l)) * 0.69314718055994530942f;
+            ++kp;
         }
     }
 
@@ -538,12 +567,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------ host side
 
 int prefill_set_attributes() {
-    if (cudaFuncSetAttribute(attn_fwd_prefill_kernel<128>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<128>::kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(attn_fwd_prefill_kernel<64>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<64>::kSmemBytes) != cudaSuccess)
+    const auto a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    if (cudaFuncSetAttribute(attn_fwd_prefill_kernel<128, false>, a, Cfg<128>::kSmemBytes) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(attn_fwd_prefill_kernel<64, false>, a, Cfg<64>::kSmemBytes) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(attn_fwd_prefill_kernel<128, true>, a, Cfg<128>::kSmemBytes) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(attn_fwd_prefill_kernel<64, true>, a, Cfg<64>::kSmemBytes) !=
+            cudaSuccess)
         return ATTN_ERR_CUDA;
     return ATTN_OK;
 }
@@ -554,8 +586,12 @@ static int launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk, const 
     using C = Cfg<D>;
     const long long items = static_cast<long long>(p.num_pairs) * p.BH;
     const long long grid = items < num_sms ? items : num_sms;  // one persistent CTA per SM
-    attn_fwd_prefill_kernel<D><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
-        tq, tk, tv, p);
+    if (p.seqlens_q || p.seqlens_k)
+        attn_fwd_prefill_kernel<D, true>
+            <<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
+    else
+        attn_fwd_prefill_kernel<D, false>
+            <<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -160,6 +160,48 @@ int attn_fwd_decode_no_alloc(const void *q, const void *k, const void *v, void *
                              int B, int H, int Nk, int d, float scale, void *stream);
 
 /*
+ * attn_fwd_ragged -- attn_fwd on a batch of sequences of different lengths.
+ *
+ * The KV cache grows per request during inference (PDC course Lecture 4,
+ * section 4.9), so a serving batch holds sequences of different lengths.
+ * The tensors keep the padded layout of attn_fwd ([B,H,Nq,d], [B,H,Nk,d]);
+ * sequence b has seqlens_q[b] queries and seqlens_k[b] keys, the first
+ * ones of its rows.  For every b, h and i < seqlens_q[b]:
+ *   s_ij = scale q_i . k_j  for j < seqlens_k[b]  (later keys do not exist)
+ *   s_ij = -inf if causal and j > i + (seqlens_k[b] - seqlens_q[b])
+ *   o, lse as attn_fwd over those keys.
+ *
+ *   seqlens_q, seqlens_k  device int32 [B], 4-byte aligned, or NULL (every
+ *               sequence has Nq queries / Nk keys).  1 <= seqlens_q[b] <= Nq,
+ *               1 <= seqlens_k[b] <= Nk, and seqlens_q[b] <= seqlens_k[b] when
+ *               causal.  The values are read on the GPU: a sequence whose
+ *               lengths break these bounds is skipped (nothing of it is
+ *               written) and attn_device_error reports ATTN_ERR_INVALID_ARG.
+ *   o, lse      rows i >= seqlens_q[b] are not written.
+ *   k, v        rows j >= seqlens_k[b] get weight 0 but are read in whole
+ *               128-key tiles: they must hold finite values (0 * inf is NaN).
+ *   Everything else as attn_fwd.
+ */
+int attn_fwd_ragged(const void *q, const void *k, const void *v, void *o, float *lse,
+                    const int *seqlens_q, const int *seqlens_k, int B, int H, int Nq, int Nk,
+                    int d, int causal, float scale, void *stream);
+
+/*
+ * attn_fwd_decode_ragged -- attn_fwd_decode on a batch whose sequences hold
+ * different numbers of keys: sequence b attends to keys j < seqlens_k[b] of
+ * the padded [B,H,Nk,d] k and v; later rows are never read.
+ *   seqlens_k   device int32 [B], 4-byte aligned, or NULL (all Nk);
+ *               1 <= seqlens_k[b] <= Nk, checked on the GPU: a sequence out
+ *               of range gets o = 0 and lse = -inf and attn_device_error
+ *               reports ATTN_ERR_INVALID_ARG.
+ *   Workspace: attn_fwd_decode_workspace_bytes(B, H, Nk, d).  Everything
+ *   else as attn_fwd_decode.
+ */
+int attn_fwd_decode_ragged(const void *q, const void *k, const void *v, void *o, float *lse,
+                           const int *seqlens_k, int B, int H, int Nk, int d, float scale,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * attn_merge -- attention over all keys from results over disjoint key sets.
  *
  * For every row (b, h, i), part s holds o_s = attention of query i over the
@@ -239,7 +281,9 @@ const char *attn_status_string(int status);
  * clears the library's device-side error word.  Returns ATTN_OK when no
  * kernel reported a problem since the last call, ATTN_ERR_TIMEOUT when a
  * kernel abandoned a bounded wait on one of its own barriers (it then wrote
- * no valid output), or ATTN_ERR_CUDA if the synchronisation failed.
+ * no valid output), ATTN_ERR_INVALID_ARG when a kernel found a per-sequence
+ * length out of range (attn_fwd_ragged, attn_fwd_decode_ragged), or
+ * ATTN_ERR_CUDA if the synchronisation failed.
  */
 int attn_device_error(void);
 

@@ -156,3 +156,24 @@ def test_merge_rejects_before_launch(lib):
     assert merge(lse=0) == INVALID and merge(n=0) == INVALID and merge(Nq=0) == INVALID
     assert merge(d=96) == UNSUPPORTED
     assert merge(op=FAKE + 8) == MISALIGNED and merge(lse=FAKE + 4) == MISALIGNED
+
+
+def test_ragged_entry_points_reject_before_launch(lib):
+    P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.attn_fwd_ragged.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, P]
+    lib.attn_fwd_ragged.restype = I
+    lib.attn_fwd_decode_ragged.argtypes = [P, P, P, P, P, P, I, I, I, I, F, P, S, P]
+    lib.attn_fwd_decode_ragged.restype = I
+
+    def rag(sq=FAKE, sk=FAKE, q=FAKE, d=64, causal=0, Nq=128, Nk=128):
+        return lib.attn_fwd_ragged(P(q), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(sq), P(sk), 2, 1,
+                                   Nq, Nk, d, causal, 0.125, P(0))
+
+    assert rag(sq=FAKE + 2) == MISALIGNED and rag(sk=FAKE + 1) == MISALIGNED
+    assert rag(q=0) == INVALID and rag(d=80) == UNSUPPORTED
+    assert rag(causal=1, Nq=256, Nk=128) == UNSUPPORTED
+    need = lib.attn_fwd_decode_workspace_bytes(1, 1, 8192, 128)
+    assert lib.attn_fwd_decode_ragged(P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE + 2), 1, 1,
+                                      8192, 128, 0.1, P(FAKE), need, P(0)) == MISALIGNED
+    assert lib.attn_fwd_decode_ragged(P(0), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1, 1,
+                                      8192, 128, 0.1, P(FAKE), need, P(0)) == INVALID
