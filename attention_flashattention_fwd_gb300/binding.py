@@ -58,6 +58,8 @@ def load():
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_device_error.argtypes = []
         lib.attn_device_error.restype = I
+        lib.attn_selftest_timeout.argtypes = [P]
+        lib.attn_selftest_timeout.restype = I
         lib.attn_version.argtypes = []
         lib.attn_version.restype = I
         _lib = lib

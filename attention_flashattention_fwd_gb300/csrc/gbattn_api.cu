@@ -358,12 +358,16 @@ const char* attn_status_string(int status) {
 int attn_device_error(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
     const unsigned e = read_and_clear_prefill_error() | read_and_clear_bwd_error() |
-                       read_and_clear_decode_error();
+                       read_and_clear_decode_error() | read_and_clear_selftest_error();
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     if (e & kErrBitTimeout) return ATTN_ERR_TIMEOUT;
     return e ? ATTN_ERR_INVALID_ARG : ATTN_OK;
 }
 
 int attn_version(void) { return kVersion; }
+
+int attn_selftest_timeout(void* stream) {
+    return launch_selftest_timeout(static_cast<cudaStream_t>(stream));
+}
 
 }  // extern "C"

@@ -92,6 +92,10 @@ size_t decode_workspace_bytes(long long BH, int Nk, int d);
 int launch_decode(int d, const DecodeParams& p, cudaStream_t stream);
 unsigned read_and_clear_decode_error();
 
+// selftest_sm103.cu
+int launch_selftest_timeout(cudaStream_t stream);
+unsigned read_and_clear_selftest_error();
+
 // merge_sm103.cu
 int launch_merge(int d, const MergeParams& p, int num_sms, cudaStream_t stream);
 

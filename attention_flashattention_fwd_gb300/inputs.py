@@ -58,6 +58,12 @@ WORKLOADS = {
                                         seed=1004),
 }
 
+# The non-causal counterpart of the 4096-token workload (the study's throughput
+# target covers causal and non-causal prefill at d = 128, N >= 4096).
+EXTRA_WORKLOADS = {
+    "b2h16n4096d128": Workload("b2h16n4096d128", 2, 16, 4096, 4096, 128, False, seed=1005),
+}
+
 
 def make_qkv(B, H, Nq, Nk, d, seed, device="cpu", sigma_qk=1.0, sigma_v=1.0):
     """Q [B,H,Nq,d], K and V [B,H,Nk,d], bf16, contiguous, on ``device``."""

@@ -524,6 +524,29 @@ def run_gpu(args):
                      "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)"},
     }
 
+    # ---- non-causal prefill at d = 128, N = 4096 (not part of the timed step)
+    from attention_flashattention_fwd_gb300.inputs import EXTRA_WORKLOADS
+    wn = EXTRA_WORKLOADS["b2h16n4096d128"]
+    qn, kn, vn = make_workload(wn, device=dev)
+    on, ln = torch.empty_like(qn), torch.empty(qn.shape[:3], dtype=torch.float32, device=dev)
+    for _ in range(3):
+        binding.attn_fwd(qn, kn, vn, causal=False, scale=wn.scale, out=on, lse=ln, stream=stream)
+    torch.cuda.synchronize()
+    n_ms = 0.0
+    for _ in range(bwd_reps):
+        flush.zero_()
+        torch.cuda._sleep(LAUNCH_COVER_CYCLES)
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        binding.attn_fwd(qn, kn, vn, causal=False, scale=wn.scale, out=on, lse=ln, stream=stream)
+        b1.record(stream)
+        torch.cuda.synchronize()
+        n_ms += b0.elapsed_time(b1)
+    (n_ms,) = max_over_ranks([n_ms], world, device=dev)
+    noncausal = prefill_part(wn, n_ms * K / bwd_reps, PREFILL_SOURCES, "ncu_prefill_" + wn.name)
+    noncausal["calls"] = bwd_reps
+    del qn, kn, vn, on, ln
+
     # ---- the exchange step of key-sharded attention (not part of the timed step):
     # attn_merge of MERGE_PARTS shard results of the headline shape
     o_parts = torch.stack([o3] * MERGE_PARTS).contiguous()
@@ -566,6 +589,7 @@ def run_gpu(args):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": p3["roofline"],
         "parts": {HEADLINE: p3, LONG: p4, DECODE: p5},
+        "noncausal": noncausal,
         "backward": backward,
         "merge": merge,
         "e2e": e2e,

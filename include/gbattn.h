@@ -290,6 +290,17 @@ int attn_device_error(void);
 /* attn_version -- library version as major*10000 + minor*100 + patch. */
 int attn_version(void);
 
+/*
+ * attn_selftest_timeout -- a check of the failure path; the lecture pages
+ * have no counterpart.  Enqueues a one-thread kernel that waits on a
+ * barrier nothing ever arrives on, with the same bounded wait the attention
+ * kernels use.  The wait gives up after the library's limit (2 s), the
+ * kernel sets the timeout bit of the device error word and returns, and the
+ * next attn_device_error returns ATTN_ERR_TIMEOUT (and clears it).  Nothing
+ * faults; the context stays usable.  Returns ATTN_OK or ATTN_ERR_CUDA.
+ */
+int attn_selftest_timeout(void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -166,6 +166,12 @@ def test_b2h16n4096d128_causal_sampled():
                 extra_rows=[0, 127, 128, 255, 256, 4095])
 
 
+def test_b2h16n4096d128_noncausal_sampled():
+    from attention_flashattention_fwd_gb300.inputs import EXTRA_WORKLOADS
+    w = EXTRA_WORKLOADS["b2h16n4096d128"]
+    _rows_check(w, full_heads=[5], n_random=256, extra_rows=[0, 127, 128, 4095])
+
+
 def test_b1h32n16384d128_causal_sampled():
     w = WORKLOADS["b1h32n16384d128_causal"]
     _rows_check(w, full_heads=[], n_random=384,
