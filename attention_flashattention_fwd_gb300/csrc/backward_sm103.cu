@@ -552,37 +552,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t pk[64];  // P^T row as bf16 pairs, 128 queries
             // ---- phase A: p = 2^{s c - L log2 e}, pairs of columns per instruction
             const float2 c2 = make_float2(cl2, cl2);
+            {
+                // the whole S^T row (128 queries): four loads in flight, one wait
+                uint32_t sr[4][32];
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {  // 64 queries at a time
-                uint32_t s0[32], s1[32];
-                tmem_ld32(tS + hf * 64, s0);
-                tmem_ld32(tS + hf * 64 + 32, s1);
-                tmem_wait_ld_into(s0, s1);
+                for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(tS + q4 * 32, sr[q4]);
+                tmem_wait_ld_into(sr[0], sr[1]);
+                after_wait_ld(sr[2], sr[3]);
 #pragma unroll
-                for (int c4 = 0; c4 < 16; ++c4) {
-                    const float4 l4 = L4[hf * 16 + c4];  // same address in every lane
-                    const int c = c4 * 4;                 // column within the 64
-                    auto sv = [&](int e) { return __uint_as_float(c < 32 ? s0[c + e] : s1[c - 32 + e]); };
-                    const float2 x0 = ffma2(make_float2(sv(0), sv(1)), c2, make_float2(l4.x, l4.y));
-                    const float2 x1 = ffma2(make_float2(sv(2), sv(3)), c2, make_float2(l4.z, l4.w));
+                for (int c4 = 0; c4 < 32; ++c4) {  // four queries per shared-memory read
+                    const float4 l4 = L4[c4];  // same address in every lane
+                    const uint32_t* sv = sr[c4 >> 3] + (c4 & 7) * 4;
+                    const float2 x0 = ffma2(make_float2(__uint_as_float(sv[0]), __uint_as_float(sv[1])),
+                                            c2, make_float2(l4.x, l4.y));
+                    const float2 x1 = ffma2(make_float2(__uint_as_float(sv[2]), __uint_as_float(sv[3])),
+                                            c2, make_float2(l4.z, l4.w));
                     float pv[4] = {ex2_approx(x0.x), ex2_approx(x0.y), ex2_approx(x1.x),
                                    ex2_approx(x1.y)};
                     if (diag) {  // tiles that straddle the causal boundary
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            if (i0 + hf * 64 + c + e < first_vis) pv[e] = 0.f;
+                            if (i0 + c4 * 4 + e < first_vis) pv[e] = 0.f;
                     }
-                    pk[hf * 32 + 2 * c4] = pack_bf16x2(pv[0], pv[1]);
-                    pk[hf * 32 + 2 * c4 + 1] = pack_bf16x2(pv[2], pv[3]);
+                    pk[2 * c4] = pack_bf16x2(pv[0], pv[1]);
+                    pk[2 * c4 + 1] = pack_bf16x2(pv[2], pv[3]);
                 }
-                if (!key_ok) {  // rows past the last key
-#pragma unroll
-                    for (int x = 0; x < 32; ++x) pk[hf * 32 + x] = 0u;
-                }
-                // packed columns hf*32.. lie below the fp32 columns still to be read
-                tmem_st16(tS + hf * 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[hf * 32]));
-                tmem_st16(tS + hf * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[hf * 32 + 16]));
             }
+            if (!key_ok) {  // rows past the last key
+#pragma unroll
+                for (int x = 0; x < 64; ++x) pk[x] = 0u;
+            }
+            // P^T over the first 64 columns of S^T (all of S^T has been read)
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+                tmem_st16(tS + x * 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[x * 16]));
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
