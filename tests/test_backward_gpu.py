@@ -150,3 +150,11 @@ def test_backward_rejects_small_workspace():
                      device="cuda")
     with pytest.raises(binding.GbattnError):
         binding.attn_bwd(q, k, v, o, lse, o, workspace=ws)
+
+
+def test_backward_d64_2048_tokens_full():
+    (q, k, v, dout), (dq, dk, dv) = _run(1, 2, 2048, 2048, 64, True, seed=151)
+    rq, rk, rv = oracle.attention_bwd(bf16_bits(q), bf16_bits(k), bf16_bits(v), bf16_bits(dout),
+                                      causal=True)
+    for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        _assert_grad_close(got.float().cpu().numpy(), ref, f"d64 2048 {name}")

@@ -342,3 +342,40 @@ def test_repeated_launches_are_bitwise_stable(name):
         binding.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)
         torch.cuda.synchronize()
         assert torch.equal(o, o0) and torch.equal(lse, l0)
+
+
+# ------------------------------------------------------------ large and wide shapes
+
+def _sampled_custom(B, H, Nq, Nk, d, causal, seed, extra_rows, n_random=96, scale=None):
+    from attention_flashattention_fwd_gb300.inputs import Workload
+    w = Workload(f"b{B}h{H}q{Nq}k{Nk}d{d}", B, H, Nq, Nk, d, causal, seed=seed)
+    return _rows_check(w, full_heads=[], n_random=n_random, extra_rows=extra_rows)
+
+
+def test_65536_token_causal_head_sampled():
+    # positions near 2^16: query and key offsets, TMA coordinates and row offsets
+    _sampled_custom(1, 1, 65536, 65536, 128, True, seed=3001,
+                    extra_rows=[0, 1, 127, 128, 32767, 32768, 65407, 65408, 65535])
+
+
+def test_32768_tokens_d64_noncausal_sampled():
+    _sampled_custom(1, 2, 32768, 32768, 64, False, seed=3002, extra_rows=[0, 16383, 32767])
+
+
+def test_many_small_heads_sampled():
+    # 1024 (b, h) pairs of 256 tokens: many work items per CTA
+    _sampled_custom(16, 64, 256, 256, 64, True, seed=3003, extra_rows=[0, 255], n_random=256)
+
+
+def test_decode_8192_heads_sampled():
+    B, H, Nk, d = 256, 32, 1024, 64
+    q, k, v = make_qkv(B, H, 1, Nk, d, seed=3004, device=_dev())
+    o, lse = binding.attn_fwd_decode(q, k, v)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(3005)
+    heads = np.unique(np.concatenate([[0, B * H - 1], rng.integers(0, B * H, 120)]))
+    rows = np.stack([heads, np.zeros_like(heads)], axis=1)
+    ro, rl = oracle.attention_rows(bf16_bits(q), bf16_bits(k), bf16_bits(v), rows)
+    og = o.reshape(B * H, d)[torch.as_tensor(heads, device=o.device)].float().cpu().numpy()
+    lg = lse.reshape(B * H)[torch.as_tensor(heads, device=o.device)].cpu().numpy()
+    _assert_close(og, lg, ro, rl, "decode 8192 heads")
