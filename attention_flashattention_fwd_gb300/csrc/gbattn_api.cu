@@ -188,6 +188,39 @@ int enqueue_bwd(const void* q, const void* k, const void* v, const void* o, cons
                            num_sms, stream);
 }
 
+// Streams and events of the host-buffer path, created on first use per device
+// and kept until the process exits.  The mutex serialises the enqueue of
+// calls from several host threads (the events are shared).
+constexpr int kHostChunks = 4;
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t compute = nullptr, copy_out = nullptr;
+    cudaEvent_t start = nullptr, out_done = nullptr;
+    cudaEvent_t in_done[kHostChunks] = {}, fwd_done[kHostChunks] = {};
+};
+HostPipe g_pipes[kMaxDevices];
+std::mutex g_pipe_mu;
+
+int host_pipe(HostPipe** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+    HostPipe& hp = g_pipes[dev];
+    if (!hp.ready) {
+        const unsigned ev = cudaEventDisableTiming;
+        bool ok = cudaStreamCreateWithFlags(&hp.compute, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaStreamCreateWithFlags(&hp.copy_out, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&hp.start, ev) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&hp.out_done, ev) == cudaSuccess;
+        for (int c = 0; c < kHostChunks && ok; ++c)
+            ok = cudaEventCreateWithFlags(&hp.in_done[c], ev) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&hp.fwd_done[c], ev) == cudaSuccess;
+        if (!ok) return ATTN_ERR_CUDA;
+        hp.ready = true;
+    }
+    *out = &hp;
+    return ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -284,17 +317,57 @@ int attn_fwd_from_host(const void* q, const void* k, const void* v, void* o, flo
     if (!dq || !dk || !dv || !do_ || !dlse) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(do_) || !aligned16(dlse))
         return ATTN_ERR_MISALIGNED;
+    // The (b, h) heads go in up to kHostChunks contiguous chunks.  Chunk c:
+    // host->device copies on the caller's stream, the prefill kernel on the
+    // compute stream once they have landed, device->host copies on the
+    // copy-out stream once it has run -- so the inputs of chunk c + 1 cross
+    // the host link while chunk c computes and chunk c - 1's results come back
+    // the other way.  The caller's stream finally waits for the last copy out.
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t BH = static_cast<size_t>(B) * H;
-    const size_t qbytes = BH * Nq * d * 2, kvbytes = BH * Nk * d * 2, lbytes = BH * Nq * 4;
-    if (cudaMemcpyAsync(dq, q, qbytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(dk, k, kvbytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(dv, v, kvbytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    const long long BH = static_cast<long long>(B) * H;
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    HostPipe* hp = nullptr;
+    if ((st = host_pipe(&hp)) != ATTN_OK) return st;
+    const int chunks = static_cast<int>(BH < kHostChunks ? BH : kHostChunks);
+    if (cudaEventRecord(hp->start, s) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->compute, hp->start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->copy_out, hp->start, 0) != cudaSuccess)
         return ATTN_ERR_CUDA;
-    st = enqueue_fwd(dq, dk, dv, do_, dlse, B, H, Nq, Nk, d, causal, scale, s);
-    if (st != ATTN_OK) return st;
-    if (cudaMemcpyAsync(o, do_, qbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        cudaMemcpyAsync(lse, dlse, lbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    const size_t qh = static_cast<size_t>(Nq) * d * 2, kh = static_cast<size_t>(Nk) * d * 2;
+    const size_t lh = static_cast<size_t>(Nq) * 4;
+    auto at = [](const void* base, size_t off) { return static_cast<const char*>(base) + off; };
+    auto atw = [](void* base, size_t off) { return static_cast<char*>(base) + off; };
+    long long h0 = 0;
+    for (int c = 0; c < chunks; ++c) {
+        const long long h1 = BH * (c + 1) / chunks;
+        const size_t n = static_cast<size_t>(h1 - h0);
+        const size_t oq = static_cast<size_t>(h0) * qh, ok = static_cast<size_t>(h0) * kh;
+        const size_t ol = static_cast<size_t>(h0) * lh;
+        if (cudaMemcpyAsync(atw(dq, oq), at(q, oq), n * qh, cudaMemcpyHostToDevice, s) !=
+                cudaSuccess ||
+            cudaMemcpyAsync(atw(dk, ok), at(k, ok), n * kh, cudaMemcpyHostToDevice, s) !=
+                cudaSuccess ||
+            cudaMemcpyAsync(atw(dv, ok), at(v, ok), n * kh, cudaMemcpyHostToDevice, s) !=
+                cudaSuccess ||
+            cudaEventRecord(hp->in_done[c], s) != cudaSuccess ||
+            cudaStreamWaitEvent(hp->compute, hp->in_done[c], 0) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        // the chunk as a batch of n heads (B = 1, H = n): the same per-head problem
+        st = enqueue_fwd(atw(dq, oq), atw(dk, ok), atw(dv, ok), atw(do_, oq),
+                         reinterpret_cast<float*>(atw(dlse, ol)), 1, static_cast<int>(n), Nq, Nk,
+                         d, causal, scale, hp->compute);
+        if (st != ATTN_OK) return st;
+        if (cudaEventRecord(hp->fwd_done[c], hp->compute) != cudaSuccess ||
+            cudaStreamWaitEvent(hp->copy_out, hp->fwd_done[c], 0) != cudaSuccess ||
+            cudaMemcpyAsync(atw(o, oq), atw(do_, oq), n * qh, cudaMemcpyDeviceToHost,
+                            hp->copy_out) != cudaSuccess ||
+            cudaMemcpyAsync(atw(lse, ol), atw(dlse, ol), n * lh, cudaMemcpyDeviceToHost,
+                            hp->copy_out) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        h0 = h1;
+    }
+    if (cudaEventRecord(hp->out_done, hp->copy_out) != cudaSuccess ||
+        cudaStreamWaitEvent(s, hp->out_done, 0) != cudaSuccess)
         return ATTN_ERR_CUDA;
     return ATTN_OK;
 }

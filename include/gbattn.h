@@ -113,13 +113,19 @@ int attn_fwd_decode(const void *q, const void *k, const void *v, void *o, float 
 /*
  * attn_fwd_from_host -- attn_fwd on HOST buffers, end to end.
  *
- * Enqueues on `stream`: host->device copies of q, k, v into the caller's
- * device buffers dq, dk, dv; attn_fwd on them into do_, dlse; device->host
- * copies of the results into o and lse.  The host buffers should be pinned
- * (page-locked) for the copies to be asynchronous.  The call returns once
- * everything is enqueued; the caller synchronises the stream before reading
- * o and lse.  Same arguments, sizes and status codes as attn_fwd; every
- * pointer must be non-NULL and the device ones 16-byte aligned.
+ * Host->device copies of q, k, v into the caller's device buffers dq, dk,
+ * dv; attn_fwd on them into do_, dlse; device->host copies of the results
+ * into o and lse.  The (b, h) heads go in up to four chunks so that one
+ * chunk's inputs cross the host link while the previous chunk computes and
+ * the one before returns its results: the input copies run on `stream`, the
+ * kernels and the output copies on two streams of the library's own
+ * (created with a few events on the first call on each device, kept until
+ * the process exits), and `stream` is made to wait for the last output copy.
+ * So, as for every call here, the caller synchronises `stream` before
+ * reading o and lse.  The host buffers should be pinned (page-locked) for
+ * the copies to be asynchronous.  Same arguments, sizes and status codes as
+ * attn_fwd; every pointer must be non-NULL and the device ones 16-byte
+ * aligned.
  */
 int attn_fwd_from_host(const void *q, const void *k, const void *v, void *o, float *lse,
                        void *dq, void *dk, void *dv, void *do_, float *dlse,

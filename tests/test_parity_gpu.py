@@ -311,17 +311,20 @@ def test_deterministic_and_stream_aware():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-def test_from_host_end_to_end():
-    B, H, N, d = 1, 4, 512, 128
-    q, k, v = make_qkv(B, H, N, N, d, seed=56, device="cpu")
+@pytest.mark.parametrize("B,H,N,d", [(1, 4, 512, 128), (1, 3, 300, 64), (1, 1, 200, 128),
+                                     (2, 5, 256, 128)])
+def test_from_host_end_to_end(B, H, N, d):
+    # the heads cross the host link in up to four chunks on three streams
+    q, k, v = make_qkv(B, H, N, N, d, seed=56 + H, device="cpu")
     qh, kh, vh = (t.pin_memory() for t in (q, k, v))
     oh = torch.empty((B, H, N, d), dtype=torch.bfloat16).pin_memory()
     lh = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
     dq, dk, dv = (torch.empty_like(t, device=_dev()) for t in (q, k, v))
     do_ = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=_dev())
     dl = torch.empty((B, H, N), dtype=torch.float32, device=_dev())
-    binding.attn_fwd_from_host(qh, kh, vh, oh, lh, dq, dk, dv, do_, dl, causal=True)
-    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    binding.attn_fwd_from_host(qh, kh, vh, oh, lh, dq, dk, dv, do_, dl, causal=True, stream=s)
+    s.synchronize()  # the caller's stream alone covers the whole call
     ro, rl = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), causal=True)
     _assert_close(oh.float().numpy(), lh.numpy(), ro, rl, "from_host")
 
