@@ -85,6 +85,7 @@ PREFILL_SOURCES = ["prefill_sm103.cu", "sm103_ptx.cuh"]
 DECODE_SOURCES = ["decode_sm103.cu", "sm103_ptx.cuh"]
 BACKWARD_SOURCES = ["backward_sm103.cu", "sm103_ptx.cuh"]
 MERGE_PARTS = 4  # key shards merged by attn_merge in the context-parallel measurement
+MERGE_SOURCES = ["merge_sm103.cu", "sm103_ptx.cuh"]
 # FLOPs of the backward: five products of the forward's size (S and dP
 # recomputed, dV, dK, dQ) against the forward's two.
 BWD_FLOP_RATIO = 2.5
@@ -573,7 +574,8 @@ def run_gpu(args):
         "workload": f"{MERGE_PARTS} shard results of {w3.name}", "value": world * m_gbs,
         "unit": "GB/s", "ms_per_call": m_per, "calls": bwd_reps, "bytes_per_call": m_bytes,
         "roofline": {"bound": "hbm", "achieved": m_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": m_gbs / peaks["hbm_gbs"], "traffic": None,
+                     "frac": m_gbs / peaks["hbm_gbs"],
+                     "traffic": profiled_traffic("ncu_merge_" + w3.name, MERGE_SOURCES),
                      "peak_source": f"{peak_src} HBM copy (MEASURED_PEAKS.json)"},
     }
 
