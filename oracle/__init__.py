@@ -17,6 +17,10 @@ Functions (each follows a passage of the lecture pages, cited in the C file):
   8.4), with D_i taken from its definition sum_j P_ij dP_ij.
 * :func:`attention_bwd_dq_rows`, :func:`attention_bwd_dkdv_keys` -- the same on
   listed query rows / key rows, for sampled checks of large problems.
+* :func:`decode_e4m3` -- value of FP8 E4M3 codes times a per-tensor descale
+  (CS336 L5 6.2; PDC L7 section 7.14).
+* :func:`fp8_operands` / :func:`attention_fp8` -- attention of per-tensor
+  scaled FP8 operands: decode, then the naive attention above.
 
 Inputs are numpy arrays, either float64 or bfloat16 bit patterns (uint16).
 """
@@ -51,6 +55,8 @@ def _declare(lib):
     lib.oracle_attention_bwd_dq_rows.restype = I
     lib.oracle_attention_bwd_dkdv_keys.argtypes = [P, P, P, P, I, P, L, P, P, L, L, L, L, L, I, D]
     lib.oracle_attention_bwd_dkdv_keys.restype = I
+    lib.oracle_decode_e4m3.argtypes = [P, P, L, D]
+    lib.oracle_decode_e4m3.restype = None
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = I
     return lib
@@ -215,3 +221,30 @@ def attention_bwd_dkdv_keys(q, k, v, dout, keys, causal=False, scale=None):
     if rc != 0:
         raise ValueError("oracle_attention_bwd_dkdv_keys rejected its arguments")
     return dk, dv
+
+
+def decode_e4m3(codes, descale=1.0):
+    """float64 values descale * E4M3(codes) of a uint8 array (same shape)."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(codes.shape, np.float64)
+    _load().oracle_decode_e4m3(_ptr(codes), _ptr(out), codes.size, float(descale))
+    return out
+
+
+def fp8_operands(q8, k8, vt8, descale_q=1.0, descale_k=1.0, descale_v=1.0):
+    """float64 Q, K, V of FP8 operands: q8 [B,H,Nq,d], k8 [B,H,Nk,d] and the
+    value tensor given transposed, vt8 [B,H,d,Nk] (uint8 E4M3 codes).  V is
+    returned in the [B,H,Nk,d] layout of :func:`attention`."""
+    q = decode_e4m3(q8, descale_q)
+    k = decode_e4m3(k8, descale_k)
+    v = np.ascontiguousarray(np.swapaxes(decode_e4m3(vt8, descale_v), 2, 3))
+    return q, k, v
+
+
+def attention_fp8(q8, k8, vt8, causal=False, scale=None, descale_q=1.0, descale_k=1.0,
+                  descale_v=1.0):
+    """Attention of per-tensor scaled FP8 operands (see :func:`fp8_operands`):
+    S = scale (descale_q Q8)(descale_k K8)^T, O = softmax(S) (descale_v V8).
+    Returns (o [B,H,Nq,d], lse [B,H,Nq]) in float64."""
+    q, k, v = fp8_operands(q8, k8, vt8, descale_q, descale_k, descale_v)
+    return attention(q, k, v, causal=causal, scale=scale)

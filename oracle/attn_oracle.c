@@ -598,3 +598,43 @@ ORACLE_ABI int oracle_attention_bwd_dkdv_keys(const void *q, const void *k, cons
     free(done);
     return err;
 }
+
+/* ---- FP8 (E4M3) inputs --------------------------------------------------- */
+
+/*
+ * Value of one 8-bit E4M3 code, the FP8 number format the lecture pages name
+ * for Blackwell's low-precision tensor cores (CS336 Lecture 5 notes, section
+ * 6.2; PDC course Lecture 7, section 7.14).  The pages name the format without
+ * spelling out its bits; the definition followed here is the OCP 8-bit floating
+ * point specification's E4M3: bit 7 the sign, bits 6-3 a biased exponent
+ * (bias 7), bits 2-0 the mantissa; exponent field 0 holds the subnormals
+ * (mantissa / 8) * 2^(1 - 7); the code with every exponent and mantissa bit
+ * set is NaN; there is no infinity, so the largest finite value is
+ * (1 + 6/8) * 2^8 = 448.
+ */
+static double e4m3_value(uint8_t code)
+{
+    const int sign = (code >> 7) & 1;
+    const int e = (code >> 3) & 15;
+    const int m = code & 7;
+    double mag;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        mag = ldexp((double)m / 8.0, 1 - 7);
+    else
+        mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+/*
+ * dst[i] = descale * value(src[i]) for n codes: the per-tensor dequantisation
+ * of an FP8 operand (PDC course Lecture 7, section 7.14: one scale per
+ * tensor).  The product of a 4-bit significand and a binary32 descale is
+ * exact in binary64.
+ */
+ORACLE_ABI void oracle_decode_e4m3(const uint8_t *src, double *dst, long n, double descale)
+{
+    for (long i = 0; i < n; ++i)
+        dst[i] = descale * e4m3_value(src[i]);
+}

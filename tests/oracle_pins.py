@@ -392,6 +392,77 @@ def pin_bwd_rows_and_keys_equal_full(orc):
             assert np.max(np.abs(dvk[t] - dv.reshape(2, 12, -1)[bh, j])) <= 1e-13
 
 
+# ---- FP8 (E4M3) operands ----------------------------------------------------
+
+def _fp8_codes(shape, seed, sigma=1.0):
+    """uint8 E4M3 codes of seeded normal values (torch's float8 rounding)."""
+    import torch
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(*shape, generator=g) * sigma
+    return x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def pin_e4m3_spec_values(orc):
+    """Codes whose values the E4M3 definition fixes: zeros, the smallest and
+    largest subnormal (2^-9, 7 * 2^-9), the smallest normal 2^-6, 0.5, 1, 1.5, 2,
+    the largest finite value 448, the sign bit and the two NaN codes."""
+    codes = np.array([0x00, 0x80, 0x01, 0x07, 0x08, 0x30, 0x38, 0x3C, 0x40, 0x7E, 0xB8, 0xFE,
+                      0x7F, 0xFF], np.uint8)
+    want = [0.0, -0.0, 2.0 ** -9, 7 * 2.0 ** -9, 2.0 ** -6, 0.5, 1.0, 1.5, 2.0, 448.0, -1.0,
+            -448.0]
+    got = orc.decode_e4m3(codes)
+    assert np.array_equal(got[:12], np.array(want))
+    assert np.signbit(got[1]) and np.all(np.isnan(got[12:]))
+
+
+def pin_e4m3_torch(orc):
+    """Every one of the 256 codes decodes to torch's float8_e4m3fn value, and the
+    descale multiplies it."""
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for ds in (1.0, 0.3125, 7.0):
+        got = orc.decode_e4m3(codes, ds)
+        nan = np.isnan(ref)
+        assert np.array_equal(np.isnan(got), nan)
+        assert np.array_equal(got[~nan], ref[~nan] * ds)
+
+
+def pin_fp8_attention_dequantised(orc):
+    """FP8 attention equals fp64 attention of the operands torch dequantises,
+    with V supplied transposed ([B,H,d,Nk]) and one descale per tensor."""
+    import torch
+    B, H, nq, nk, d = 1, 2, 7, 11, 16
+    q8, k8 = _fp8_codes((B, H, nq, d), 40), _fp8_codes((B, H, nk, d), 41)
+    vt8 = _fp8_codes((B, H, d, nk), 42)
+    dq, dk, dv = 0.375, 1.75, 0.0625
+
+    def deq(c, ds):
+        return torch.from_numpy(c.copy()).view(torch.float8_e4m3fn).to(torch.float64) * ds
+
+    q, k = deq(q8, dq).numpy(), deq(k8, dk).numpy()
+    v = deq(vt8, dv).transpose(2, 3).contiguous().numpy()
+    for causal in (False, True):
+        o1, l1 = orc.attention_fp8(q8, k8, vt8, causal=causal, scale=0.3, descale_q=dq,
+                                   descale_k=dk, descale_v=dv)
+        o2, l2 = orc.attention(q, k, v, causal=causal, scale=0.3)
+        assert np.max(np.abs(o1 - o2)) <= 1e-14 and np.max(np.abs(l1 - l2)) <= 1e-14
+
+
+def pin_fp8_descales(orc):
+    """The value descale multiplies O and leaves lse alone; the query and key
+    descales act as one factor on the scores (a change of scale)."""
+    B, H, nq, nk, d = 1, 1, 5, 9, 8
+    q8, k8, vt8 = _fp8_codes((B, H, nq, d), 43), _fp8_codes((B, H, nk, d), 44), \
+        _fp8_codes((B, H, d, nk), 45)
+    o1, l1 = orc.attention_fp8(q8, k8, vt8, scale=0.5)
+    o2, l2 = orc.attention_fp8(q8, k8, vt8, scale=0.5, descale_v=3.0)
+    assert np.max(np.abs(o2 - 3.0 * o1)) <= 1e-13 and np.array_equal(l1, l2)
+    o3, l3 = orc.attention_fp8(q8, k8, vt8, scale=0.5, descale_q=2.0, descale_k=0.25)
+    o4, l4 = orc.attention_fp8(q8, k8, vt8, scale=0.25)
+    assert np.max(np.abs(o3 - o4)) <= 1e-13 and np.max(np.abs(l3 - l4)) <= 1e-13
+
+
 ALL_PINS = [
     pin_exercise8_online_softmax,
     pin_memory_table,
@@ -414,4 +485,8 @@ ALL_PINS = [
     pin_bwd_exercise9_identity,
     pin_bwd_invariants,
     pin_bwd_rows_and_keys_equal_full,
+    pin_e4m3_spec_values,
+    pin_e4m3_torch,
+    pin_fp8_attention_dequantised,
+    pin_fp8_descales,
 ]
