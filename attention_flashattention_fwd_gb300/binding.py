@@ -38,6 +38,8 @@ def load():
         P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]
         lib.attn_fwd.restype = I
+        lib.attn_fwd_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, F, F, F, P]
+        lib.attn_fwd_fp8.restype = I
         lib.attn_fwd_decode_workspace_bytes.argtypes = [I, I, I, I]
         lib.attn_fwd_decode_workspace_bytes.restype = S
         lib.attn_fwd_decode.argtypes = [P, P, P, P, P, I, I, I, I, F, P, S, P]
@@ -125,6 +127,39 @@ def attn_fwd(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None)
     st = load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nk, d,
                          int(bool(causal)), float(scale), _stream_ptr(stream))
     _check(st, "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_fp8(q8, k8, vt8, descale_q=1.0, descale_k=1.0, descale_v=1.0, causal=False,
+                 scale=None, out=None, lse=None, stream=None):
+    """The C entry point ``attn_fwd_fp8`` on torch tensors.
+
+    q8 [B,H,Nq,d], k8 [B,H,Nk,d] and the transposed values vt8 [B,H,d,Nk]:
+    contiguous CUDA tensors of E4M3 codes (torch.float8_e4m3fn or uint8).
+    The operands are descale_* times the E4M3 values.  Returns
+    (o bf16 [B,H,Nq,d], lse fp32 [B,H,Nq]).
+    """
+    for name, t in (("q8", q8), ("k8", k8), ("vt8", vt8)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+            raise ValueError(f"{name} must hold E4M3 codes (float8_e4m3fn or uint8)")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D tensor")
+    B, H, Nq, d = q8.shape
+    Nk = k8.shape[2]
+    if k8.shape != (B, H, Nk, d) or vt8.shape != (B, H, d, Nk):
+        raise ValueError("k8 must be [B, H, Nk, d] and vt8 [B, H, d, Nk] with q8's B, H and d")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q8.device)
+    st = load().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(vt8), _ptr(out), _ptr(lse), B, H, Nq, Nk,
+                             d, int(bool(causal)), float(scale), float(descale_q),
+                             float(descale_k), float(descale_v), _stream_ptr(stream))
+    _check(st, "attn_fwd_fp8")
     return out, lse
 
 

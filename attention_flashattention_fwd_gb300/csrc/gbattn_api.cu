@@ -5,6 +5,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -139,7 +140,25 @@ int enqueue_fwd(const void* q, const void* k, const void* v, void* o, float* lse
     p.H = H;
     p.seqlens_q = seqlens_q;
     p.seqlens_k = seqlens_k;
+    p.o_scale = 1.f;
     return launch_prefill(d, tq, tk, tv, p, num_sms, stream);
+}
+
+// A 3-D byte tensor {x, y, BH} (x innermost, x bytes per row, y rows per
+// (b, h)) in boxes of 128 x 128 x 1 with the 128-byte swizzle: E4M3 Q and K
+// ({d, N, BH}) and the transposed values ({Nk, d, BH}).
+int encode_u8(CUtensorMap* m, const void* base, long long BH, int x, int y) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(x), static_cast<cuuint64_t>(y),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(x),
+                             static_cast<cuuint64_t>(x) * static_cast<cuuint64_t>(y)};
+    cuuint32_t box[3] = {128, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
+                                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 int enqueue_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
@@ -295,6 +314,43 @@ int attn_fwd_decode_ragged(const void* q, const void* k, const void* v, void* o,
     if (seqlens_k && (reinterpret_cast<uintptr_t>(seqlens_k) & 3u)) return ATTN_ERR_MISALIGNED;
     return decode_impl(q, k, v, o, lse, B, H, Nk, d, scale, workspace, workspace_bytes,
                        seqlens_k, stream);
+}
+
+int attn_fwd_fp8(const void* q, const void* k, const void* vt, void* o, float* lse, int B,
+                 int H, int Nq, int Nk, int d, int causal, float scale, float descale_q,
+                 float descale_k, float descale_v, void* stream) {
+    int st = validate_fwd(q, k, vt, o, lse, B, H, Nq, Nk, d, causal, scale);
+    if (st != ATTN_OK) return st;
+    for (float ds : {descale_q, descale_k, descale_v})
+        if (!(std::isfinite(ds) && ds > 0.f)) return ATTN_ERR_INVALID_ARG;
+    const double c = static_cast<double>(scale) * descale_q * descale_k;
+    if (!(c < 3.0e38)) return ATTN_ERR_INVALID_ARG;  // the folded score scale stays finite
+    if (d != 128) return ATTN_ERR_UNSUPPORTED;   // one 128-byte atom per row
+    if (Nk % 16 != 0) return ATTN_ERR_UNSUPPORTED;  // V^T rows: a multiple of 16 bytes
+    if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(o) || !aligned16(lse))
+        return ATTN_ERR_MISALIGNED;
+    if ((st = ensure_init()) != ATTN_OK) return st;
+    int num_sms = 0;
+    if ((st = current_sm_count(&num_sms)) != ATTN_OK) return st;
+    const long long BH = static_cast<long long>(B) * H;
+    CUtensorMap tq, tk, tvt;
+    if ((st = encode_u8(&tq, q, BH, d, Nq)) != ATTN_OK) return st;
+    if ((st = encode_u8(&tk, k, BH, d, Nk)) != ATTN_OK) return st;
+    if ((st = encode_u8(&tvt, vt, BH, Nk, d)) != ATTN_OK) return st;
+    PrefillParams p;
+    p.o = static_cast<__nv_bfloat16*>(o);
+    p.lse = lse;
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.BH = static_cast<int>(BH);
+    p.num_pairs = (Nq + 255) / 256;
+    p.causal = causal;
+    p.scale_log2 = static_cast<float>(c * 1.4426950408889634074);
+    p.H = H;
+    p.seqlens_q = nullptr;
+    p.seqlens_k = nullptr;
+    p.o_scale = descale_v;
+    return launch_prefill_fp8(tq, tk, tvt, p, num_sms, static_cast<cudaStream_t>(stream));
 }
 
 int attn_fwd_ragged(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -23,6 +23,7 @@ struct PrefillParams {
     int H;
     const int* seqlens_q;  // [B] per-sequence query counts, or null (all Nq)
     const int* seqlens_k;  // [B] per-sequence key counts, or null (all Nk)
+    float o_scale;         // FP8 operands: the value descale applied to O / l
 };
 
 // Arguments of the split-K decode kernels.
@@ -80,6 +81,9 @@ int prefill_set_attributes();
 // Persistent launch: min(work items, num_sms) CTAs, one per SM.
 int launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                    const PrefillParams& p, int num_sms, cudaStream_t stream);
+// E4M3 operands, d = 128; tvt maps the transposed values [BH, d, Nk].
+int launch_prefill_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+                       const PrefillParams& p, int num_sms, cudaStream_t stream);
 int prefill_smem_bytes(int d);
 unsigned read_and_clear_prefill_error();
 // Device error bits (shared by the kernels' error words)

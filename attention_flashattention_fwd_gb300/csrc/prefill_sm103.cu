@@ -31,6 +31,15 @@
 //     tensor core works on the other tile.
 // Scores use base 2: with c = scale * log2(e), p = 2^{s c - m} and
 // lse = ln2 (m + log2 l), identical in exact arithmetic to the e-based form.
+//
+// FP8 operands (kFp8): Q, K and V are E4M3 with one descale per tensor, the
+// per-tensor scaling of PDC course Lecture 7, section 7.14.  The products run
+// as kind::f8f6f4 (32 keys or 32 of d per instruction, half the instructions
+// of bf16 for the same tile), P is rounded to E4M3 for the P V product, the
+// query and key descales fold into c and the value descale into the final
+// 1 / l.  Both operands of an 8-bit product are K-major, so V comes
+// transposed ([B, H, d, Nk]: keys innermost), and its tile is one 128-byte
+// swizzle atom wide like the Q and K tiles at d = 128.
 #include <cuda_bf16.h>
 #include <cuda.h>
 
@@ -56,15 +65,21 @@ constexpr uint32_t kSoftmaxRegs = 192;
 constexpr uint32_t kControlRegs = 112;
 constexpr uint32_t kTmemCols = 512;
 // A key tile whose row sum against the stale reference max exceeds this moves
-// the reference (2^62: far from fp32 overflow for O and l).
-constexpr float kTileSumLimit = 4.611686018427387904e18f;
+// the reference.  bf16 P: 2^62, far from fp32 overflow for O and l.  E4M3 P:
+// 448, the largest finite E4M3 value; a row sum within it bounds every p of
+// the row, so no p saturates.
+constexpr float kTileSumLimitBf16 = 4.611686018427387904e18f;
+constexpr float kTileSumLimitE4m3 = 448.f;
 
-template <int D>
+template <int D, bool kFp8>
 struct Cfg {
-    static constexpr int kSub = D / 64;                  // 128-byte swizzle atoms along d
+    static constexpr int kElem = kFp8 ? 1 : 2;           // bytes per Q, K, V element
+    static constexpr int kSubElems = 128 / kElem;        // elements per 128-byte atom row
+    static constexpr int kSub = D / kSubElems;           // 128-byte swizzle atoms along d
     static constexpr int kSubBytes = 128 * 128;          // one atom column: 128 rows x 128 B
-    static constexpr int kTileBytes = kBM * D * 2;       // a Q, K or V tile in bf16
-    static constexpr int kSlots = (D == 128) ? 4 : 8;    // K/V ring slots
+    static constexpr int kTileBytes = kBM * D * kElem;   // a Q, K or V tile
+    static constexpr int kSlots = (kTileBytes >= 32768) ? 4 : 8;  // K/V ring slots
+    static constexpr int kKSteps = D * kElem / 32;       // MMA k-steps of S = Q K^T (32 B each)
     static constexpr int kQOff = 0;
     static constexpr int kRingOff = 2 * kTileBytes;
     static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
@@ -75,7 +90,7 @@ struct Cfg {
     static constexpr int kAbortOff = kTmemSlotOff + 4;
     static constexpr int kSmemBytes = kAbortOff + 4 + 1024;  // + alignment slack
     // Tensor Memory columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 after it;
-    // P_t (bf16 pairs) overwrites the first 64 columns of S_t.
+    // P_t (bf16 pairs: 64 columns; E4M3 quads: 32) overwrites the first columns of S_t.
     __device__ static uint32_t col_s(int t) { return static_cast<uint32_t>(t) * 128u; }
     __device__ static uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(t) * D; }
 };
@@ -173,13 +188,15 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
 }  // namespace
 
 // kRagged: per-sequence lengths (seqlens_q / seqlens_k) are read; the
-// instantiation without them is the plain [B, H, Nq, Nk] problem.
-template <int D, bool kRagged>
+// instantiation without them is the plain [B, H, Nq, Nk] problem.  kFp8: E4M3
+// operands, tm_v maps the transposed values [BH, d, Nk].
+template <int D, bool kRagged, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                             const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, PrefillParams p) {
-    using C = Cfg<D>;
+    static_assert(!kFp8 || (D == 128 && !kRagged), "E4M3 operands: d = 128, no sequence lengths");
+    using C = Cfg<D, kFp8>;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle pattern
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -241,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(bars.q_full(t), C::kTileBytes);
                 for (int s = 0; s < C::kSub; ++s)
                     tma_load_3d(sQ + t * C::kTileBytes + s * C::kSubBytes, &tm_q, bars.q_full(t),
-                                s * 64, it.row0 + t * kBM, it.bh);
+                                s * C::kSubElems, it.row0 + t * kBM, it.bh);
             };
             auto load_kv = [&](int which, int j, const Item& it) {  // K_j (0) or V_j (1)
                 const int u = issued;  // K_j is use 2j, V_j is use 2j + 1 of the item
@@ -250,10 +267,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     !(ok = wait_or_abort(bars.empty(slot), ((u / C::kSlots) & 1) ^ 1, abort_flag)))
                     return;
                 mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
-                const CUtensorMap* tm = which ? &tm_v : &tm_k;
-                for (int s = 0; s < C::kSub; ++s)
-                    tma_load_3d(sRing + slot * C::kTileBytes + s * C::kSubBytes, tm,
-                                bars.full(slot), s * 64, j * kBN, it.bh);
+                if (kFp8 && which) {
+                    // V^T tile: d rows of 128 keys, one atom wide
+                    tma_load_3d(sRing + slot * C::kTileBytes, &tm_v, bars.full(slot), j * kBN, 0,
+                                it.bh);
+                } else {
+                    const CUtensorMap* tm = which ? &tm_v : &tm_k;
+                    for (int s = 0; s < C::kSub; ++s)
+                        tma_load_3d(sRing + slot * C::kTileBytes + s * C::kSubBytes, tm,
+                                    bars.full(slot), s * C::kSubElems, j * kBN, it.bh);
+                }
                 ++issued;
             };
             int kp = 0;  // items processed (empty items are skipped by every role)
@@ -273,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const Item nx = item_at<kRagged>(p, nidx);
                     for (int t = 0; t < 2; ++t)
                         for (int s = 0; s < C::kSub; ++s)
-                            tma_prefetch_l2_3d(&tm_q, s * 64, nx.row0 + t * kBM, nx.bh);
+                            tma_prefetch_l2_3d(&tm_q, s * C::kSubElems, nx.row0 + t * kBM, nx.bh);
                 }
                 for (int j = 1; j < it.n_kv_max() && ok; ++j) {
                     load_kv(0, j, it);
@@ -302,8 +325,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // tile 1 instead (see there) and P V completion is only committed at
         // the end of an item.
         if (lane == 0) {
-            const uint32_t idesc_qk = umma_idesc_bf16(kBM, kBN, false);
-            const uint32_t idesc_pv = umma_idesc_bf16(kBM, D, true);
+            const uint32_t idesc_qk =
+                kFp8 ? umma_idesc_e4m3(kBM, kBN) : umma_idesc_bf16(kBM, kBN, false);
+            const uint32_t idesc_pv =
+                kFp8 ? umma_idesc_e4m3(kBM, D) : umma_idesc_bf16(kBM, D, true);
             int u = 0;             // ring use of the current K tile
             int iter[2] = {0, 0};  // key tiles processed per query tile, over all items
             auto wait_use = [&](int use) {
@@ -312,17 +337,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             // Descriptors are built once; the k-steps only move the start address
             // (bits 0-13 of the low word, in 16-byte units), which never carries.
+            // bf16 V is the MN-major B operand (its two 64-wide halves of d
+            // kSubBytes apart); E4M3 V^T is K-major like K.
             const uint64_t dq0 = umma_desc_sw128(sQ, 16, 1024);
             const uint64_t dk0 = umma_desc_sw128(sRing, 16, 1024);
-            const uint64_t dv0 = umma_desc_sw128(sRing, C::kSubBytes, 1024);
+            const uint64_t dv0 = umma_desc_sw128(sRing, kFp8 ? 16u : C::kSubBytes, 1024);
             auto issue_s = [&](int t, int use) {  // S_t = Q_t K^T, K in ring use `use`
                 const uint64_t da = dq0 + ((t * C::kTileBytes) >> 4);
                 const uint64_t db = dk0 + (((use % C::kSlots) * C::kTileBytes) >> 4);
                 const uint32_t dst = tmem + C::col_s(t);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
+                for (int kk = 0; kk < C::kKSteps; ++kk) {
                     const uint32_t off = ((kk >> 2) * C::kSubBytes + (kk & 3) * 32) >> 4;
-                    umma_ss(dst, da + off, db + off, idesc_qk, kk > 0 ? 1u : 0u);
+                    if constexpr (kFp8)
+                        umma_ss_f8(dst, da + off, db + off, idesc_qk, kk > 0 ? 1u : 0u);
+                    else
+                        umma_ss(dst, da + off, db + off, idesc_qk, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(bars.s_full(t));
             };
@@ -330,12 +360,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t db = dv0 + (((use % C::kSlots) * C::kTileBytes) >> 4);
                 const uint32_t dst = tmem + C::col_o(t);
                 const uint32_t pa = tmem + C::col_s(t);
+                if constexpr (kFp8) {
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    // P: 16 keys = 8 packed columns; V: 16 key rows of 128 B,
-                    // the two 64-wide halves of d are kSubBytes apart (LBO)
-                    umma_ts(dst, pa + kk * 8, db + ((kk * 16 * 128) >> 4), idesc_pv,
-                            (!first || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kBN / 32; ++kk) {
+                        // P: 32 keys = 8 packed columns; V^T: the next 32 bytes
+                        // (keys) of every d row
+                        umma_ts_f8(dst, pa + kk * 8, db + ((kk * 32) >> 4), idesc_pv,
+                                   (!first || kk > 0) ? 1u : 0u);
+                    }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk) {
+                        // P: 16 keys = 8 packed columns; V: 16 key rows of 128 B,
+                        // the two 64-wide halves of d are kSubBytes apart (LBO)
+                        umma_ts(dst, pa + kk * 8, db + ((kk * 16 * 128) >> 4), idesc_pv,
+                                (!first || kk > 0) ? 1u : 0u);
+                    }
                 }
             };
             bool ok = true;
@@ -463,21 +503,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float mneg = (m_ref == -INFINITY) ? 0.f : -m_ref;
                     const float2 c2 = make_float2(cl2, cl2), m2 = make_float2(mneg, mneg);
                     float2 ls0 = make_float2(0.f, 0.f), ls1 = make_float2(0.f, 0.f);
+                    if constexpr (kFp8) {
+                        uint32_t pk[32];  // 4 E4M3 values per column
 #pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            const float2 x = ffma2(
-                                make_float2(s[h * 32 + 2 * c], s[h * 32 + 2 * c + 1]), c2, m2);
-                            const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                            if (c & 1) ls1 = fadd2(ls1, pp); else ls0 = fadd2(ls0, pp);
-                            pk[c] = pack_bf16x2(pp.x, pp.y);
+                        for (int c = 0; c < 32; ++c) {
+                            const float2 x0 = ffma2(make_float2(s[4 * c], s[4 * c + 1]), c2, m2);
+                            const float2 x1 =
+                                ffma2(make_float2(s[4 * c + 2], s[4 * c + 3]), c2, m2);
+                            const float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+                            const float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+                            ls0 = fadd2(ls0, p0);
+                            ls1 = fadd2(ls1, p1);
+                            pk[c] = pack_e4m3x4(p0.x, p0.y, p1.x, p1.y);
                         }
-                        tmem_st16(tS + h * 16, pk);  // P over the first 64 columns of S
+                        tmem_st32(tS, pk);  // P over the first 32 columns of S
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) {
+                                const float2 x = ffma2(
+                                    make_float2(s[h * 32 + 2 * c], s[h * 32 + 2 * c + 1]), c2, m2);
+                                const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                                if (c & 1) ls1 = fadd2(ls1, pp); else ls0 = fadd2(ls0, pp);
+                                pk[c] = pack_bf16x2(pp.x, pp.y);
+                            }
+                            tmem_st16(tS + h * 16, pk);  // P over the first 64 columns of S
+                        }
                     }
                     return (ls0.x + ls0.y) + (ls1.x + ls1.y);
                 };
+                constexpr float kTileSumLimit = kFp8 ? kTileSumLimitE4m3 : kTileSumLimitBf16;
                 // The reference m_ref is the row max of the item's first key tile and
                 // is only moved when a later tile would overflow against it: O and l
                 // share the reference, so any reference gives the same O / l, and
@@ -526,7 +583,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the item's last V tile is free once its last P V product is done
             if (t == 1 && wq == 0 && lane == 0)
                 mbar_arrive(bars.empty((2 * iter - 1) % C::kSlots));
-            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            float inv_l = l > 0.f ? 1.f / l : 0.f;
+            if constexpr (kFp8) inv_l *= p.o_scale;
             __nv_bfloat16* orow = p.o + (static_cast<size_t>(it.bh) * p.Nq + row) * D;
 #pragma unroll
             for (int ch = 0; ch < D / 32; ++ch) {
@@ -568,14 +626,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int prefill_set_attributes() {
     const auto a = cudaFuncAttributeMaxDynamicSharedMemorySize;
-    if (cudaFuncSetAttribute(attn_fwd_prefill_kernel<128, false>, a, Cfg<128>::kSmemBytes) !=
+    const int s128 = Cfg<128, false>::kSmemBytes, s64 = Cfg<64, false>::kSmemBytes;
+    if (cudaFuncSetAttribute(attn_fwd_prefill_kernel<128, false, false>, a, s128) !=
             cudaSuccess ||
-        cudaFuncSetAttribute(attn_fwd_prefill_kernel<64, false>, a, Cfg<64>::kSmemBytes) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(attn_fwd_prefill_kernel<128, true>, a, Cfg<128>::kSmemBytes) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(attn_fwd_prefill_kernel<64, true>, a, Cfg<64>::kSmemBytes) !=
-            cudaSuccess)
+        cudaFuncSetAttribute(attn_fwd_prefill_kernel<64, false, false>, a, s64) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_fwd_prefill_kernel<128, true, false>, a, s128) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_fwd_prefill_kernel<64, true, false>, a, s64) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_fwd_prefill_kernel<128, false, true>, a,
+                             Cfg<128, true>::kSmemBytes) != cudaSuccess)
         return ATTN_ERR_CUDA;
     return ATTN_OK;
 }
@@ -583,14 +641,14 @@ int prefill_set_attributes() {
 template <int D>
 static int launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const PrefillParams& p, int num_sms, cudaStream_t stream) {
-    using C = Cfg<D>;
+    using C = Cfg<D, false>;
     const long long items = static_cast<long long>(p.num_pairs) * p.BH;
     const long long grid = items < num_sms ? items : num_sms;  // one persistent CTA per SM
     if (p.seqlens_q || p.seqlens_k)
-        attn_fwd_prefill_kernel<D, true>
+        attn_fwd_prefill_kernel<D, true, false>
             <<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
     else
-        attn_fwd_prefill_kernel<D, false>
+        attn_fwd_prefill_kernel<D, false, false>
             <<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -601,7 +659,19 @@ int launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CU
                     : launch_prefill_d<64>(tq, tk, tv, p, num_sms, stream);
 }
 
-int prefill_smem_bytes(int d) { return d == 128 ? Cfg<128>::kSmemBytes : Cfg<64>::kSmemBytes; }
+int launch_prefill_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+                       const PrefillParams& p, int num_sms, cudaStream_t stream) {
+    using C = Cfg<128, true>;
+    const long long items = static_cast<long long>(p.num_pairs) * p.BH;
+    const long long grid = items < num_sms ? items : num_sms;
+    attn_fwd_prefill_kernel<128, false, true>
+        <<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tq, tk, tvt, p);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int prefill_smem_bytes(int d) {
+    return d == 128 ? Cfg<128, false>::kSmemBytes : Cfg<64, false>::kSmemBytes;
+}
 
 unsigned read_and_clear_prefill_error() {
     unsigned v = 0, zero = 0;

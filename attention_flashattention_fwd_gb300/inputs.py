@@ -83,6 +83,37 @@ def make_workload(w: Workload, device="cpu", seed=None):
                     sigma_qk=w.sigma_qk)
 
 
+E4M3_MAX = 448.0  # largest finite float8_e4m3fn value
+
+
+def make_qkv_fp8(B, H, Nq, Nk, d, seed, device="cpu", sigma_qk=1.0, sigma_v=1.0):
+    """FP8 (E4M3) operands with one descale per tensor, for ``attn_fwd_fp8``.
+
+    The Gaussian draws of :func:`make_qkv` (same seed and order, fp32 before any
+    rounding), each tensor divided by its descale amax / 448 (so its largest
+    magnitude lands on the largest E4M3 value) and rounded by torch to
+    float8_e4m3fn.  Returns (q8 [B,H,Nq,d], k8 [B,H,Nk,d], vt8 [B,H,d,Nk] -- the
+    values transposed, keys innermost -- as uint8 codes, and the descales
+    (dq, dk, dv) as Python floats holding fp32 values)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    out, ds = [], []
+    for shape, sigma in (((B, H, Nq, d), sigma_qk), ((B, H, Nk, d), sigma_qk),
+                         ((B, H, Nk, d), sigma_v)):
+        x = torch.randn(shape, generator=g, device=device, dtype=torch.float32) * sigma
+        descale = torch.clamp(x.abs().max() / E4M3_MAX, min=2.0 ** -100).to(torch.float32)
+        codes = torch.clamp(x / descale, -E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+        out.append(codes.view(torch.uint8))
+        ds.append(float(descale))
+    q8, k8, v8 = out
+    return q8, k8, v8.transpose(2, 3).contiguous(), tuple(ds)
+
+
+def make_workload_fp8(w: Workload, device="cpu", seed=None):
+    return make_qkv_fp8(w.B, w.H, w.Nq, w.Nk, w.d, w.seed if seed is None else seed, device,
+                        sigma_qk=w.sigma_qk)
+
+
 def bf16_bits(t: torch.Tensor):
     """The raw 16-bit patterns of a bf16 tensor as a numpy uint16 array (CPU copy)."""
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view("uint16")

@@ -55,8 +55,9 @@ def parse_args():
                     help="run only this workload's kernel(s) (profiling runs); prints its time")
     ap.add_argument("--shape", default=None,
                     help="with --case custom: B,H,Nq,Nk,d,causal of a profiling workload")
-    ap.add_argument("--pass", dest="which", choices=["fwd", "bwd"], default="fwd",
-                    help="with --case: time the forward (default) or the backward call")
+    ap.add_argument("--pass", dest="which", choices=["fwd", "bwd", "fp8"], default="fwd",
+                    help="with --case: time the forward (default), the backward call or the "
+                         "forward on FP8 (E4M3) operands")
     a = ap.parse_args()
     a.warmup = max(3, a.warmup)
     a.steps = max(1, a.steps)
@@ -84,6 +85,7 @@ def _sources_sha(names):
 PREFILL_SOURCES = ["prefill_sm103.cu", "sm103_ptx.cuh"]
 DECODE_SOURCES = ["decode_sm103.cu", "sm103_ptx.cuh"]
 BACKWARD_SOURCES = ["backward_sm103.cu", "sm103_ptx.cuh"]
+FP8_PEAK_RATIO = 2.0  # nominal dense fp8 : bf16 tensor rate (4.5 : 2.25 PFLOP/s)
 MERGE_PARTS = 4  # key shards merged by attn_merge in the context-parallel measurement
 MERGE_SOURCES = ["merge_sm103.cu", "sm103_ptx.cuh"]
 # FLOPs of the backward: five products of the forward's size (S and dP
@@ -334,6 +336,16 @@ def run_case(args):
         def launch():  # noqa: F811  (the timed call is the backward)
             binding.attn_bwd(q, k, v, o, lse, dout, causal=w.causal, scale=w.scale, dq=dq, dk=dk,
                              dv=dv, workspace=bws)
+    elif args.which == "fp8":
+        if w.decode or w.d != 128:
+            raise SystemExit("--pass fp8 needs a d = 128 prefill workload")
+        from attention_flashattention_fwd_gb300.inputs import make_workload_fp8
+        del q, k, v
+        q8, k8, vt8, ds8 = make_workload_fp8(w, device=dev)
+
+        def launch():  # noqa: F811  (the timed call is the FP8 forward)
+            binding.attn_fwd_fp8(q8, k8, vt8, *ds8, causal=w.causal, scale=w.scale, out=o,
+                                 lse=lse)
 
     for _ in range(args.warmup):
         launch()
@@ -548,6 +560,47 @@ def run_gpu(args):
     noncausal["calls"] = bwd_reps
     del qn, kn, vn, on, ln
 
+    # ---- FP8 (E4M3) operands on the headline workload (not part of the timed
+    # step): the same Gaussian draws, per-tensor scaled to E4M3
+    from attention_flashattention_fwd_gb300.inputs import make_workload_fp8
+    q8, k8, vt8, ds8 = make_workload_fp8(w3, device=dev)
+    o8, l8 = torch.empty_like(o3), torch.empty_like(l3)
+
+    def fp8_call():
+        binding.attn_fwd_fp8(q8, k8, vt8, *ds8, causal=True, scale=w3.scale, out=o8, lse=l8,
+                             stream=stream)
+
+    for _ in range(3):
+        fp8_call()
+    torch.cuda.synchronize()
+    f_ms = 0.0
+    for _ in range(bwd_reps):
+        flush.zero_()
+        torch.cuda._sleep(LAUNCH_COVER_CYCLES)
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        fp8_call()
+        b1.record(stream)
+        torch.cuda.synchronize()
+        f_ms += b0.elapsed_time(b1)
+    if binding.device_error() != 0:
+        raise RuntimeError("a kernel reported a device-side error in the FP8 forward")
+    (f_ms,) = max_over_ranks([f_ms], world, device=dev)
+    f_per = f_ms / bwd_reps
+    f_tf = w3.flops() / (f_per * 1e-3) / 1e12
+    fp8_peak = FP8_PEAK_RATIO * peaks["bf16_tflops"]
+    fp8 = {
+        "workload": w3.name, "operands": "E4M3, one descale per tensor; V transposed",
+        "value": world * f_tf, "unit": "TFLOP/s", "ms_per_call": f_per, "calls": bwd_reps,
+        "frac_of_4500": f_tf / 4500.0,
+        "roofline": {"bound": "tensor", "achieved": f_tf, "peak": fp8_peak, "unit": "TFLOP/s",
+                     "frac": f_tf / fp8_peak,
+                     "traffic": profiled_traffic("ncu_prefill_fp8_" + w3.name, PREFILL_SOURCES),
+                     "peak_source": f"{FP8_PEAK_RATIO:g} x {peak_src} bf16 dense burst "
+                                    "(MEASURED_PEAKS.json; nominal fp8:bf16 = 4.5:2.25)"},
+    }
+    del q8, k8, vt8, o8, l8
+
     # ---- the exchange step of key-sharded attention (not part of the timed step):
     # attn_merge of MERGE_PARTS shard results of the headline shape
     o_parts = torch.stack([o3] * MERGE_PARTS).contiguous()
@@ -592,6 +645,7 @@ def run_gpu(args):
         "roofline": p3["roofline"],
         "parts": {HEADLINE: p3, LONG: p4, DECODE: p5},
         "noncausal": noncausal,
+        "fp8": fp8,
         "backward": backward,
         "merge": merge,
         "e2e": e2e,

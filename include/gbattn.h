@@ -81,6 +81,39 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
              int B, int H, int Nq, int Nk, int d, int causal, float scale, void *stream);
 
 /*
+ * attn_fwd_fp8 -- attn_fwd on FP8 (E4M3) operands with one descale per tensor.
+ *
+ * Blackwell's tensor cores run 8-bit products at twice the bf16 rate, with
+ * per-tensor (or finer) scaling (PDC course Lecture 7, section 7.14; E4M3 in
+ * CS336 Lecture 5 notes, section 6.2).  With Q = descale_q * q, K = descale_k
+ * * k and V = descale_v * v (q, k, v the E4M3 values), computes exactly what
+ * attn_fwd computes on Q, K, V:
+ *   s_ij = scale * sum_c Q[b,h,i,c] K[b,h,j,c], the same causal rule,
+ *   o = softmax(s) V (bf16), lse = log sum_j e^{s_ij} (fp32, natural log).
+ *
+ *   q        device, E4M3 codes (one byte each) [B,H,Nq,d]; read only.
+ *   k        device, E4M3 [B,H,Nk,d]; read only.
+ *   vt       device, E4M3, the values TRANSPOSED: [B,H,d,Nk] (keys innermost).
+ *            Both operands of an 8-bit tensor-core product are read with the
+ *            reduction dimension innermost, and for O += P V that is the key.
+ *   o        device, bf16 [B,H,Nq,d]; written.
+ *   lse      device, fp32 [B,H,Nq]; written.
+ *   B, H, Nq, Nk >= 1;  d = 128;  Nk a multiple of 16 (rows of vt are TMA
+ *            rows and must span a multiple of 16 bytes); causal as attn_fwd.
+ *   scale, descale_q, descale_k, descale_v  > 0 and finite, with
+ *            scale * descale_q * descale_k finite in fp32.
+ * Internal arithmetic: exact E4M3 products accumulated in fp32, the query and
+ * key descales folded into the fp32 score scale, probabilities rounded to E4M3
+ * before the P V product (row sums from the unrounded fp32 values), descale_v
+ * applied with 1 / l in the epilogue.
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED (d != 128,
+ * Nk % 16 != 0, causal with Nq > Nk), ATTN_ERR_MISALIGNED or ATTN_ERR_CUDA.
+ */
+int attn_fwd_fp8(const void *q, const void *k, const void *vt, void *o, float *lse,
+                 int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                 float descale_q, float descale_k, float descale_v, void *stream);
+
+/*
  * attn_fwd_decode_workspace_bytes -- bytes of device workspace attn_fwd_decode
  * needs for these sizes (0 when a single split covers every key).  Pure host
  * arithmetic; never touches the GPU.  Returns 0 for invalid sizes as well.

@@ -177,3 +177,21 @@ def test_ragged_entry_points_reject_before_launch(lib):
                                       8192, 128, 0.1, P(FAKE), need, P(0)) == MISALIGNED
     assert lib.attn_fwd_decode_ragged(P(0), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1, 1,
                                       8192, 128, 0.1, P(FAKE), need, P(0)) == INVALID
+
+
+def test_fp8_entry_point_rejects_before_launch(lib):
+    P = ctypes.c_void_p
+
+    def f8(q=FAKE, vt=FAKE, o=FAKE, d=128, Nq=128, Nk=128, causal=0, scale=0.1, dq=0.01,
+           dk=0.01, dv=0.01):
+        return lib.attn_fwd_fp8(P(q), P(FAKE), P(vt), P(o), P(FAKE), 1, 2, Nq, Nk, d, causal,
+                                scale, dq, dk, dv, P(0))
+
+    assert f8(q=0) == INVALID and f8(vt=0) == INVALID and f8(Nq=0) == INVALID
+    assert f8(dq=0.0) == INVALID and f8(dk=-1.0) == INVALID and f8(dv=float("nan")) == INVALID
+    assert f8(dv=float("inf")) == INVALID and f8(scale=0.0) == INVALID
+    assert f8(scale=1e30, dq=1e10, dk=1e10) == INVALID    # folded score scale overflows fp32
+    assert f8(d=64) == UNSUPPORTED and f8(d=96) == UNSUPPORTED
+    assert f8(Nk=120) == UNSUPPORTED                        # V^T rows of 120 bytes
+    assert f8(causal=1, Nq=256, Nk=128) == UNSUPPORTED
+    assert f8(vt=FAKE + 8) == MISALIGNED and f8(o=FAKE + 2) == MISALIGNED
