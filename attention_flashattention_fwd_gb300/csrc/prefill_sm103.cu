@@ -21,12 +21,15 @@
 //     concept 2, deeper than two), running ahead across item boundaries;
 //   * warp 8 (one thread) issues tcgen05.mma: S_t = Q_t K_j^T into Tensor
 //     Memory, then O_t += P_t V_j with P read from Tensor Memory;
+//   * warp 10 (one thread) relays the ring: it waits for V_j and K_{j+1} to
+//     land and adds its arrival to the barrier the softmax warps signal P_t(j)
+//     on, so the MMA thread waits on one barrier per pair of products;
 //   * warps 0-3 and 4-7 are the softmax warpgroups of query tiles 0 and 1: a
 //     thread owns one query row (= one TMEM lane), so row max and row sum need
 //     no shuffles; it writes P back as bf16 over its own S columns, rescales
 //     its O row in TMEM when a key tile lies far above the running reference
-//     max, and at the end of an item writes O / l and the logsumexp, then
-//     hands the O columns back to the MMA warp for the next item;
+//     max, and at the end of an item writes O / l and the logsumexp (its next
+//     P arrival tells the MMA warp that the O columns are free again);
 //   * the two query tiles ping-pong: while one warpgroup runs its softmax the
 //     tensor core works on the other tile.
 // Scores use base 2: with c = scale * log2(e), p = 2^{s c - m} and
@@ -54,9 +57,10 @@ namespace {
 
 constexpr int kBM = 128;            // query rows per tile (MMA M)
 constexpr int kBN = 128;            // keys per tile (MMA N of S = Q K^T)
-constexpr int kThreads = 384;       // 12 warps: 8 softmax, MMA, TMA, 2 idle
+constexpr int kThreads = 384;       // 12 warps: 8 softmax, MMA, TMA, relay, 1 idle
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
+constexpr int kRelayWarp = 10;
 // Register split.  The launch gives every thread 168 registers (65536 / 384,
 // rounded down to 8): 384 x 168 = 64512.  The warpgroup of the MMA and TMA warps
 // gives most of its share to the two softmax warpgroups:
@@ -84,8 +88,8 @@ struct Cfg {
     static constexpr int kRingOff = 2 * kTileBytes;
     static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
     // barriers: full[kSlots], empty[kSlots], then per query tile q_full, q_empty,
-    // s_full, p_ready, pv_done, o_free, then fin
-    static constexpr int kNumBars = 2 * kSlots + 12 + 1;
+    // s_full, p_ready, pv_done, then fin
+    static constexpr int kNumBars = 2 * kSlots + 10 + 1;
     static constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
     static constexpr int kAbortOff = kTmemSlotOff + 4;
     static constexpr int kSmemBytes = kAbortOff + 4 + 1024;  // + alignment slack
@@ -99,13 +103,12 @@ struct Bars {
     uint32_t full0, empty0, tile0, fin;
     __device__ uint32_t full(int i) const { return full0 + 8u * i; }
     __device__ uint32_t empty(int i) const { return empty0 + 8u * i; }
-    // six barriers per query tile t
-    __device__ uint32_t q_full(int t) const { return tile0 + 8u * (6 * t + 0); }
-    __device__ uint32_t q_empty(int t) const { return tile0 + 8u * (6 * t + 1); }
-    __device__ uint32_t s_full(int t) const { return tile0 + 8u * (6 * t + 2); }
-    __device__ uint32_t p_ready(int t) const { return tile0 + 8u * (6 * t + 3); }
-    __device__ uint32_t pv_done(int t) const { return tile0 + 8u * (6 * t + 4); }
-    __device__ uint32_t o_free(int t) const { return tile0 + 8u * (6 * t + 5); }
+    // five barriers per query tile t
+    __device__ uint32_t q_full(int t) const { return tile0 + 8u * (5 * t + 0); }
+    __device__ uint32_t q_empty(int t) const { return tile0 + 8u * (5 * t + 1); }
+    __device__ uint32_t s_full(int t) const { return tile0 + 8u * (5 * t + 2); }
+    __device__ uint32_t p_ready(int t) const { return tile0 + 8u * (5 * t + 3); }
+    __device__ uint32_t pv_done(int t) const { return tile0 + 8u * (5 * t + 4); }
 };
 
 // Geometry of work item `idx` (0 <= idx < num_pairs * BH).  With per-sequence
@@ -208,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars.full0 = sbase + C::kBarOff;
     bars.empty0 = bars.full0 + 8 * C::kSlots;
     bars.tile0 = bars.empty0 + 8 * C::kSlots;
-    bars.fin = bars.tile0 + 8 * 12;
+    bars.fin = bars.tile0 + 8 * 10;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kTmemSlotOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
 
@@ -226,9 +229,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bars.q_full(t), 1);
             mbar_init(bars.q_empty(t), 1);
             mbar_init(bars.s_full(t), 1);
-            mbar_init(bars.p_ready(t), 4);  // one arrival per softmax warp
+            // one arrival per softmax warp and one from the relay warp
+            mbar_init(bars.p_ready(t), 5);
             mbar_init(bars.pv_done(t), 1);
-            mbar_init(bars.o_free(t), 4);   // one arrival per softmax warp
         }
         mbar_init(bars.fin, 1);
         *abort_flag = 0;
@@ -397,25 +400,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 for (int j = 0; j < nmax && ok; ++j) {
                     const int uv = u + 1, uk = u + 2;  // V_j, K_{j+1}
-                    ok = wait_use(uv);
-                    bool k_next_ready = false;
                     for (int t = 0; t < 2 && ok; ++t) {
                         if (j >= it.n_kv(t)) continue;
+                        // one wait covers P_t(j) in Tensor Memory, V_j and K_{j+1} in
+                        // shared memory (the relay warp's arrival) and, at j = 0, the
+                        // previous item's O_t read by its epilogue (the softmax warps
+                        // arrive here only after their epilogue's loads completed)
                         if (!(ok = wait_or_abort(bars.p_ready(t), iter[t] & 1, abort_flag)))
-                            break;
-                        // O_t of the previous item has been read by its epilogue
-                        if (j == 0 && kp > 0 &&
-                            !(ok = wait_or_abort(bars.o_free(t), (kp - 1) & 1, abort_flag)))
                             break;
                         tc_fence_after();
                         issue_pv(t, uv, j == 0);
                         ++iter[t];
                         if (j + 1 < it.n_kv(t)) {
-                            if (!k_next_ready) {
-                                if (!(ok = wait_use(uk))) break;
-                                tc_fence_after();
-                                k_next_ready = true;
-                            }
                             issue_s(t, uk);
                             if (j + 2 == it.n_kv(t)) umma_commit(bars.q_empty(t));
                         } else {
@@ -431,7 +427,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(bars.fin, 0);
         }
         __syncwarp();
-    }  // warps 10 and 11 have no role
+    } else if (warp == kRelayWarp) {
+        // ================================================= ring relay
+        // Every barrier wait costs the MMA thread about as long as two products
+        // take to run once the softmax warps share its sub-partition, and the
+        // tensor core's queue holds only a few products.  This thread takes the
+        // ring waits off it: it waits for V_j and K_{j+1} to land and adds one
+        // arrival to p_ready(t) of each query tile t that visits key tile j, so
+        // the MMA thread waits once per product pair.  An arrival for phase g
+        // must not land before phase g - 1 completes, hence the wait on the
+        // previous phase (the softmax arrivals already come in phase order).
+        if (lane == 0) {
+            auto wait_use = [&](int use) {
+                return wait_or_abort(bars.full(use % C::kSlots), (use / C::kSlots) & 1,
+                                     abort_flag);
+            };
+            int u = 0;             // ring use of the current K tile
+            int iter[2] = {0, 0};  // p_ready phases per query tile, over all items
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int idx = item_index(k, n_items);
+                if (idx < 0) break;
+                const Item it = item_at<kRagged>(p, idx);
+                if (it.empty) continue;
+                const int nmax = it.n_kv_max();
+                for (int j = 0; j < nmax && ok; ++j) {
+                    ok = wait_use(u + 1) && (j + 1 >= nmax || wait_use(u + 2));  // V_j, K_{j+1}
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (j >= it.n_kv(t)) continue;
+                        if (iter[t] > 0 &&
+                            !(ok = wait_or_abort(bars.p_ready(t), (iter[t] - 1) & 1, abort_flag)))
+                            break;
+                        mbar_arrive(bars.p_ready(t));
+                        ++iter[t];
+                    }
+                    u += 2;
+                }
+            }
+        }
+        __syncwarp();
+    }  // warp 11 has no role
     } else {
         // ================================================= softmax warpgroups
         setmaxnreg_inc<kSoftmaxRegs>();
@@ -604,10 +639,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              pk[4 * v4 + 3]);
                 }
             }
-            // O_t has been read: the next item's first P V product may overwrite it
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bars.o_free(t));
+            // O_t has been read (each load above was waited for): the MMA thread
+            // learns it from this warp's next p_ready arrival, which follows
             if (row < it.nq)
                 p.lse[static_cast<size_t>(it.bh) * p.Nq + row] =
                     (m_ref + log2f(l)) * 0.69314718055994530942f;
