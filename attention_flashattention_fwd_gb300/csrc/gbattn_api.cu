@@ -99,6 +99,22 @@ int encode_bhnd(CUtensorMap* m, const void* base, long long BH, int N, int d) {
     return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// O [BH, Nq, d] bf16 as a 3-D tensor {d, Nq, BH} in boxes of 32 x 32 x 1 with
+// the 64-byte swizzle: the target of the prefill epilogue's TMA stores (a warp
+// stores 32 rows x 32 columns at a time; rows past Nq are clipped).
+int encode_o_store(CUtensorMap* m, void* base, long long BH, int N, int d) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                             static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 // The fp32 dQ accumulator [BH, Nq_pad, d] of the backward as a 3-D tensor
 // {d, Nq_pad, BH} in boxes of 32 x 128 x 1 with the 128-byte swizzle (the
 // target of the backward's TMA reduce-adds).
@@ -124,10 +140,11 @@ int enqueue_fwd(const void* q, const void* k, const void* v, void* o, float* lse
     int num_sms = 0;
     if ((st = current_sm_count(&num_sms)) != ATTN_OK) return st;
     const long long BH = static_cast<long long>(B) * H;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if ((st = encode_bhnd(&tq, q, BH, Nq, d)) != ATTN_OK) return st;
     if ((st = encode_bhnd(&tk, k, BH, Nk, d)) != ATTN_OK) return st;
     if ((st = encode_bhnd(&tv, v, BH, Nk, d)) != ATTN_OK) return st;
+    if ((st = encode_o_store(&to, o, BH, Nq, d)) != ATTN_OK) return st;
     PrefillParams p;
     p.o = static_cast<__nv_bfloat16*>(o);
     p.lse = lse;
@@ -141,7 +158,7 @@ int enqueue_fwd(const void* q, const void* k, const void* v, void* o, float* lse
     p.seqlens_q = seqlens_q;
     p.seqlens_k = seqlens_k;
     p.o_scale = 1.f;
-    return launch_prefill(d, tq, tk, tv, p, num_sms, stream);
+    return launch_prefill(d, tq, tk, tv, to, p, num_sms, stream);
 }
 
 // A 3-D byte tensor {x, y, BH} (x innermost, x bytes per row, y rows per
@@ -333,10 +350,11 @@ int attn_fwd_fp8(const void* q, const void* k, const void* vt, void* o, float* l
     int num_sms = 0;
     if ((st = current_sm_count(&num_sms)) != ATTN_OK) return st;
     const long long BH = static_cast<long long>(B) * H;
-    CUtensorMap tq, tk, tvt;
+    CUtensorMap tq, tk, tvt, to;
     if ((st = encode_u8(&tq, q, BH, d, Nq)) != ATTN_OK) return st;
     if ((st = encode_u8(&tk, k, BH, d, Nk)) != ATTN_OK) return st;
     if ((st = encode_u8(&tvt, vt, BH, Nk, d)) != ATTN_OK) return st;
+    if ((st = encode_o_store(&to, o, BH, Nq, d)) != ATTN_OK) return st;
     PrefillParams p;
     p.o = static_cast<__nv_bfloat16*>(o);
     p.lse = lse;
@@ -350,7 +368,7 @@ int attn_fwd_fp8(const void* q, const void* k, const void* vt, void* o, float* l
     p.seqlens_q = nullptr;
     p.seqlens_k = nullptr;
     p.o_scale = descale_v;
-    return launch_prefill_fp8(tq, tk, tvt, p, num_sms, static_cast<cudaStream_t>(stream));
+    return launch_prefill_fp8(tq, tk, tvt, to, p, num_sms, static_cast<cudaStream_t>(stream));
 }
 
 int attn_fwd_ragged(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -79,11 +79,15 @@ struct MergeParams {
 // prefill_sm103.cu
 int prefill_set_attributes();
 // Persistent launch: min(work items, num_sms) CTAs, one per SM.
+// `to` maps O [BH, Nq, d] in boxes of 32 x 32 x 1 with the 64-byte swizzle (the
+// target of the epilogue's TMA stores; unused with per-sequence lengths).
 int launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                   const PrefillParams& p, int num_sms, cudaStream_t stream);
+                   const CUtensorMap& to, const PrefillParams& p, int num_sms,
+                   cudaStream_t stream);
 // E4M3 operands, d = 128; tvt maps the transposed values [BH, d, Nk].
 int launch_prefill_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
-                       const PrefillParams& p, int num_sms, cudaStream_t stream);
+                       const CUtensorMap& to, const PrefillParams& p, int num_sms,
+                       cudaStream_t stream);
 int prefill_smem_bytes(int d);
 unsigned read_and_clear_prefill_error();
 // Device error bits (shared by the kernels' error words)

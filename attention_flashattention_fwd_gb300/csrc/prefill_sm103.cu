@@ -68,6 +68,7 @@ constexpr int kRelayWarp = 10;
 constexpr uint32_t kSoftmaxRegs = 192;
 constexpr uint32_t kControlRegs = 112;
 constexpr uint32_t kTmemCols = 512;
+constexpr int kStageBufBytes = 32 * 64;  // one O staging buffer: 32 rows x 64 bytes
 // A key tile whose row sum against the stale reference max exceeds this moves
 // the reference.  bf16 P: 2^62, far from fp32 overflow for O and l.  E4M3 P:
 // 448, the largest finite E4M3 value; a row sum within it bounds every p of
@@ -86,7 +87,11 @@ struct Cfg {
     static constexpr int kKSteps = D * kElem / 32;       // MMA k-steps of S = Q K^T (32 B each)
     static constexpr int kQOff = 0;
     static constexpr int kRingOff = 2 * kTileBytes;
-    static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
+    // O staging of the epilogue: per softmax warp two buffers of 32 rows x 32 bf16
+    // (64-byte swizzle), the source of the TMA stores of O
+    static constexpr int kStageOff = kRingOff + kSlots * kTileBytes;
+    static constexpr int kStageBytes = 8 * 2 * kStageBufBytes;
+    static constexpr int kBarOff = kStageOff + kStageBytes;
     // barriers: full[kSlots], empty[kSlots], then per query tile q_full, q_empty,
     // s_full, p_ready, pv_done, then fin
     static constexpr int kNumBars = 2 * kSlots + 10 + 1;
@@ -172,6 +177,38 @@ __device__ __forceinline__ void flag_abort(volatile int* abort_flag) {
 }
 
 // Bounded wait that also gives up as soon as another role has aborted.
+// TMA store of a box of O from shared memory, tracked by this thread's bulk
+// async-group; coordinates in elements, innermost first.
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+            tmap),
+        "r"(x), "r"(y), "r"(z), "r"(src)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// All but the newest N of this thread's committed bulk groups have read their source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// This thread's committed bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+// Shared-memory writes of this thread become visible to the async proxy (TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
                                               volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -197,7 +234,8 @@ template <int D, bool kRagged, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                             const __grid_constant__ CUtensorMap tm_k,
-                            const __grid_constant__ CUtensorMap tm_v, PrefillParams p) {
+                            const __grid_constant__ CUtensorMap tm_v,
+                            const __grid_constant__ CUtensorMap tm_o, PrefillParams p) {
     static_assert(!kFp8 || (D == 128 && !kRagged), "E4M3 operands: d = 128, no sequence lengths");
     using C = Cfg<D, kFp8>;
     extern __shared__ uint8_t smem_raw[];
@@ -207,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sbase = smem_addr(smem);
     const uint32_t sQ = sbase + C::kQOff;
     const uint32_t sRing = sbase + C::kRingOff;
+    const uint32_t sStage = sbase + C::kStageOff;
     Bars bars;
     bars.full0 = sbase + C::kBarOff;
     bars.empty0 = bars.full0 + 8 * C::kSlots;
@@ -620,23 +659,67 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(bars.empty((2 * iter - 1) % C::kSlots));
             float inv_l = l > 0.f ? 1.f / l : 0.f;
             if constexpr (kFp8) inv_l *= p.o_scale;
-            __nv_bfloat16* orow = p.o + (static_cast<size_t>(it.bh) * p.Nq + row) * D;
+            if constexpr (kRagged) {
+                // rows past the sequence's length must stay untouched: direct stores
+                __nv_bfloat16* orow = p.o + (static_cast<size_t>(it.bh) * p.Nq + row) * D;
 #pragma unroll
-            for (int ch = 0; ch < D / 32; ++ch) {
-                uint32_t o[32];
-                tmem_ld32(tO + ch * 32, o);
-                tmem_wait_ld();
-                if (row < it.nq) {
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + ch * 32, o);
+                    tmem_wait_ld();
+                    if (row < it.nq) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int c = 0; c < 16; ++c)
+                            pk[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l,
+                                                __uint_as_float(o[2 * c + 1]) * inv_l);
+                        uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
+                                                 pk[4 * v4 + 3]);
+                    }
+                }
+            } else {
+                // A thread holds one row of O, so direct stores would write 32 rows
+                // 2 d bytes apart per instruction.  Instead each warp stages 32 rows
+                // x 32 columns in shared memory (64-byte swizzle: the 16-byte granule
+                // q of row i sits at granule q ^ ((i >> 1) & 3), so 8 neighbouring
+                // rows hit distinct banks) and one lane stores the box with TMA, two
+                // buffers per warp so the next chunk is written while one drains.
+                // The store clips rows past Nq.
+                const int wrow0 = it.row0 + t * kBM + wq * 32;
+                const bool store = wrow0 < it.nq;
+                if (lane == 0) bulk_wait_read<0>();  // the previous item's stores have read
+                __syncwarp();
+#pragma unroll
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + ch * 32, o);
+                    tmem_wait_ld();
                     uint32_t pk[16];
 #pragma unroll
                     for (int c = 0; c < 16; ++c)
                         pk[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l,
                                             __uint_as_float(o[2 * c + 1]) * inv_l);
-                    uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+                    const uint32_t buf =
+                        sStage + static_cast<uint32_t>((warp * 2 + (ch & 1)) * kStageBufBytes);
+                    if (ch >= 2) {  // buffer ch & 1 was last the source of chunk ch - 2
+                        if (lane == 0) bulk_wait_read<1>();
+                        __syncwarp();
+                    }
+                    const uint32_t rbase = buf + static_cast<uint32_t>(lane * 64);
+                    const int sw = (lane >> 1) & 3;
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4)
-                        dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
-                                             pk[4 * v4 + 3]);
+                    for (int q = 0; q < 4; ++q)
+                        st_shared_v4(rbase + static_cast<uint32_t>(((q ^ sw) * 16)), pk[4 * q],
+                                     pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && store) {
+                        tma_store_3d(&tm_o, buf, ch * 32, wrow0, it.bh);
+                        bulk_commit();
+                    }
                 }
             }
             // O_t has been read (each load above was waited for): the MMA thread
@@ -646,6 +729,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     (m_ref + log2f(l)) * 0.69314718055994530942f;
             ++kp;
         }
+        // the TMA stores of O have completed before the CTA (and its shared memory) ends
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     // ---- teardown: all Tensor Memory traffic is complete; free the columns
@@ -673,32 +759,35 @@ int prefill_set_attributes() {
 
 template <int D>
 static int launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const PrefillParams& p, int num_sms, cudaStream_t stream) {
+                            const CUtensorMap& to, const PrefillParams& p, int num_sms,
+                            cudaStream_t stream) {
     using C = Cfg<D, false>;
     const long long items = static_cast<long long>(p.num_pairs) * p.BH;
     const long long grid = items < num_sms ? items : num_sms;  // one persistent CTA per SM
     if (p.seqlens_q || p.seqlens_k)
         attn_fwd_prefill_kernel<D, true, false>
-            <<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
+            <<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, p);
     else
         attn_fwd_prefill_kernel<D, false, false>
-            <<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
+            <<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 int launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                   const PrefillParams& p, int num_sms, cudaStream_t stream) {
-    return d == 128 ? launch_prefill_d<128>(tq, tk, tv, p, num_sms, stream)
-                    : launch_prefill_d<64>(tq, tk, tv, p, num_sms, stream);
+                   const CUtensorMap& to, const PrefillParams& p, int num_sms,
+                   cudaStream_t stream) {
+    return d == 128 ? launch_prefill_d<128>(tq, tk, tv, to, p, num_sms, stream)
+                    : launch_prefill_d<64>(tq, tk, tv, to, p, num_sms, stream);
 }
 
 int launch_prefill_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
-                       const PrefillParams& p, int num_sms, cudaStream_t stream) {
+                       const CUtensorMap& to, const PrefillParams& p, int num_sms,
+                       cudaStream_t stream) {
     using C = Cfg<128, true>;
     const long long items = static_cast<long long>(p.num_pairs) * p.BH;
     const long long grid = items < num_sms ? items : num_sms;
     attn_fwd_prefill_kernel<128, false, true>
-        <<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tq, tk, tvt, p);
+        <<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tq, tk, tvt, to, p);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
