@@ -6,8 +6,9 @@ input: the prefill kernel on the causal B=2, H=16, N=4096, d=128 workload
 (the headline: attention fwd TFLOP/s against the bf16 tensor peak), the
 prefill kernel on the causal B=1, H=32, N=16384, d=128 long-sequence workload,
 and the split-K decode (split kernel + combine kernel) on the
-B=64, H=32, Nk=8192, d=128 decode workload (HBM GB/s).  L2 is flushed (256 MiB
-write) before every step.  Each kernel is timed with CUDA events on the
+B=64, H=32, Nk=8192, d=128 decode workload (HBM GB/s).  L2 is flushed before
+every step: a 256 MiB write, then a 256 MiB read of another buffer, so no dirty
+line of the flush is left for the timed kernels to write back.  Each kernel is timed with CUDA events on the
 stream it is launched on.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
@@ -392,10 +393,20 @@ def run_gpu(args):
     splits = binding.decode_workspace_bytes(w5.B, w5.H, w5.Nk, w5.d) > 0
     launches_per_step = 1 + 1 + (2 if splits else 1)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=dev)
+
+    def flush_l2():
+        # write a buffer larger than L2, then read another one: the write evicts
+        # every line the previous work left, and the read evicts the written
+        # buffer's dirty lines, so the next timed kernel neither hits in L2 nor
+        # pays for writing back lines it did not produce
+        flush.zero_()
+        flush_rd.max()
+
     stream = torch.cuda.current_stream()
 
     def step(ev):
-        flush.zero_()
+        flush_l2()
         # keep the GPU busy while the host enqueues this step's launches, so the
         # events below time the kernels and not host-side launch latency
         torch.cuda._sleep(LAUNCH_COVER_CYCLES)
@@ -513,7 +524,7 @@ def run_gpu(args):
     bwd_reps = min(K, 20)
     bwd_ms = 0.0
     for _ in range(bwd_reps):
-        flush.zero_()
+        flush_l2()
         torch.cuda._sleep(LAUNCH_COVER_CYCLES)
         b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         b0.record(stream)
@@ -547,7 +558,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     n_ms = 0.0
     for _ in range(bwd_reps):
-        flush.zero_()
+        flush_l2()
         torch.cuda._sleep(LAUNCH_COVER_CYCLES)
         b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         b0.record(stream)
@@ -575,7 +586,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     f_ms = 0.0
     for _ in range(bwd_reps):
-        flush.zero_()
+        flush_l2()
         torch.cuda._sleep(LAUNCH_COVER_CYCLES)
         b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         b0.record(stream)
@@ -611,7 +622,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     m_ms = 0.0
     for _ in range(bwd_reps):
-        flush.zero_()
+        flush_l2()
         torch.cuda._sleep(LAUNCH_COVER_CYCLES)
         b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         b0.record(stream)
@@ -640,7 +651,7 @@ def run_gpu(args):
         "config": {"workload": HEADLINE, "B": w3.B, "H": w3.H, "Nq": w3.Nq, "Nk": w3.Nk,
                    "d": w3.d, "causal": True, "scale": w3.scale,
                    "step": f"prefill {HEADLINE} + prefill {LONG} + decode {DECODE}",
-                   "l2": "flushed before every step (256 MiB write)",
+                   "l2": "flushed before every step (256 MiB write, then a 256 MiB read so no dirty line remains)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": p3["roofline"],
         "parts": {HEADLINE: p3, LONG: p4, DECODE: p5},

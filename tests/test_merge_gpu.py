@@ -29,6 +29,8 @@ def _check(o, lse, ro, rl, what):
     (2, 3, 1, (700, 1000, 300, 48), 128),     # decode-shaped shards
     (1, 4, 256, (512, 512), 64),
     (1, 1, 77, (5,), 64),                     # one part: the identity
+    (1, 2, 190, (200, 100, 300, 50, 129, 77), 128),  # more than 4 parts: batched online form
+    (2, 1, 64, (64, 64, 64, 64, 64), 64),
 ])
 def test_sharded_attention_merges_to_full(B, H, Nq, split, d):
     Nk = sum(split)
@@ -56,7 +58,14 @@ def test_empty_parts_have_no_weight():
     torch.cuda.synchronize()
     assert torch.equal(lse, l1)
     assert (o.float() - o1.float()).abs().max().item() <= 2 ** -8 * o1.float().abs().max().item()
-    # every part empty: o = 0, lse = -inf
-    o, lse = binding.attn_merge(torch.stack([junk, junk]), torch.stack([ninf, ninf]))
+    # more than 4 parts (the batched form): empty parts before and after the live one
+    o, lse = binding.attn_merge(torch.stack([junk, junk, junk, junk, o1, junk]),
+                                torch.stack([ninf, ninf, ninf, ninf, l1, ninf]))
     torch.cuda.synchronize()
-    assert (o.float() == 0).all() and torch.isinf(lse).all() and (lse < 0).all()
+    assert torch.equal(lse, l1)
+    assert (o.float() - o1.float()).abs().max().item() <= 2 ** -8 * o1.float().abs().max().item()
+    # every part empty: o = 0, lse = -inf (both forms)
+    for n in (2, 5):
+        o, lse = binding.attn_merge(torch.stack([junk] * n), torch.stack([ninf] * n))
+        torch.cuda.synchronize()
+        assert (o.float() == 0).all() and torch.isinf(lse).all() and (lse < 0).all()
