@@ -24,6 +24,11 @@ struct PrefillParams {
     const int* seqlens_q;  // [B] per-sequence query counts, or null (all Nq)
     const int* seqlens_k;  // [B] per-sequence key counts, or null (all Nk)
     float o_scale;         // FP8 operands: the value descale applied to O / l
+    // Set by the launcher: the number of work items, and the first of them that
+    // is a single 128-row query tile (items split_start + 2 i and + 2 i + 1 are
+    // the two halves of query-tile pair split_start + i; no split when
+    // split_start == n_items).
+    int n_items, split_start;
 };
 
 // Arguments of the split-K decode kernels.

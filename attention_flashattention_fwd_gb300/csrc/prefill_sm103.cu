@@ -116,9 +116,11 @@ struct Bars {
     __device__ uint32_t pv_done(int t) const { return tile0 + 8u * (5 * t + 4); }
 };
 
-// Geometry of work item `idx` (0 <= idx < num_pairs * BH).  With per-sequence
-// lengths, nq / nk are sequence b's; an item whose rows all lie past nq is
-// empty and every role skips it.
+// Geometry of work item `idx` (0 <= idx < n_items).  Items below split_start
+// are pairs of query tiles; the ones from split_start on are single query
+// tiles, the two halves of the pairs left for the last wave (tile slot 0 only,
+// n_kv1 = 0).  With per-sequence lengths, nq / nk are sequence b's; an item
+// whose rows all lie past nq is empty and every role skips it.
 struct Item {
     int bh, row0, n_kv0, n_kv1;
     int nq, nk, off;  // query and key count of the sequence; causal offset nk - nq
@@ -130,15 +132,20 @@ struct Item {
 template <bool kRagged>
 __device__ __forceinline__ Item item_at(const PrefillParams& p, int idx) {
     Item it;
+    int pidx = idx, half = -1;  // half >= 0: a single query tile of pair pidx
+    if (idx >= p.split_start) {
+        pidx = p.split_start + (idx - p.split_start) / 2;
+        half = (idx - p.split_start) & 1;
+    }
     int pair;
     if (p.causal) {  // heaviest pairs (most key tiles) first
-        pair = p.num_pairs - 1 - idx / p.BH;
-        it.bh = idx % p.BH;
+        pair = p.num_pairs - 1 - pidx / p.BH;
+        it.bh = pidx % p.BH;
     } else {  // a head's pairs are consecutive: its K/V stay in L2
-        pair = idx % p.num_pairs;
-        it.bh = idx / p.num_pairs;
+        pair = pidx % p.num_pairs;
+        it.bh = pidx / p.num_pairs;
     }
-    it.row0 = pair * 2 * kBM;
+    it.row0 = pair * 2 * kBM + (half > 0 ? kBM : 0);
     it.nq = p.Nq;
     it.nk = p.Nk;
     if constexpr (kRagged) {
@@ -159,7 +166,7 @@ __device__ __forceinline__ Item item_at(const PrefillParams& p, int idx) {
     // every tile tile 0 does, and at most one more
     const int last0 = it.row0 + kBM - 1 + it.off;
     it.n_kv0 = p.causal ? min(n_kv_all, last0 / kBN + 1) : n_kv_all;
-    it.n_kv1 = p.causal ? min(n_kv_all, (last0 + kBM) / kBN + 1) : n_kv_all;
+    it.n_kv1 = half >= 0 ? 0 : p.causal ? min(n_kv_all, (last0 + kBM) / kBN + 1) : n_kv_all;
     return it;
 }
 
@@ -256,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int n_items = p.num_pairs * p.BH;
+    const int n_items = p.n_items;
 
     // ---- set-up: barriers (one thread), Tensor Memory (warp 0)
     if (threadIdx.x == kLoadWarp * 32) {
@@ -293,8 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_v);
             int issued = 0;  // ring uses (K or V tiles) issued so far
             bool ok = true;
-            auto load_q = [&](int kp, int t, const Item& it) {
+            int kq[2] = {0, 0};  // items in which query tile slot t took part
+            auto load_q = [&](int t, const Item& it) {
                 // the previous item's last Q_t K^T product has finished
+                const int kp = kq[t]++;
                 if (kp > 0 && !(ok = wait_or_abort(bars.q_empty(t), (kp - 1) & 1, abort_flag)))
                     return;
                 mbar_arrive_expect_tx(bars.q_full(t), C::kTileBytes);
@@ -321,22 +330,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ++issued;
             };
-            int kp = 0;  // items processed (empty items are skipped by every role)
-            for (int k = 0; ok; ++k) {
+            for (int k = 0; ok; ++k) {  // empty items are skipped by every role
                 const int idx = item_index(k, n_items);
                 if (idx < 0) break;
                 const Item it = item_at<kRagged>(p, idx);
                 if (it.empty) continue;
                 // in the order the MMA warp needs them: Q_0, K_0, Q_1, V_0, K_1, V_1, ...
-                load_q(kp, 0, it);
+                load_q(0, it);
                 if (ok) load_kv(0, 0, it);
-                if (ok) load_q(kp, 1, it);
+                if (ok && it.n_kv1 > 0) load_q(1, it);
                 if (ok) load_kv(1, 0, it);
                 // warm L2 with the next item's query tiles (read once, from DRAM)
                 const int nidx = item_index(k + 1, n_items);
                 if (ok && nidx >= 0) {
                     const Item nx = item_at<kRagged>(p, nidx);
-                    for (int t = 0; t < 2; ++t)
+                    for (int t = 0; t < (nx.n_kv1 > 0 ? 2 : 1); ++t)
                         for (int s = 0; s < C::kSub; ++s)
                             tma_prefetch_l2_3d(&tm_q, s * C::kSubElems, nx.row0 + t * kBM, nx.bh);
                 }
@@ -344,7 +352,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     load_kv(0, j, it);
                     if (ok) load_kv(1, j, it);
                 }
-                ++kp;
             }
             if (!ok) {
                 // drain: every slot's most recent copy must land before exit
@@ -421,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             bool ok = true;
-            int kp = 0;  // items processed
+            int kq[2] = {0, 0};  // items in which query tile slot t took part
             for (int k = 0; ok; ++k) {
                 const int idx = item_index(k, n_items);
                 if (idx < 0) break;
@@ -429,11 +436,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (it.empty) continue;
                 const int nmax = it.n_kv_max();
                 // prologue of the item: S_0(0) once Q_0 and K_0 are in, then S_1(0)
+                // (a single-tile item has no tile 1)
                 for (int t = 0; t < 2 && ok; ++t) {
-                    ok = wait_or_abort(bars.q_full(t), kp & 1, abort_flag) && (t == 1 || wait_use(u));
+                    if (it.n_kv(t) == 0) continue;
+                    ok = wait_or_abort(bars.q_full(t), kq[t]++ & 1, abort_flag) &&
+                         (t == 1 || wait_use(u));
                     if (!ok) break;
                     tc_fence_after();
-                    issue_s(t, u);  // n_kv0, n_kv1 >= 1
+                    issue_s(t, u);  // n_kv0 >= 1
                     if (it.n_kv(t) == 1) umma_commit(bars.q_empty(t));
                 }
                 if (!ok) break;
@@ -459,7 +469,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     u += 2;
                 }
-                ++kp;
             }
             // every MMA this thread issued has completed once `fin` flips
             umma_commit(bars.fin);
@@ -517,7 +526,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem + lane_off + C::col_o(t);
         const float cl2 = p.scale_log2;
         int iter = 0;  // key tiles processed by this tile over all items
-        int kp = 0;    // items processed
+        int kp = 0;    // items in which this tile took part
+        int ring = 0;  // ring use of the current item's K_0 (2 per key tile of an item)
         bool ok = true;
         for (int k = 0; ok; ++k) {
             const int idx = item_index(k, n_items);
@@ -526,6 +536,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (it.empty) continue;
             const int row = it.row0 + t * kBM + r;
             const int nkv = it.n_kv(t);
+            const int item_ring = ring;
+            ring += 2 * it.n_kv_max();
+            if (nkv == 0) continue;  // tile slot 1 of a single-tile item
+            // the tile that visits every key tile of the item returns the ring
+            // slots: tile 1, or tile 0 of a single-tile item
+            const bool releaser = (it.n_kv1 > 0 ? t == 1 : t == 0) && wq == 0 && lane == 0;
             float m_ref = -INFINITY;  // running reference max, log2 units
             float l = 0.f;
             for (int j = 0; j < nkv; ++j, ++iter) {
@@ -534,13 +550,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
                 // S_t(j) was issued after every earlier product of this CTA, so its
-                // completion means K_j (last read by S_1(j)) and V_{j-1} (last read
-                // by P_1(j-1) V_{j-1}) are free: tile 1, which visits every key
-                // tile of an item, hands their ring slots back to the producer.
-                // K_j and V_j are ring uses 2 iter and 2 iter + 1.
-                if (t == 1 && wq == 0 && lane == 0) {
-                    mbar_arrive(bars.empty((2 * iter) % C::kSlots));
-                    if (j > 0) mbar_arrive(bars.empty((2 * iter - 1) % C::kSlots));
+                // completion means K_j (last read by S_t(j)) and V_{j-1} (last read
+                // by P_t(j-1) V_{j-1}) are free: the releasing tile hands their ring
+                // slots back to the producer.  K_j and V_j are ring uses
+                // item_ring + 2 j and + 2 j + 1.
+                if (releaser) {
+                    mbar_arrive(bars.empty((item_ring + 2 * j) % C::kSlots));
+                    if (j > 0) mbar_arrive(bars.empty((item_ring + 2 * j - 1) % C::kSlots));
                 }
                 // S row: four 32-column loads in flight, one wait
                 uint32_t sr[kBN];
@@ -655,8 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             // the item's last V tile is free once its last P V product is done
-            if (t == 1 && wq == 0 && lane == 0)
-                mbar_arrive(bars.empty((2 * iter - 1) % C::kSlots));
+            if (releaser) mbar_arrive(bars.empty((item_ring + 2 * nkv - 1) % C::kSlots));
             float inv_l = l > 0.f ? 1.f / l : 0.f;
             if constexpr (kFp8) inv_l *= p.o_scale;
             if constexpr (kRagged) {
@@ -757,13 +772,34 @@ int prefill_set_attributes() {
     return ATTN_OK;
 }
 
+// The persistent grid (one CTA per SM, at most one per pair) and the work
+// items.  Without a causal mask or per-sequence lengths every pair costs the
+// same, so pairs that would leave the last wave part-full run as two
+// single-tile items instead, when those fit in one wave: e.g. 512 pairs on 152
+// SMs take 3 waves of pairs and one of 112 single tiles instead of 4 waves.
+static long long plan_items(PrefillParams& p, int num_sms) {
+    const long long pairs = static_cast<long long>(p.num_pairs) * p.BH;
+    const long long grid = pairs < num_sms ? pairs : num_sms;
+    long long items = pairs, split = pairs;
+    if (!p.causal && !p.seqlens_q && !p.seqlens_k && pairs > grid) {
+        const long long full = pairs / grid * grid, tail = pairs - full;
+        if (tail > 0 && 2 * tail <= grid && full + 2 * tail <= 0x7fffffffLL) {
+            split = full;
+            items = full + 2 * tail;
+        }
+    }
+    p.n_items = static_cast<int>(items);
+    p.split_start = static_cast<int>(split);
+    return grid;
+}
+
 template <int D>
 static int launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& to, const PrefillParams& p, int num_sms,
+                            const CUtensorMap& to, const PrefillParams& params, int num_sms,
                             cudaStream_t stream) {
     using C = Cfg<D, false>;
-    const long long items = static_cast<long long>(p.num_pairs) * p.BH;
-    const long long grid = items < num_sms ? items : num_sms;  // one persistent CTA per SM
+    PrefillParams p = params;
+    const long long grid = plan_items(p, num_sms);
     if (p.seqlens_q || p.seqlens_k)
         attn_fwd_prefill_kernel<D, true, false>
             <<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, p);
@@ -781,11 +817,11 @@ int launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CU
 }
 
 int launch_prefill_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
-                       const CUtensorMap& to, const PrefillParams& p, int num_sms,
+                       const CUtensorMap& to, const PrefillParams& params, int num_sms,
                        cudaStream_t stream) {
     using C = Cfg<128, true>;
-    const long long items = static_cast<long long>(p.num_pairs) * p.BH;
-    const long long grid = items < num_sms ? items : num_sms;
+    PrefillParams p = params;
+    const long long grid = plan_items(p, num_sms);
     attn_fwd_prefill_kernel<128, false, true>
         <<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tq, tk, tvt, to, p);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;

@@ -81,6 +81,17 @@ def test_prefill_matches_oracle(B, H, Nq, Nk, d, causal):
     _full_check(q, k, v, causal, what=f"{(B, H, Nq, Nk, d, causal)}")
 
 
+# Non-causal work whose query-tile pairs would leave the last wave of the
+# persistent grid part-full runs that tail as single 128-row tiles.  On a
+# 152-SM GB300: 158 pairs -> 152 pairs + 12 single tiles (of which the last
+# head's upper halves, rows 384..511 of 300, are empty), and 154 pairs ->
+# 152 pairs + 4 single tiles.  Every row is checked.
+@pytest.mark.parametrize("B,H,N,d", [(1, 79, 300, 64), (1, 77, 512, 128)])
+def test_last_wave_single_tiles_match_oracle(B, H, N, d):
+    q, k, v = make_qkv(B, H, N, N, d, seed=23 + N + d, device=_dev())
+    _full_check(q, k, v, False, what=f"{(B, H, N, d)} split tail")
+
+
 def test_chunked_prefill_equals_prefill_at_once():
     """A 1000-token causal prefill run as three query chunks, each against the
     keys and values of every token up to its end (the KV cache so far), gives
