@@ -227,7 +227,7 @@ int enqueue_bwd(const void* q, const void* k, const void* v, const void* o, cons
 // Streams and events of the host-buffer path, created on first use per device
 // and kept until the process exits.  The mutex serialises the enqueue of
 // calls from several host threads (the events are shared).
-constexpr int kHostChunks = 4;
+constexpr int kHostChunks = 5;
 struct HostPipe {
     bool ready = false;
     cudaStream_t compute = nullptr, copy_out = nullptr;
@@ -397,6 +397,9 @@ int attn_fwd_from_host(const void* q, const void* k, const void* v, void* o, flo
     // copy-out stream once it has run -- so the inputs of chunk c + 1 cross
     // the host link while chunk c computes and chunk c - 1's results come back
     // the other way.  The caller's stream finally waits for the last copy out.
+    // Chunk sizes fall off in the ratio 5 : 4 : 3 : 2 : 1: the host link is
+    // the bottleneck and only the last chunk's kernel and copy out are left
+    // exposed after the inputs have crossed, so the last chunk is the smallest.
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     const long long BH = static_cast<long long>(B) * H;
     std::lock_guard<std::mutex> lock(g_pipe_mu);
@@ -411,9 +414,16 @@ int attn_fwd_from_host(const void* q, const void* k, const void* v, void* o, flo
     const size_t lh = static_cast<size_t>(Nq) * 4;
     auto at = [](const void* base, size_t off) { return static_cast<const char*>(base) + off; };
     auto atw = [](void* base, size_t off) { return static_cast<char*>(base) + off; };
-    long long h0 = 0;
+    // chunk c ends near head BH * W(c) / W(chunks), W(c) = the sum of the first
+    // c + 1 weights chunks, chunks - 1, ..., 1, clamped so that every chunk has
+    // at least one head
+    const long long wsum = static_cast<long long>(chunks) * (chunks + 1) / 2;
+    long long h0 = 0, wacc = 0;
     for (int c = 0; c < chunks; ++c) {
-        const long long h1 = BH * (c + 1) / chunks;
+        wacc += chunks - c;
+        long long h1 = BH * wacc / wsum;
+        if (h1 < h0 + 1) h1 = h0 + 1;
+        if (h1 > BH - (chunks - 1 - c)) h1 = BH - (chunks - 1 - c);
         const size_t n = static_cast<size_t>(h1 - h0);
         const size_t oq = static_cast<size_t>(h0) * qh, ok = static_cast<size_t>(h0) * kh;
         const size_t ol = static_cast<size_t>(h0) * lh;

@@ -148,9 +148,11 @@ int attn_fwd_decode(const void *q, const void *k, const void *v, void *o, float 
  *
  * Host->device copies of q, k, v into the caller's device buffers dq, dk,
  * dv; attn_fwd on them into do_, dlse; device->host copies of the results
- * into o and lse.  The (b, h) heads go in up to four chunks so that one
- * chunk's inputs cross the host link while the previous chunk computes and
- * the one before returns its results: the input copies run on `stream`, the
+ * into o and lse.  The (b, h) heads go in up to five chunks, each smaller
+ * than the one before, so that one chunk's inputs cross the host link while
+ * the previous chunk computes and the one before returns its results (the
+ * last, smallest chunk's kernel and output copy are all that remain after
+ * the inputs have crossed): the input copies run on `stream`, the
  * kernels and the output copies on two streams of the library's own
  * (created with a few events on the first call on each device, kept until
  * the process exits), and `stream` is made to wait for the last output copy.

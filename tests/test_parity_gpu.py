@@ -323,9 +323,10 @@ def test_deterministic_and_stream_aware():
 
 
 @pytest.mark.parametrize("B,H,N,d", [(1, 4, 512, 128), (1, 3, 300, 64), (1, 1, 200, 128),
+                                     (1, 5, 200, 64), (1, 7, 130, 128),
                                      (2, 5, 256, 128)])
 def test_from_host_end_to_end(B, H, N, d):
-    # the heads cross the host link in up to four chunks on three streams
+    # the heads cross the host link in up to five chunks (sizes falling off) on three streams
     q, k, v = make_qkv(B, H, N, N, d, seed=56 + H, device="cpu")
     qh, kh, vh = (t.pin_memory() for t in (q, k, v))
     oh = torch.empty((B, H, N, d), dtype=torch.bfloat16).pin_memory()
