@@ -87,6 +87,17 @@ PREFILL_SOURCES = ["prefill_sm103.cu", "sm103_ptx.cuh"]
 DECODE_SOURCES = ["decode_sm103.cu", "sm103_ptx.cuh"]
 BACKWARD_SOURCES = ["backward_sm103.cu", "sm103_ptx.cuh"]
 FP8_PEAK_RATIO = 2.0  # nominal dense fp8 : bf16 tensor rate (4.5 : 2.25 PFLOP/s)
+# ex2.approx.f32 per clock per SM on GB300 (measured: 4 cycles per warp instruction
+# per SM sub-partition); the SFU roofline of the softmax's exponentials
+SFU_EX2_PER_CLK_SM = 32.0
+
+
+def visible_pairs(w):
+    """(query, key) pairs a prefill workload scores: one exponential each."""
+    if not w.causal:
+        return w.B * w.H * w.Nq * w.Nk
+    off = w.Nk - w.Nq  # query i sees keys j <= i + off
+    return w.B * w.H * (w.Nq * (off + 1) + w.Nq * (w.Nq - 1) // 2)
 MERGE_PARTS = 4  # key shards merged by attn_merge in the context-parallel measurement
 MERGE_SOURCES = ["merge_sm103.cu", "sm103_ptx.cuh"]
 # FLOPs of the backward: five products of the forward's size (S and dP
@@ -455,10 +466,16 @@ def run_gpu(args):
     ms3, ms4, ms5, total_ms = max_over_ranks(ms + [total_ms], world, device=dev)
     K = args.steps
 
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sfu_mhz = clocks.get("sm_mhz") or clocks.get("sm_max_mhz") or 2070.0
+    sfu_peak = SFU_EX2_PER_CLK_SM * n_sms * sfu_mhz * 1e6 / 1e12  # Texp/s
+
     def prefill_part(w, ms_sum, sources, prof):
         per_launch = ms_sum / K
         tflops = world * K * w.flops() / (ms_sum * 1e-3) / 1e12
         achieved = w.flops() / (per_launch * 1e-3) / 1e12
+        exps = visible_pairs(w)
+        exp_rate = exps / (per_launch * 1e-3) / 1e12
         return {
             "workload": w.name, "value": tflops, "unit": "TFLOP/s", "ms_per_launch": per_launch,
             "frac_of_2250": achieved / 2250.0,
@@ -467,6 +484,11 @@ def run_gpu(args):
                          "frac": achieved / peaks["bf16_tflops"],
                          "traffic": profiled_traffic(prof, sources),
                          "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)"},
+            # secondary: the softmax's exponentials against the SFU rate
+            "sfu": {"exps_per_launch": exps, "achieved": exp_rate, "peak": sfu_peak,
+                    "unit": "Texp/s", "frac": exp_rate / sfu_peak,
+                    "peak_source": f"{SFU_EX2_PER_CLK_SM:g} ex2 per clock per SM (measured) x "
+                                   f"{n_sms} SMs x {sfu_mhz:g} MHz (median SM clock under load)"},
         }
 
     p3 = prefill_part(w3, ms3, PREFILL_SOURCES, "ncu_prefill_" + HEADLINE)
