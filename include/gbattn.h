@@ -21,8 +21,15 @@
  *   - Arguments are validated on the host before anything is launched; a
  *     rejected call launches nothing and touches no buffer.
  *   - Nothing is thrown across the ABI; every call returns a status code.
- *   - Thread safety: calls may be made from several host threads; the only
- *     shared host state is a once-initialised table of kernel attributes.
+ *   - Thread safety: calls may be made from several host threads.  The shared
+ *     host state is a once-initialised table of kernel attributes, a cached
+ *     SM count per device, and the streams and events attn_fwd_from_host
+ *     creates per device on first use (its enqueue is serialised by a mutex).
+ *   - CUDA graphs: after one call on a device (which creates that state),
+ *     every call can be captured in a CUDA graph and replayed.  Calls enqueue
+ *     only kernel launches; attn_fwd_from_host also enqueues copies (capture
+ *     needs pinned host buffers) and event waits that fork its own streams
+ *     from the caller's stream and join them back before it returns.
  */
 #ifndef GBATTN_H
 #define GBATTN_H
