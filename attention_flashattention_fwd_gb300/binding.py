@@ -10,6 +10,7 @@ raises.
 import ctypes
 import math
 import os
+import threading
 
 import torch
 
@@ -18,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libgbattn.so")
 
 ATTN_OK = 0
 _lib = None
+_lib_lock = threading.Lock()
 
 
 class GbattnError(RuntimeError):
@@ -27,45 +29,54 @@ class GbattnError(RuntimeError):
 
 
 def load():
-    """Load the CUDA library (raises if it is missing)."""
+    """Load the CUDA library (raises if it is missing).  Safe to call from
+    several threads: the first caller configures it under a lock."""
     global _lib
-    if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise ImportError(
-                f"{LIB_PATH} is not built; run `python -c \"import __graft_entry__ as g; "
-                f"g.build()\"` (or attention_flashattention_fwd_gb300/build_lib.py)")
-        lib = ctypes.CDLL(LIB_PATH)
-        P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
-        lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]
-        lib.attn_fwd.restype = I
-        lib.attn_fwd_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, F, F, F, P]
-        lib.attn_fwd_fp8.restype = I
-        lib.attn_fwd_decode_workspace_bytes.argtypes = [I, I, I, I]
-        lib.attn_fwd_decode_workspace_bytes.restype = S
-        lib.attn_fwd_decode.argtypes = [P, P, P, P, P, I, I, I, I, F, P, S, P]
-        lib.attn_fwd_decode.restype = I
-        lib.attn_fwd_from_host.argtypes = [P] * 10 + [I, I, I, I, I, I, F, P]
-        lib.attn_fwd_from_host.restype = I
-        lib.attn_bwd_workspace_bytes.argtypes = [I, I, I, I, I]
-        lib.attn_bwd_workspace_bytes.restype = S
-        lib.attn_bwd.argtypes = [P] * 9 + [I, I, I, I, I, I, F, P, S, P]
-        lib.attn_bwd.restype = I
-        lib.attn_fwd_ragged.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, P]
-        lib.attn_fwd_ragged.restype = I
-        lib.attn_fwd_decode_ragged.argtypes = [P, P, P, P, P, P, I, I, I, I, F, P, S, P]
-        lib.attn_fwd_decode_ragged.restype = I
-        lib.attn_merge.argtypes = [P, P, I, P, P, I, I, I, I, P]
-        lib.attn_merge.restype = I
-        lib.attn_status_string.argtypes = [I]
-        lib.attn_status_string.restype = ctypes.c_char_p
-        lib.attn_device_error.argtypes = []
-        lib.attn_device_error.restype = I
-        lib.attn_selftest_timeout.argtypes = [P]
-        lib.attn_selftest_timeout.restype = I
-        lib.attn_version.argtypes = []
-        lib.attn_version.restype = I
-        _lib = lib
+    if _lib is not None:
+        return _lib
+    with _lib_lock:
+        if _lib is None:
+            _lib = _configure()
     return _lib
+
+
+def _configure():
+    """dlopen the library and declare every entry point's argument types."""
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is not built; run `python -c \"import __graft_entry__ as g; "
+            f"g.build()\"` (or attention_flashattention_fwd_gb300/build_lib.py)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]
+    lib.attn_fwd.restype = I
+    lib.attn_fwd_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, F, F, F, P]
+    lib.attn_fwd_fp8.restype = I
+    lib.attn_fwd_decode_workspace_bytes.argtypes = [I, I, I, I]
+    lib.attn_fwd_decode_workspace_bytes.restype = S
+    lib.attn_fwd_decode.argtypes = [P, P, P, P, P, I, I, I, I, F, P, S, P]
+    lib.attn_fwd_decode.restype = I
+    lib.attn_fwd_from_host.argtypes = [P] * 10 + [I, I, I, I, I, I, F, P]
+    lib.attn_fwd_from_host.restype = I
+    lib.attn_bwd_workspace_bytes.argtypes = [I, I, I, I, I]
+    lib.attn_bwd_workspace_bytes.restype = S
+    lib.attn_bwd.argtypes = [P] * 9 + [I, I, I, I, I, I, F, P, S, P]
+    lib.attn_bwd.restype = I
+    lib.attn_fwd_ragged.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, P]
+    lib.attn_fwd_ragged.restype = I
+    lib.attn_fwd_decode_ragged.argtypes = [P, P, P, P, P, P, I, I, I, I, F, P, S, P]
+    lib.attn_fwd_decode_ragged.restype = I
+    lib.attn_merge.argtypes = [P, P, I, P, P, I, I, I, I, P]
+    lib.attn_merge.restype = I
+    lib.attn_status_string.argtypes = [I]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_device_error.argtypes = []
+    lib.attn_device_error.restype = I
+    lib.attn_selftest_timeout.argtypes = [P]
+    lib.attn_selftest_timeout.restype = I
+    lib.attn_version.argtypes = []
+    lib.attn_version.restype = I
+    return lib
 
 
 def status_string(status: int) -> str:
