@@ -38,31 +38,44 @@ int validate_fwd(const void* q, const void* k, const void* v, const void* o, con
     return ATTN_OK;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-int g_init_status = ATTN_OK;
-std::once_flag g_init_once;
+constexpr int kMaxDevices = 64;
 
-void init_once() {
+// The driver's tensor-map encoder: looked up once per process.
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+int g_encode_status = ATTN_OK;
+std::once_flag g_encode_once;
+
+void init_encode() {
     cudaDriverEntryPointQueryResult qres;
     void* fn = nullptr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
                                          &qres) != cudaSuccess ||
         qres != cudaDriverEntryPointSuccess || fn == nullptr) {
-        g_init_status = ATTN_ERR_CUDA;
+        g_encode_status = ATTN_ERR_CUDA;
         return;
     }
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    g_init_status = prefill_set_attributes();
-    if (g_init_status == ATTN_OK) g_init_status = bwd_set_attributes();
 }
 
+// Kernel attributes (the large dynamic shared memory opt-in) belong to the
+// device context they are set in, so they are set once per device.
+std::once_flag g_attr_once[kMaxDevices];
+int g_attr_status[kMaxDevices];
+
 int ensure_init() {
-    std::call_once(g_init_once, init_once);
-    return g_init_status;
+    std::call_once(g_encode_once, init_encode);
+    if (g_encode_status != ATTN_OK) return g_encode_status;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+    std::call_once(g_attr_once[dev], [dev] {
+        int st = prefill_set_attributes();
+        if (st == ATTN_OK) st = bwd_set_attributes();
+        g_attr_status[dev] = st;
+    });
+    return g_attr_status[dev];
 }
 
 // Streaming multiprocessors of the current device (cached per device).
-constexpr int kMaxDevices = 64;
 std::atomic<int> g_num_sms[kMaxDevices];
 
 int current_sm_count(int* out) {

@@ -21,10 +21,12 @@
  *   - Arguments are validated on the host before anything is launched; a
  *     rejected call launches nothing and touches no buffer.
  *   - Nothing is thrown across the ABI; every call returns a status code.
- *   - Thread safety: calls may be made from several host threads.  The shared
- *     host state is a once-initialised table of kernel attributes, a cached
- *     SM count per device, and the streams and events attn_fwd_from_host
- *     creates per device on first use (its enqueue is serialised by a mutex).
+ *   - Thread safety: calls may be made from several host threads, and on
+ *     several devices (each call runs on the current device).  The shared host
+ *     state is the driver's tensor-map encoder (looked up once), kernel
+ *     attributes and an SM count set once per device, and the streams and
+ *     events attn_fwd_from_host creates per device on first use (its enqueue
+ *     is serialised by a mutex).
  *   - CUDA graphs: after one call on a device (which creates that state),
  *     every call can be captured in a CUDA graph and replayed.  Calls enqueue
  *     only kernel launches; attn_fwd_from_host also enqueues copies (capture
