@@ -97,6 +97,38 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _out(t, shape, dtype, device, name):
+    """An output buffer: a new one, or the caller's after checking that it is
+    what the kernels will write (``shape`` elements of ``dtype`` at its
+    address, on the inputs' device), since a mismatch would be written past."""
+    shape = tuple(shape)
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    if (t.device != device or t.dtype != dtype or tuple(t.shape) != shape
+            or not t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {shape} "
+                         f"on {device}")
+    return t
+
+
+def _workspace(t, need, device):
+    """A device workspace of at least ``need`` bytes (its size is checked by
+    the C entry point): a new one, or the caller's on the right device."""
+    if t is None:
+        return torch.empty(need, dtype=torch.uint8, device=device) if need > 0 else None
+    if t.device != device or not t.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous tensor on {device}")
+    return t
+
+
+def _on(device, stream):
+    """The C entry points run on the current device: make the tensors' device
+    current for the call, and refuse a stream of another device."""
+    if stream is not None and stream.device != device:
+        raise ValueError(f"stream is on {stream.device}, the tensors on {device}")
+    return torch.cuda.device(device)
+
+
 def _check_inputs(q, k, v):
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not t.is_cuda:
@@ -105,6 +137,8 @@ def _check_inputs(q, k, v):
             raise ValueError(f"{name} must be bfloat16")
         if t.dim() != 4 or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous [B, H, N, d] tensor")
+    if k.device != q.device or v.device != q.device:
+        raise ValueError("q, k and v must be on the same device")
     B, H, Nq, d = q.shape
     if k.shape != (B, H, k.shape[2], d) or v.shape != k.shape:
         raise ValueError("k and v must be [B, H, Nk, d] with q's B, H and d")
@@ -131,12 +165,11 @@ def attn_fwd(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None)
     B, H, Nq, Nk, d = _check_inputs(q, k, v)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    if out is None:
-        out = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q.device)
-    if lse is None:
-        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
-    st = load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nk, d,
-                         int(bool(causal)), float(scale), _stream_ptr(stream))
+    out = _out(out, (B, H, Nq, d), torch.bfloat16, q.device, "out")
+    lse = _out(lse, (B, H, Nq), torch.float32, q.device, "lse")
+    with _on(q.device, stream):
+        st = load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nk, d,
+                             int(bool(causal)), float(scale), _stream_ptr(stream))
     _check(st, "attn_fwd")
     return out, lse
 
@@ -161,15 +194,16 @@ def attn_fwd_fp8(q8, k8, vt8, descale_q=1.0, descale_k=1.0, descale_v=1.0, causa
     Nk = k8.shape[2]
     if k8.shape != (B, H, Nk, d) or vt8.shape != (B, H, d, Nk):
         raise ValueError("k8 must be [B, H, Nk, d] and vt8 [B, H, d, Nk] with q8's B, H and d")
+    if k8.device != q8.device or vt8.device != q8.device:
+        raise ValueError("q8, k8 and vt8 must be on the same device")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    if out is None:
-        out = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q8.device)
-    if lse is None:
-        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q8.device)
-    st = load().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(vt8), _ptr(out), _ptr(lse), B, H, Nq, Nk,
-                             d, int(bool(causal)), float(scale), float(descale_q),
-                             float(descale_k), float(descale_v), _stream_ptr(stream))
+    out = _out(out, (B, H, Nq, d), torch.bfloat16, q8.device, "out")
+    lse = _out(lse, (B, H, Nq), torch.float32, q8.device, "lse")
+    with _on(q8.device, stream):
+        st = load().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(vt8), _ptr(out), _ptr(lse), B, H, Nq,
+                                 Nk, d, int(bool(causal)), float(scale), float(descale_q),
+                                 float(descale_k), float(descale_v), _stream_ptr(stream))
     _check(st, "attn_fwd_fp8")
     return out, lse
 
@@ -186,17 +220,14 @@ def attn_fwd_decode(q, k, v, scale=None, out=None, lse=None, workspace=None, str
         raise ValueError("attn_fwd_decode takes a single query row (Nq = 1)")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    if out is None:
-        out = torch.empty((B, H, 1, d), dtype=torch.bfloat16, device=q.device)
-    if lse is None:
-        lse = torch.empty((B, H, 1), dtype=torch.float32, device=q.device)
-    need = decode_workspace_bytes(B, H, Nk, d)
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    out = _out(out, (B, H, 1, d), torch.bfloat16, q.device, "out")
+    lse = _out(lse, (B, H, 1), torch.float32, q.device, "lse")
+    workspace = _workspace(workspace, decode_workspace_bytes(B, H, Nk, d), q.device)
     ws_ptr = _ptr(workspace) if workspace is not None else ctypes.c_void_p(0)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    st = load().attn_fwd_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nk, d,
-                                float(scale), ws_ptr, ws_bytes, _stream_ptr(stream))
+    with _on(q.device, stream):
+        st = load().attn_fwd_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nk,
+                                    d, float(scale), ws_ptr, ws_bytes, _stream_ptr(stream))
     _check(st, "attn_fwd_decode")
     return out, lse
 
@@ -206,28 +237,40 @@ def attn_fwd_from_host(q, k, v, o, lse, dq, dk, dv, do_, dlse, causal=False, sca
     """End-to-end attn_fwd on pinned HOST tensors (q, k, v in; o, lse out)
     through the caller's device buffers dq, dk, dv, do_, dlse.  Asynchronous
     on ``stream``: synchronise before reading o and lse."""
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q must be [B, H, Nq, d] and k, v [B, H, Nk, d]")
     B, H, Nq, d = q.shape
     Nk = k.shape[2]
-    for t in (q, k, v, o, lse):
-        if t.is_cuda or not t.is_contiguous():
-            raise ValueError("q, k, v, o, lse must be contiguous host tensors")
-    for t in (dq, dk, dv, do_, dlse):
-        if not t.is_cuda:
-            raise ValueError("dq, dk, dv, do_, dlse must be CUDA tensors")
+    bf, f32 = torch.bfloat16, torch.float32
+    for name, t, shape, dt in (("q", q, (B, H, Nq, d), bf), ("k", k, (B, H, Nk, d), bf),
+                               ("v", v, (B, H, Nk, d), bf), ("o", o, (B, H, Nq, d), bf),
+                               ("lse", lse, (B, H, Nq), f32)):
+        if t.is_cuda or not t.is_contiguous() or t.dtype != dt or tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be a contiguous {dt} host tensor of shape {shape}")
+    dev = dq.device if dq is not None else torch.device("cuda", torch.cuda.current_device())
+    if dev.type != "cuda":
+        raise ValueError("dq, dk, dv, do_, dlse must be CUDA tensors")
+    dq = _out(dq, (B, H, Nq, d), bf, dev, "dq")
+    dk = _out(dk, (B, H, Nk, d), bf, dev, "dk")
+    dv = _out(dv, (B, H, Nk, d), bf, dev, "dv")
+    do_ = _out(do_, (B, H, Nq, d), bf, dev, "do_")
+    dlse = _out(dlse, (B, H, Nq), f32, dev, "dlse")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    st = load().attn_fwd_from_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dq),
-                                   _ptr(dk), _ptr(dv), _ptr(do_), _ptr(dlse), B, H, Nq, Nk, d,
-                                   int(bool(causal)), float(scale), _stream_ptr(stream))
+    with _on(dev, stream):
+        st = load().attn_fwd_from_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dq),
+                                       _ptr(dk), _ptr(dv), _ptr(do_), _ptr(dlse), B, H, Nq, Nk,
+                                       d, int(bool(causal)), float(scale), _stream_ptr(stream))
     _check(st, "attn_fwd_from_host")
     return o, lse
 
 
-def _seqlens_ptr(t, B, name):
+def _seqlens_ptr(t, B, name, device):
     if t is None:
         return ctypes.c_void_p(0)
-    if not t.is_cuda or t.dtype != torch.int32 or t.shape != (B,) or not t.is_contiguous():
-        raise ValueError(f"{name} must be a contiguous int32 CUDA tensor of shape [B]")
+    if (t.device != device or t.dtype != torch.int32 or t.shape != (B,)
+            or not t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous int32 tensor of shape [B] on {device}")
     return _ptr(t)
 
 
@@ -239,14 +282,14 @@ def attn_fwd_ragged(q, k, v, seqlens_q=None, seqlens_k=None, causal=False, scale
     B, H, Nq, Nk, d = _check_inputs(q, k, v)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    if out is None:
-        out = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q.device)
-    if lse is None:
-        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
-    st = load().attn_fwd_ragged(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
-                                _seqlens_ptr(seqlens_q, B, "seqlens_q"),
-                                _seqlens_ptr(seqlens_k, B, "seqlens_k"), B, H, Nq, Nk, d,
-                                int(bool(causal)), float(scale), _stream_ptr(stream))
+    out = _out(out, (B, H, Nq, d), torch.bfloat16, q.device, "out")
+    lse = _out(lse, (B, H, Nq), torch.float32, q.device, "lse")
+    sq = _seqlens_ptr(seqlens_q, B, "seqlens_q", q.device)
+    sk = _seqlens_ptr(seqlens_k, B, "seqlens_k", q.device)
+    with _on(q.device, stream):
+        st = load().attn_fwd_ragged(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), sq, sk, B,
+                                    H, Nq, Nk, d, int(bool(causal)), float(scale),
+                                    _stream_ptr(stream))
     _check(st, "attn_fwd_ragged")
     return out, lse
 
@@ -260,18 +303,16 @@ def attn_fwd_decode_ragged(q, k, v, seqlens_k=None, scale=None, out=None, lse=No
         raise ValueError("attn_fwd_decode_ragged takes a single query row (Nq = 1)")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    if out is None:
-        out = torch.empty((B, H, 1, d), dtype=torch.bfloat16, device=q.device)
-    if lse is None:
-        lse = torch.empty((B, H, 1), dtype=torch.float32, device=q.device)
-    need = decode_workspace_bytes(B, H, Nk, d)
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    out = _out(out, (B, H, 1, d), torch.bfloat16, q.device, "out")
+    lse = _out(lse, (B, H, 1), torch.float32, q.device, "lse")
+    workspace = _workspace(workspace, decode_workspace_bytes(B, H, Nk, d), q.device)
     ws_ptr = _ptr(workspace) if workspace is not None else ctypes.c_void_p(0)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    st = load().attn_fwd_decode_ragged(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
-                                       _seqlens_ptr(seqlens_k, B, "seqlens_k"), B, H, Nk, d,
-                                       float(scale), ws_ptr, ws_bytes, _stream_ptr(stream))
+    sk = _seqlens_ptr(seqlens_k, B, "seqlens_k", q.device)
+    with _on(q.device, stream):
+        st = load().attn_fwd_decode_ragged(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), sk,
+                                           B, H, Nk, d, float(scale), ws_ptr, ws_bytes,
+                                           _stream_ptr(stream))
     _check(st, "attn_fwd_decode_ragged")
     return out, lse
 
@@ -285,13 +326,14 @@ def attn_merge(o_parts, lse_parts, out=None, lse=None, stream=None):
     for name, t, dt in (("o_parts", o_parts, torch.bfloat16), ("lse_parts", lse_parts, torch.float32)):
         if not t.is_cuda or t.dtype != dt or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous {dt} CUDA tensor")
+    if lse_parts.device != o_parts.device:
+        raise ValueError("o_parts and lse_parts must be on the same device")
     S, B, H, Nq, d = o_parts.shape
-    if out is None:
-        out = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=o_parts.device)
-    if lse is None:
-        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=o_parts.device)
-    st = load().attn_merge(_ptr(o_parts), _ptr(lse_parts), S, _ptr(out), _ptr(lse), B, H, Nq, d,
-                           _stream_ptr(stream))
+    out = _out(out, (B, H, Nq, d), torch.bfloat16, o_parts.device, "out")
+    lse = _out(lse, (B, H, Nq), torch.float32, o_parts.device, "lse")
+    with _on(o_parts.device, stream):
+        st = load().attn_merge(_ptr(o_parts), _ptr(lse_parts), S, _ptr(out), _ptr(lse), B, H,
+                               Nq, d, _stream_ptr(stream))
     _check(st, "attn_merge")
     return out, lse
 
@@ -309,25 +351,21 @@ def attn_bwd(q, k, v, o, lse, dout, causal=False, scale=None, dq=None, dk=None, 
     B, H, Nq, Nk, d = _check_inputs(q, k, v)
     for name, t, dt in (("o", o, torch.bfloat16), ("dout", dout, torch.bfloat16),
                         ("lse", lse, torch.float32)):
-        if not t.is_cuda or t.dtype != dt or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous {dt} CUDA tensor")
+        if t.device != q.device or t.dtype != dt or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {dt} tensor on {q.device}")
     if o.shape != q.shape or dout.shape != q.shape or lse.shape != (B, H, Nq):
         raise ValueError("o and dout must be [B, H, Nq, d] and lse [B, H, Nq]")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    if dq is None:
-        dq = torch.empty_like(q)
-    if dk is None:
-        dk = torch.empty_like(k)
-    if dv is None:
-        dv = torch.empty_like(v)
-    need = bwd_workspace_bytes(B, H, Nq, Nk, d)
-    if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    st = load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
-                         _ptr(dk), _ptr(dv), B, H, Nq, Nk, d, int(bool(causal)), float(scale),
-                         _ptr(workspace), workspace.numel() * workspace.element_size(),
-                         _stream_ptr(stream))
+    dq = _out(dq, q.shape, torch.bfloat16, q.device, "dq")
+    dk = _out(dk, k.shape, torch.bfloat16, q.device, "dk")
+    dv = _out(dv, v.shape, torch.bfloat16, q.device, "dv")
+    workspace = _workspace(workspace, bwd_workspace_bytes(B, H, Nq, Nk, d), q.device)
+    with _on(q.device, stream):
+        st = load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                             _ptr(dq), _ptr(dk), _ptr(dv), B, H, Nq, Nk, d, int(bool(causal)),
+                             float(scale), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     _check(st, "attn_bwd")
     return dq, dk, dv
 
