@@ -236,7 +236,8 @@ def attn_fwd_from_host(q, k, v, o, lse, dq, dk, dv, do_, dlse, causal=False, sca
                        stream=None):
     """End-to-end attn_fwd on pinned HOST tensors (q, k, v in; o, lse out)
     through the caller's device buffers dq, dk, dv, do_, dlse.  Asynchronous
-    on ``stream``: synchronise before reading o and lse."""
+    on ``stream``: synchronise before reading o and lse.  Host tensors that
+    are not pinned are refused."""
     if q.dim() != 4 or k.dim() != 4:
         raise ValueError("q must be [B, H, Nq, d] and k, v [B, H, Nk, d]")
     B, H, Nq, d = q.shape
@@ -247,6 +248,11 @@ def attn_fwd_from_host(q, k, v, o, lse, dq, dk, dv, do_, dlse, causal=False, sca
                                ("lse", lse, (B, H, Nq), f32)):
         if t.is_cuda or not t.is_contiguous() or t.dtype != dt or tuple(t.shape) != shape:
             raise ValueError(f"{name} must be a contiguous {dt} host tensor of shape {shape}")
+        # pageable memory would make every copy synchronous and serialise the
+        # chunked pipeline whose overlap of copies and kernels is the point
+        if not t.is_pinned():
+            raise ValueError(f"{name} must be in pinned (page-locked) host memory "
+                             f"(tensor.pin_memory())")
     dev = dq.device if dq is not None else torch.device("cuda", torch.cuda.current_device())
     if dev.type != "cuda":
         raise ValueError("dq, dk, dv, do_, dlse must be CUDA tensors")

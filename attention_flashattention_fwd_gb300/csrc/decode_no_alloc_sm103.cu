@@ -7,13 +7,21 @@
 // memory is owned and budgeted by that application, or a latency-critical
 // serving loop where cudaMalloc/cudaFree are off limits because they can
 // synchronise the whole device.  attn_fwd_decode_no_alloc serves them: its
-// scratch is a fixed array in the library's own device memory, reserved when
-// the library is loaded, so the call itself allocates nothing.
+// scratch is a fixed array in the library's own device memory, so the call
+// allocates nothing itself.
 //
 // The array is file-scope, so host code cannot use its name as a device
 // address; the address is looked up once per device with
 // cudaGetSymbolAddress (on the first call made while that device is current)
 // and handed to the same split and combine kernels attn_fwd_decode uses.
+// CUDA loads a library's device code lazily, on first use per device, so it
+// is that first call's lookup that loads this file's module and reserves the
+// array on the device (and may synchronise it): make the first call during
+// set-up, outside any serving loop or stream capture.  The cached address
+// belongs to the device's primary context; after cudaDeviceReset the module
+// is reloaded elsewhere and the cached address is stale, so this call (like
+// the rest of the library, whose per-device state is cached the same way)
+// must not be used after a reset in the same process.
 #include <mutex>
 
 #include "gbattn_internal.h"
@@ -58,19 +66,20 @@ extern "C" int attn_fwd_decode_no_alloc(const void* q, const void* k, const void
     if (!(scale > 0.f && scale < INFINITY)) return ATTN_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
     const long long BH = static_cast<long long>(B) * H;
-    int splits, kps;
-    gbattn::decode_split_plan(BH, Nk, &splits, &kps);
-    if (BH * splits > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-    // more partial results than the fixed scratch holds: use attn_fwd_decode
-    const size_t need = gbattn::decode_workspace_bytes(BH, Nk, d);
-    if (need > kScratchBytes) return ATTN_ERR_UNSUPPORTED;
+    if (BH * gbattn::kDecodeMaxSplits > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    // more partial results than the fixed scratch holds (the workspace
+    // attn_fwd_decode would ask for, which bounds every device's plan): use
+    // attn_fwd_decode with a workspace of the caller's
+    if (gbattn::decode_workspace_bytes(BH, Nk, d) > kScratchBytes) return ATTN_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return ATTN_ERR_MISALIGNED;
+    int num_sms = 0;
+    int st = gbattn::current_sm_count(&num_sms);
+    if (st != ATTN_OK) return st;
+    int splits, kps;
+    gbattn::decode_split_plan(BH, Nk, num_sms, &splits, &kps);
     void* scratch = nullptr;
-    if (need > 0) {
-        const int st = scratch_address(&scratch);
-        if (st != ATTN_OK) return st;
-    }
+    if (splits > 1 && (st = scratch_address(&scratch)) != ATTN_OK) return st;
     // Nothing in the scratch has to start at zero: every partial the combine
     // kernel reads is written by the split kernel of the same call.
     gbattn::DecodeParams p;
@@ -80,7 +89,7 @@ extern "C" int attn_fwd_decode_no_alloc(const void* q, const void* k, const void
     p.o = static_cast<__nv_bfloat16*>(o);
     p.lse = lse;
     p.part_o = static_cast<float*>(scratch);
-    p.part_lse = need > 0 ? static_cast<float*>(scratch) + BH * splits * d : nullptr;
+    p.part_lse = splits > 1 ? static_cast<float*>(scratch) + BH * splits * d : nullptr;
     p.BH = static_cast<int>(BH);
     p.Nk = Nk;
     p.splits = splits;

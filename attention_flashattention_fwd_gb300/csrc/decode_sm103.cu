@@ -31,6 +31,7 @@ namespace {
 constexpr int kDecThreads = 256;   // 8 warps
 constexpr int kUnroll = 8;         // key rows in flight per lane group and iteration
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr int kDecMinKeysPerSplit = 512;  // a split streams at least this many keys
 
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
     uint4 r;
@@ -218,15 +219,14 @@ __global__ void __launch_bounds__(D) attn_fwd_decode_combine_kernel(DecodeParams
 
 // ------------------------------------------------------------------ host side
 
-// Split policy: aim for a few thousand CTAs (the GPU has 152 SMs), never fewer
+// Split policy: aim for 16 CTAs per SM of the device (num_sms), never fewer
 // than 512 keys per split, at most 64 splits.  Pure arithmetic on the sizes.
-void decode_split_plan(long long BH, int Nk, int* splits, int* keys_per_split) {
-    const long long kTargetCtas = 4 * 152 * 4;
-    const int kMinKeys = 512;
-    long long s = (kTargetCtas + BH - 1) / BH;
-    const long long max_by_keys = (Nk + kMinKeys - 1) / kMinKeys;
+void decode_split_plan(long long BH, int Nk, int num_sms, int* splits, int* keys_per_split) {
+    const long long target_ctas = 16LL * (num_sms > 0 ? num_sms : 1);
+    long long s = (target_ctas + BH - 1) / BH;
+    const long long max_by_keys = (Nk + kDecMinKeysPerSplit - 1) / kDecMinKeysPerSplit;
     if (s > max_by_keys) s = max_by_keys;
-    if (s > 64) s = 64;
+    if (s > kDecodeMaxSplits) s = kDecodeMaxSplits;
     if (s < 1) s = 1;
     int kps = static_cast<int>((Nk + s - 1) / s);
     s = (Nk + kps - 1) / kps;  // no empty split
@@ -234,13 +234,19 @@ void decode_split_plan(long long BH, int Nk, int* splits, int* keys_per_split) {
     *keys_per_split = kps;
 }
 
-size_t decode_workspace_bytes(long long BH, int Nk, int d) {
-    int splits, kps;
-    decode_split_plan(BH, Nk, &splits, &kps);
+size_t decode_partials_bytes(long long BH, int splits, int d) {
     if (splits <= 1) return 0;
     const size_t n = static_cast<size_t>(BH) * splits;
     // partial outputs [BH, splits, d] fp32, then partial lse [BH, splits] fp32
     return n * d * sizeof(float) + n * sizeof(float);
+}
+
+// The most splits the plan takes on any device: the bound depends on the
+// sizes alone, so the workspace a caller sizes on one machine fits every GPU.
+size_t decode_workspace_bytes(long long BH, int Nk, int d) {
+    long long s = (Nk + kDecMinKeysPerSplit - 1) / kDecMinKeysPerSplit;
+    if (s > kDecodeMaxSplits) s = kDecodeMaxSplits;
+    return decode_partials_bytes(BH, static_cast<int>(s), d);
 }
 
 int launch_decode(int d, const DecodeParams& p, cudaStream_t stream) {

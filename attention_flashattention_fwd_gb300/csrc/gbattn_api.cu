@@ -78,6 +78,10 @@ int ensure_init() {
 // Streaming multiprocessors of the current device (cached per device).
 std::atomic<int> g_num_sms[kMaxDevices];
 
+}  // namespace
+
+namespace gbattn {
+
 int current_sm_count(int* out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
@@ -95,6 +99,10 @@ int current_sm_count(int* out) {
     *out = n;
     return ATTN_OK;
 }
+
+}  // namespace gbattn
+
+namespace {
 
 // [BH, N, d] bf16 viewed as a 3-D tensor (d innermost), boxes of 64 x 128 x 1
 // with the 128-byte swizzle the tcgen05 operand descriptors expect.
@@ -301,14 +309,18 @@ int decode_impl(const void* q, const void* k, const void* v, void* o, float* lse
     if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
     const long long BH = static_cast<long long>(B) * H;
-    int splits, kps;
-    decode_split_plan(BH, Nk, &splits, &kps);
-    if (BH * splits > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    // the workspace bound covers every device's plan; it is checked before any CUDA call
     const size_t need = decode_workspace_bytes(BH, Nk, d);
+    if (BH * kDecodeMaxSplits > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
         (need > 0 && !aligned16(workspace)))
         return ATTN_ERR_MISALIGNED;
+    int num_sms = 0;
+    const int sst = current_sm_count(&num_sms);
+    if (sst != ATTN_OK) return sst;
+    int splits, kps;
+    decode_split_plan(BH, Nk, num_sms, &splits, &kps);
     DecodeParams p;
     p.q = static_cast<const __nv_bfloat16*>(q);
     p.k = static_cast<const __nv_bfloat16*>(k);
@@ -316,7 +328,7 @@ int decode_impl(const void* q, const void* k, const void* v, void* o, float* lse
     p.o = static_cast<__nv_bfloat16*>(o);
     p.lse = lse;
     p.part_o = static_cast<float*>(workspace);
-    p.part_lse = need > 0 ? static_cast<float*>(workspace) + BH * splits * d : nullptr;
+    p.part_lse = splits > 1 ? static_cast<float*>(workspace) + BH * splits * d : nullptr;
     p.BH = static_cast<int>(BH);
     p.Nk = Nk;
     p.splits = splits;

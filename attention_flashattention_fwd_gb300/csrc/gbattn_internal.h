@@ -81,6 +81,10 @@ struct MergeParams {
     int n_parts;
 };
 
+// gbattn_api.cu: streaming multiprocessors of the current device (cached per
+// device ordinal).
+int current_sm_count(int* out);
+
 // prefill_sm103.cu
 int prefill_set_attributes();
 // Persistent launch: min(work items, num_sms) CTAs, one per SM.
@@ -100,7 +104,14 @@ constexpr unsigned kErrBitTimeout = 1u;  // a bounded barrier wait ran out
 constexpr unsigned kErrBitLengths = 4u;  // a per-sequence length was out of range
 
 // decode_sm103.cu
-void decode_split_plan(long long BH, int Nk, int* splits, int* keys_per_split);
+// Splits of each (b, h)'s keys for a device with num_sms SMs (at most
+// kDecodeMaxSplits).
+constexpr int kDecodeMaxSplits = 64;
+void decode_split_plan(long long BH, int Nk, int num_sms, int* splits, int* keys_per_split);
+// Bytes of the split partials of a plan with `splits` splits (0 for one split).
+size_t decode_partials_bytes(long long BH, int splits, int d);
+// Workspace the caller provides: the partials of the largest plan any device
+// takes for these sizes (depends on the sizes alone).
 size_t decode_workspace_bytes(long long BH, int Nk, int d);
 int launch_decode(int d, const DecodeParams& p, cudaStream_t stream);
 unsigned read_and_clear_decode_error();

@@ -2,9 +2,10 @@
 """Benchmark of the fused attention forward on GB300.
 
 One step is one pass of the whole hot path over one batch of synthetic
-input: the prefill kernel on the causal B=2, H=16, N=4096, d=128 workload
-(the headline: attention fwd TFLOP/s against the bf16 tensor peak), the
-prefill kernel on the causal B=1, H=32, N=16384, d=128 long-sequence workload,
+input: the prefill kernel on the causal B=2, H=16, N=4096, d=128 workload,
+the prefill kernel on the causal B=1, H=32, N=16384, d=128 long-sequence
+workload (the largest single-GPU prefill workload of the study, whose
+attention fwd TFLOP/s against the bf16 tensor peak is the line's `value`),
 and the split-K decode (split kernel + combine kernel) on the
 B=64, H=32, Nk=8192, d=128 decode workload (HBM GB/s).  L2 is flushed before
 every step: a 256 MiB write, then a 256 MiB read of another buffer, so no dirty
@@ -233,8 +234,8 @@ def head_rows(w, bh, stride=1, offset=0):
 
 
 def cpu_baseline_leg(w, q_bits, k_bits, v_bits, o_gpu=None, lse_gpu=None):
-    """Time the oracle, as it stands, on whole heads of the headline workload
-    until about CPU_SAMPLE_SECONDS have passed."""
+    """Time the oracle, as it stands, on whole heads of workload `w` until about
+    CPU_SAMPLE_SECONDS have passed."""
     import numpy as np
 
     import oracle
@@ -273,11 +274,11 @@ def run_reference(args):
 
     import oracle
     from attention_flashattention_fwd_gb300.inputs import WORKLOADS, bf16_bits, make_workload
-    w = WORKLOADS[HEADLINE]
+    w = WORKLOADS[LONG]
     q, k, v = make_workload(w, device="cpu")
     qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
     BH = w.B * w.H
-    stride = 8  # a step = every 8th query row of one head (512 rows, ~0.5 GFLOP)
+    stride = 32  # a step = every 32nd query row of one head (512 rows, ~2.1 GFLOP)
     times, flops = [], []
     for s in range(args.warmup + args.steps):
         rows = head_rows(w, s % BH, stride=stride, offset=s % stride)
@@ -483,12 +484,12 @@ def run_gpu(args):
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": achieved / peaks["bf16_tflops"],
                          "traffic": profiled_traffic(prof, sources),
-                         "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)"},
+                         "peak_source": f"{peak_src} bf16 burst"},
             # secondary: the softmax's exponentials against the SFU rate
             "sfu": {"exps_per_launch": exps, "achieved": exp_rate, "peak": sfu_peak,
                     "unit": "Texp/s", "frac": exp_rate / sfu_peak,
-                    "peak_source": f"{SFU_EX2_PER_CLK_SM:g} ex2 per clock per SM (measured) x "
-                                   f"{n_sms} SMs x {sfu_mhz:g} MHz (median SM clock under load)"},
+                    "peak_source": f"{SFU_EX2_PER_CLK_SM:g} ex2/clk/SM x {n_sms} SMs x "
+                                   f"{sfu_mhz:g} MHz"},
         }
 
     p3 = prefill_part(w3, ms3, PREFILL_SOURCES, "ncu_prefill_" + HEADLINE)
@@ -500,31 +501,33 @@ def run_gpu(args):
           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                        "frac": gbs / peaks["hbm_gbs"],
                        "traffic": profiled_traffic("ncu_decode_" + DECODE, DECODE_SOURCES),
-                       "peak_source": f"{peak_src} HBM copy (MEASURED_PEAKS.json)"}}
+                       "peak_source": f"{peak_src} HBM copy"}}
 
-    # ---- end to end through the C ABI with host buffers (headline workload)
-    qh, kh, vh = (t.cpu().pin_memory() for t in (q3, k3, v3))
-    oh = torch.empty(q3.shape, dtype=torch.bfloat16).pin_memory()
-    lh = torch.empty(q3.shape[:3], dtype=torch.float32).pin_memory()
-    e2e_steps = min(K, 20)
+    # ---- end to end through the C ABI with host buffers (the long workload,
+    # the line's `value`): pinned host q, k, v in, pinned host o, lse out
+    qh, kh, vh = (t.cpu().pin_memory() for t in (q4, k4, v4))
+    oh = torch.empty(q4.shape, dtype=torch.bfloat16).pin_memory()
+    lh = torch.empty(q4.shape[:3], dtype=torch.float32).pin_memory()
+    e2e_steps = min(K, 10)
     for _ in range(3):
-        binding.attn_fwd_from_host(qh, kh, vh, oh, lh, q3, k3, v3, o3, l3, causal=True,
-                                   scale=w3.scale, stream=stream)
+        binding.attn_fwd_from_host(qh, kh, vh, oh, lh, q4, k4, v4, o4, l4, causal=True,
+                                   scale=w4.scale, stream=stream)
     torch.cuda.synchronize()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
-        binding.attn_fwd_from_host(qh, kh, vh, oh, lh, q3, k3, v3, o3, l3, causal=True,
-                                   scale=w3.scale, stream=stream)
+        binding.attn_fwd_from_host(qh, kh, vh, oh, lh, q4, k4, v4, o4, l4, causal=True,
+                                   scale=w4.scale, stream=stream)
     e1.record(stream)
     torch.cuda.synchronize()
     (e2e_ms,) = max_over_ranks([e0.elapsed_time(e1)], world, device=dev)
-    e2e = {"value": world * e2e_steps * w3.flops() / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+    e2e = {"value": world * e2e_steps * w4.flops() / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
            "h2d_bytes_per_step": int(qh.nbytes + kh.nbytes + vh.nbytes),
            "d2h_bytes_per_step": int(oh.nbytes + lh.nbytes),
            "ms_per_step": e2e_ms / e2e_steps,
            "path": "attn_fwd_from_host (pinned host q,k,v -> device -> kernel -> host o,lse)"}
+    del qh, kh, vh, oh, lh
 
     # ---- the backward pass (next-row widening; not part of the timed step):
     # attn_bwd on the headline workload with the step's own o and lse, timed
@@ -567,7 +570,7 @@ def run_gpu(args):
         "roofline": {"bound": "tensor", "achieved": bwd_tf, "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": bwd_tf / peaks["bf16_tflops"],
                      "traffic": profiled_traffic("ncu_backward_" + HEADLINE, BACKWARD_SOURCES),
-                     "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)"},
+                     "peak_source": f"{peak_src} bf16 burst"},
     }
 
     # ---- non-causal prefill at d = 128, N = 4096 (not part of the timed step)
@@ -629,8 +632,7 @@ def run_gpu(args):
         "roofline": {"bound": "tensor", "achieved": f_tf, "peak": fp8_peak, "unit": "TFLOP/s",
                      "frac": f_tf / fp8_peak,
                      "traffic": profiled_traffic("ncu_prefill_fp8_" + w3.name, PREFILL_SOURCES),
-                     "peak_source": f"{FP8_PEAK_RATIO:g} x {peak_src} bf16 dense burst "
-                                    "(MEASURED_PEAKS.json; nominal fp8:bf16 = 4.5:2.25)"},
+                     "peak_source": f"{FP8_PEAK_RATIO:g} x {peak_src} bf16 burst"},
     }
     del q8, k8, vt8, o8, l8
 
@@ -662,36 +664,55 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "achieved": m_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": m_gbs / peaks["hbm_gbs"],
                      "traffic": profiled_traffic("ncu_merge_" + w3.name, MERGE_SOURCES),
-                     "peak_source": f"{peak_src} HBM copy (MEASURED_PEAKS.json)"},
+                     "peak_source": f"{peak_src} HBM copy"},
     }
 
     line = {
-        "metric": METRIC, "value": p3["value"], "unit": "TFLOP/s", "n_gpus": world,
+        "metric": METRIC, "value": p4["value"], "unit": "TFLOP/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": total_ms / K,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded iid Gaussian Q,K,V rounded to bf16)",
-        "config": {"workload": HEADLINE, "B": w3.B, "H": w3.H, "Nq": w3.Nq, "Nk": w3.Nk,
-                   "d": w3.d, "causal": True, "scale": w3.scale,
+        "config": {"workload": LONG, "B": w4.B, "H": w4.H, "Nq": w4.Nq, "Nk": w4.Nk,
+                   "d": w4.d, "causal": True, "scale": w4.scale,
                    "step": f"prefill {HEADLINE} + prefill {LONG} + decode {DECODE}",
-                   "l2": "flushed before every step (256 MiB write, then a 256 MiB read so no dirty line remains)",
+                   "l2": "flushed before every step (256 MiB write, then a 256 MiB read)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": p3["roofline"],
+        "roofline": p4["roofline"],
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": launches_per_step * K,
         "parts": {HEADLINE: p3, LONG: p4, DECODE: p5},
         "noncausal": noncausal,
         "fp8": fp8,
         "backward": backward,
         "merge": merge,
-        "e2e": e2e,
-        "clocks": clocks,
-        "gpu_launches": launches_per_step * K,
     }
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        BH = w3.B * w3.H
-        o_np = o3.reshape(BH, w3.Nq, w3.d).float().cpu().numpy()
-        l_np = l3.reshape(BH, w3.Nq).cpu().numpy()
-        line["cpu_baseline"] = cpu_baseline_leg(w3, bf16_bits(q3), bf16_bits(k3), bf16_bits(v3),
+        BH = w4.B * w4.H
+        o_np = o4.reshape(BH, w4.Nq, w4.d).float().cpu().numpy()
+        l_np = l4.reshape(BH, w4.Nq).cpu().numpy()
+        line["cpu_baseline"] = cpu_baseline_leg(w4, bf16_bits(q4), bf16_bits(k4), bf16_bits(v4),
                                                 o_np, l_np)
+
+    # last: one compact entry per measured kernel (value, unit, fraction of its
+    # measured roofline, ms per launch), so the end of the line holds them all
+    def brief(part, ms_key):
+        r = part["roofline"]
+        return [round(part["value"], 1), part["unit"], round(r["frac"], 3),
+                round(part[ms_key], 4)]
+
+    line["summary"] = {
+        "fields": ["value", "unit", "frac_of_measured_peak", "ms_per_launch"],
+        "prefill_" + LONG: brief(p4, "ms_per_launch"),
+        "prefill_" + HEADLINE: brief(p3, "ms_per_launch"),
+        "prefill_" + wn.name: brief(noncausal, "ms_per_launch"),
+        "decode_" + w5.name.replace("decode_", ""): brief(p5, "ms_per_call"),
+        "fp8_" + w3.name: brief(fp8, "ms_per_call"),
+        "backward_" + w3.name: brief(backward, "ms_per_call"),
+        "merge4_" + w3.name: brief(merge, "ms_per_call"),
+        "e2e_" + LONG: [round(e2e["value"], 1), e2e["unit"], None, round(e2e["ms_per_step"], 4)],
+    }
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -27,6 +27,10 @@
  *     attributes and an SM count set once per device, and the streams and
  *     events attn_fwd_from_host creates per device on first use (its enqueue
  *     is serialised by a mutex).
+ *   - Contexts: that per-device state is cached by device ordinal for the
+ *     life of the process and belongs to the device's primary context (the
+ *     one the CUDA runtime uses).  After cudaDeviceReset it is stale: do not
+ *     call the library again in that process.
  *   - CUDA graphs: after one call on a device (which creates that state),
  *     every call can be captured in a CUDA graph and replayed.  Calls enqueue
  *     only kernel launches; attn_fwd_from_host also enqueues copies (capture
@@ -124,7 +128,10 @@ int attn_fwd_fp8(const void *q, const void *k, const void *vt, void *o, float *l
 
 /*
  * attn_fwd_decode_workspace_bytes -- bytes of device workspace attn_fwd_decode
- * needs for these sizes (0 when a single split covers every key).  Pure host
+ * needs for these sizes: room for the split partials of the largest split
+ * plan any device takes (at most one split per 512 keys and 64 splits per
+ * (b, h); the plan itself follows the device's SM count), so a workspace
+ * sized once fits every GPU.  0 when Nk <= 512 (one split).  Pure host
  * arithmetic; never touches the GPU.  Returns 0 for invalid sizes as well.
  */
 size_t attn_fwd_decode_workspace_bytes(int B, int H, int Nk, int d);
@@ -197,8 +204,12 @@ int attn_fwd_from_host(const void *q, const void *k, const void *v, void *o, flo
  *   rejected with ATTN_ERR_UNSUPPORTED before anything is launched; use
  *   attn_fwd_decode with your own workspace for them.
  *   The first call on each device looks up the scratch array's device
- *   address (cudaGetSymbolAddress) with that device current; make that first
- *   call before any stream capture.
+ *   address (cudaGetSymbolAddress) with that device current.  CUDA loads the
+ *   library's device code lazily, so it is this first call that loads the
+ *   module holding the array and reserves its memory on that device (and it
+ *   may synchronise the device): make the first call during set-up, outside
+ *   the serving loop and before any stream capture.  Later calls allocate
+ *   and look up nothing.
  *   All calls share the one array and it keeps the previous call's contents;
  *   nothing in it needs to start at zero.  Calls whose kernels overlap on the
  *   GPU (other streams, other host threads) race on the array: order them on
@@ -313,8 +324,9 @@ size_t attn_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d);
  *   stream      cudaStream_t.
  * Internal arithmetic: S and dP in fp32 on the tensor cores, P and dS
  * rounded to bf16 for the dV, dK and dQ products, fp32 accumulation of dK
- * and dV in Tensor Memory and of dQ in the workspace (atomic adds, so the
- * last bits of dQ may differ from run to run).
+ * and dV in Tensor Memory and of dQ in the workspace (TMA bulk reduce-adds
+ * from every key tile, in no fixed order, so the last bits of dQ may differ
+ * from run to run).
  * Returns ATTN_OK, ATTN_ERR_INVALID_ARG (also for a missing or too-small
  * workspace), ATTN_ERR_UNSUPPORTED, ATTN_ERR_MISALIGNED or ATTN_ERR_CUDA.
  */

@@ -25,3 +25,40 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def poisoned_outputs(request, monkeypatch):
+    """In GPU tests every output buffer the binding allocates starts as NaN and
+    every workspace as 0xFF bytes (a NaN in fp32), so an output element a
+    kernel failed to write can never pass as a value an earlier call left in
+    reused memory.  Only the tests' allocations change: the binding's checks
+    and the C entry points run as they are."""
+    if "gpu" not in request.keywords:
+        yield
+        return
+    import torch
+
+    from attention_flashattention_fwd_gb300 import binding
+    real_out, real_ws = binding._out, binding._workspace
+
+    def out(t, shape, dtype, device, name):
+        if t is None:
+            return torch.full(tuple(shape), float("nan"), dtype=dtype, device=device)
+        return real_out(t, shape, dtype, device, name)
+
+    def workspace(t, need, device):
+        if t is None and need > 0:
+            return torch.full((need,), 0xFF, dtype=torch.uint8, device=device)
+        return real_ws(t, need, device)
+
+    monkeypatch.setattr(binding, "_out", out)
+    monkeypatch.setattr(binding, "_workspace", workspace)
+    yield
+
+
+def nan_full(shape, dtype, device=None, pin=False):
+    """A buffer of NaN (for outputs a test passes in explicitly)."""
+    import torch
+    t = torch.full(tuple(shape), float("nan"), dtype=dtype, device=device)
+    return t.pin_memory() if pin else t

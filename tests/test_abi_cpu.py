@@ -69,10 +69,13 @@ def test_attn_fwd_rejects_before_launch(lib, kw, expect):
 
 
 def test_decode_workspace_bytes_is_host_arithmetic(lib):
-    # 2048 heads of 8192 keys: two splits, d + 1 floats per (head, split)
-    assert lib.attn_fwd_decode_workspace_bytes(64, 32, 8192, 128) == 2048 * 2 * (128 + 1) * 4
-    # few heads: more splits, at least 512 keys each
+    # room for the largest plan of any device: one split per 512 keys, d + 1
+    # floats per (head, split); 2048 heads of 8192 keys -> 16 splits each
+    assert lib.attn_fwd_decode_workspace_bytes(64, 32, 8192, 128) == 2048 * 16 * (128 + 1) * 4
     assert lib.attn_fwd_decode_workspace_bytes(1, 1, 8192, 128) == 16 * (128 + 1) * 4
+    assert lib.attn_fwd_decode_workspace_bytes(1, 1, 8193, 64) == 17 * (64 + 1) * 4
+    # at most 64 splits
+    assert lib.attn_fwd_decode_workspace_bytes(2, 3, 1 << 20, 128) == 6 * 64 * (128 + 1) * 4
     # a single split needs no workspace
     assert lib.attn_fwd_decode_workspace_bytes(64, 32, 300, 64) == 0
     assert lib.attn_fwd_decode_workspace_bytes(1, 1, 0, 64) == 0

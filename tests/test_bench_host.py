@@ -27,7 +27,7 @@ def test_reference_arm_prints_one_json_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
-    assert d["config"]["workload"] == bench.HEADLINE
+    assert d["config"]["workload"] == bench.LONG  # the GPU arm's `value` workload
 
 
 def test_reference_arm_non_zero_rank_does_no_work():

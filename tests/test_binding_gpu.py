@@ -86,3 +86,14 @@ def test_host_path_refuses_wrong_host_dtype():
     with pytest.raises(ValueError):
         binding.attn_fwd_from_host(q, k, v, o, lse, dq, dk, dv, torch.empty_like(dq),
                                    torch.empty((B, H, NQ), device="cuda"))
+
+
+def test_host_path_refuses_pageable_host_memory():
+    # pageable buffers would turn the pipelined copies synchronous
+    q, k, v = (t.cpu() for t in _qkv())
+    o = torch.empty((B, H, NQ, D), dtype=torch.bfloat16)
+    lse = torch.empty((B, H, NQ), dtype=torch.float32)
+    dq, dk, dv = (torch.empty_like(t, device="cuda") for t in (q, k, v))
+    with pytest.raises(ValueError, match="pinned"):
+        binding.attn_fwd_from_host(q, k, v, o, lse, dq, dk, dv, torch.empty_like(dq),
+                                   torch.empty((B, H, NQ), device="cuda"))

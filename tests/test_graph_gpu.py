@@ -16,6 +16,7 @@ import torch
 import oracle
 from attention_flashattention_fwd_gb300 import binding
 from attention_flashattention_fwd_gb300.inputs import bf16_bits, make_qkv, make_qkv_fp8
+from tests.conftest import nan_full
 
 pytestmark = pytest.mark.gpu
 
@@ -120,15 +121,15 @@ def test_graph_replay_host_buffer_path():
     one graph; a replay after new values land in the pinned inputs returns the
     same host outputs as an eager call."""
     dev = torch.device("cuda:0")
-    h = {n: torch.empty(s, dtype=dt, pin_memory=True) for n, s, dt in (
+    h = {n: nan_full(s, dt, pin=True) for n, s, dt in (
         ("q", (B, H, NQ, D), torch.bfloat16), ("k", (B, H, NK, D), torch.bfloat16),
         ("v", (B, H, NK, D), torch.bfloat16), ("o", (B, H, NQ, D), torch.bfloat16),
         ("lse", (B, H, NQ), torch.float32))}
-    d = {"dq": torch.empty((B, H, NQ, D), dtype=torch.bfloat16, device=dev),
-         "dk": torch.empty((B, H, NK, D), dtype=torch.bfloat16, device=dev),
-         "dv": torch.empty((B, H, NK, D), dtype=torch.bfloat16, device=dev),
-         "do_": torch.empty((B, H, NQ, D), dtype=torch.bfloat16, device=dev),
-         "dlse": torch.empty((B, H, NQ), dtype=torch.float32, device=dev)}
+    d = {"dq": nan_full((B, H, NQ, D), torch.bfloat16, dev),
+         "dk": nan_full((B, H, NK, D), torch.bfloat16, dev),
+         "dv": nan_full((B, H, NK, D), torch.bfloat16, dev),
+         "do_": nan_full((B, H, NQ, D), torch.bfloat16, dev),
+         "dlse": nan_full((B, H, NQ), torch.float32, dev)}
 
     def fill(seed):
         q, k, v = make_qkv(B, H, NQ, NK, D, seed=seed, device="cpu")
@@ -148,8 +149,8 @@ def test_graph_replay_host_buffer_path():
         call()
     for seed in (303, 404):
         fill(seed)
-        h["o"].zero_()
-        h["lse"].zero_()
+        h["o"].fill_(float("nan"))
+        h["lse"].fill_(float("nan"))
         graph.replay()
         torch.cuda.synchronize()
         o_r, lse_r = h["o"].clone(), h["lse"].clone()

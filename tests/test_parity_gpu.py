@@ -14,6 +14,7 @@ import torch
 import oracle
 from attention_flashattention_fwd_gb300 import binding
 from attention_flashattention_fwd_gb300.inputs import WORKLOADS, bf16_bits, make_qkv, make_workload
+from tests.conftest import nan_full
 
 O_MAX, O_MEAN, LSE_MAX = 2e-2, 1e-3, 2e-3
 
@@ -185,7 +186,8 @@ def test_b2h16n4096d128_noncausal_sampled():
 
 def test_b1h32n16384d128_causal_sampled():
     w = WORKLOADS["b1h32n16384d128_causal"]
-    _rows_check(w, full_heads=[], n_random=384,
+    # one full head (all 16384 rows, ~70 GFLOP in the fp64 oracle) plus samples
+    _rows_check(w, full_heads=[w.B * w.H - 1], n_random=384,
                 extra_rows=[0, 1, 127, 128, 255, 256, 8191, 8192, 16383] + list(range(0, 512, 7)))
 
 
@@ -329,11 +331,11 @@ def test_from_host_end_to_end(B, H, N, d):
     # the heads cross the host link in up to five chunks (sizes falling off) on three streams
     q, k, v = make_qkv(B, H, N, N, d, seed=56 + H, device="cpu")
     qh, kh, vh = (t.pin_memory() for t in (q, k, v))
-    oh = torch.empty((B, H, N, d), dtype=torch.bfloat16).pin_memory()
-    lh = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
-    dq, dk, dv = (torch.empty_like(t, device=_dev()) for t in (q, k, v))
-    do_ = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=_dev())
-    dl = torch.empty((B, H, N), dtype=torch.float32, device=_dev())
+    oh = nan_full((B, H, N, d), torch.bfloat16, pin=True)
+    lh = nan_full((B, H, N), torch.float32, pin=True)
+    dq, dk, dv = (nan_full(t.shape, t.dtype, _dev()) for t in (q, k, v))
+    do_ = nan_full((B, H, N, d), torch.bfloat16, _dev())
+    dl = nan_full((B, H, N), torch.float32, _dev())
     s = torch.cuda.Stream()
     binding.attn_fwd_from_host(qh, kh, vh, oh, lh, dq, dk, dv, do_, dl, causal=True, stream=s)
     s.synchronize()  # the caller's stream alone covers the whole call
@@ -354,6 +356,8 @@ def test_repeated_launches_are_bitwise_stable(name):
     o0, l0 = binding.attn_fwd(q, k, v, causal=w.causal, scale=w.scale)
     o, lse = torch.empty_like(o0), torch.empty_like(l0)
     for _ in range(30):
+        o.fill_(float("nan"))
+        lse.fill_(float("nan"))
         binding.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)
         torch.cuda.synchronize()
         assert torch.equal(o, o0) and torch.equal(lse, l0)

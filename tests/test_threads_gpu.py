@@ -26,6 +26,10 @@ SCRIPT = textwrap.dedent(r"""
     from attention_flashattention_fwd_gb300 import binding
     from attention_flashattention_fwd_gb300.inputs import make_qkv
 
+    def nan_full(shape, dtype, device=None, pin=False):
+        t = torch.full(tuple(shape), float("nan"), dtype=dtype, device=device)
+        return t.pin_memory() if pin else t
+
     dev = torch.device("cuda:0")
     torch.cuda.init()
     DEVICE_CASES = [  # B, H, Nq, Nk, d, causal
@@ -42,11 +46,11 @@ SCRIPT = textwrap.dedent(r"""
         q, k, v = make_qkv(B, H, Nq, Nk, d, seed=950 + i, device="cpu")
         pin = lambda t: t.pin_memory()
         h = dict(q=pin(q), k=pin(k), v=pin(v),
-                 o=torch.empty((B, H, Nq, d), dtype=torch.bfloat16).pin_memory(),
-                 lse=torch.empty((B, H, Nq), dtype=torch.float32).pin_memory())
-        dd = dict(dq=torch.empty_like(q, device=dev), dk=torch.empty_like(k, device=dev),
-                  dv=torch.empty_like(v, device=dev), do_=torch.empty_like(q, device=dev),
-                  dlse=torch.empty((B, H, Nq), dtype=torch.float32, device=dev))
+                 o=nan_full((B, H, Nq, d), torch.bfloat16, pin=True),
+                 lse=nan_full((B, H, Nq), torch.float32, pin=True))
+        dd = dict(dq=nan_full(q.shape, q.dtype, dev), dk=nan_full(k.shape, k.dtype, dev),
+                  dv=nan_full(v.shape, v.dtype, dev), do_=nan_full(q.shape, q.dtype, dev),
+                  dlse=nan_full((B, H, Nq), torch.float32, dev))
         return h, dd, c
 
     dev_in = [dev_inputs(i) for i in range(len(DEVICE_CASES))]
@@ -102,7 +106,8 @@ SCRIPT = textwrap.dedent(r"""
     for i in range(len(host_in)):
         h, dd, c = host_in[i]
         ro, rl = results[("host", i)]
-        h["o"].zero_()
+        h["o"].fill_(float("nan"))
+        h["lse"].fill_(float("nan"))
         binding.attn_fwd_from_host(h["q"], h["k"], h["v"], h["o"], h["lse"], dd["dq"], dd["dk"],
                                    dd["dv"], dd["do_"], dd["dlse"], causal=c)
         torch.cuda.synchronize()
