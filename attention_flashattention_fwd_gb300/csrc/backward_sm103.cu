@@ -348,11 +348,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Work item: key tile j of head bh, most query tiles (lowest j under a
-    // causal mask) first.  Key tile j is seen by query q iff some key k of
-    // it has k <= q + causal_off, i.e. from query tile (kj0 - off) / 128 on.
-    const int j = static_cast<int>(blockIdx.x) / p.BH;
-    const int bh = static_cast<int>(blockIdx.x) % p.BH;
+    // Work item: key tile j of head bh.  The grid runs through groups of
+    // head_group heads; within a group, most query tiles (lowest j under a
+    // causal mask) first, the group's heads side by side.  Key tile j is seen
+    // by query q iff some key k of it has k <= q + causal_off, i.e. from
+    // query tile (kj0 - off) / 128 on.
+    const int per_group = p.head_group * p.n_kt;
+    const int grp = static_cast<int>(blockIdx.x) / per_group;
+    const int within = static_cast<int>(blockIdx.x) - grp * per_group;
+    const int g_heads = min(p.head_group, p.BH - grp * p.head_group);
+    const int j = within / g_heads;
+    const int bh = grp * p.head_group + within % g_heads;
     const int kj0 = j * kTile;
     const int n_qt = p.Nq_pad / kTile;
     int i_first = 0;

@@ -199,6 +199,21 @@ int encode_u8(CUtensorMap* m, const void* base, long long BH, int x, int y) {
     return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// Heads per group of the backward's CTA order: as many as keep their Q and dO
+// rows (bf16) and fp32 dQ accumulator rows within a quarter of the L2 cache.
+int bwd_head_group(long long BH, int Nq, int d, int* out) {
+    int dev = 0, l2 = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    const long long per_head = (static_cast<long long>(Nq) + 127) / 128 * 128 * d * (2 + 2 + 4);
+    long long g = (static_cast<long long>(l2) / 4) / per_head;
+    if (g < 1) g = 1;
+    if (g > BH) g = BH;
+    *out = static_cast<int>(g);
+    return ATTN_OK;
+}
+
 int enqueue_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
                 const float* lse, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk,
                 int d, int causal, float scale, void* workspace, cudaStream_t stream) {
@@ -237,6 +252,7 @@ int enqueue_bwd(const void* q, const void* k, const void* v, const void* o, cons
     p.Nq_pad = nq_pad;
     p.BH = static_cast<int>(BH);
     p.n_kt = (Nk + 127) / 128;
+    if ((st = bwd_head_group(BH, Nq, d, &p.head_group)) != ATTN_OK) return st;
     p.causal = causal;
     p.causal_off = causal ? Nk - Nq : 0;
     p.scale = scale;

@@ -67,6 +67,10 @@ struct BwdParams {
     const float* nD;     // [BH, Nq_pad] -D
     int Nq, Nk, Nq_pad, BH;
     int n_kt;            // key tiles per head: ceil(Nk / 128)
+    // CTAs are ordered in groups of head_group heads: within a group by key
+    // tile (most query tiles first), then by head, so the CTAs in flight at
+    // once share the Q, dO and dQ accumulator rows of a few heads in L2
+    int head_group;
     int causal, causal_off;
     float scale, scale_log2;
 };
