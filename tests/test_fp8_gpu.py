@@ -105,6 +105,7 @@ SHAPES = [
     (1, 1, 1008, 1008, True),    # many tiles, ragged, causal
     (1, 1, 1, 704, True),        # one causal query row sees every key
     (1, 77, 512, 512, False),    # 154 pairs on 152 SMs: the last wave as single tiles
+    (1, 79, 300, 384, False),    # 158 pairs: 12 single tiles
     (2, 1, 640, 1280, False),
 ]
 

@@ -85,12 +85,20 @@ def test_prefill_matches_oracle(B, H, Nq, Nk, d, causal):
 # Non-causal work whose query-tile pairs would leave the last wave of the
 # persistent grid part-full runs that tail as single 128-row tiles.  On a
 # 152-SM GB300: 158 pairs -> 152 pairs + 12 single tiles (of which the last
-# head's upper halves, rows 384..511 of 300, are empty), and 154 pairs ->
-# 152 pairs + 4 single tiles.  Every row is checked.
-@pytest.mark.parametrize("B,H,N,d", [(1, 79, 300, 64), (1, 77, 512, 128)])
-def test_last_wave_single_tiles_match_oracle(B, H, N, d):
-    q, k, v = make_qkv(B, H, N, N, d, seed=23 + N + d, device=_dev())
-    _full_check(q, k, v, False, what=f"{(B, H, N, d)} split tail")
+# head's upper halves, rows 384..511 of 300, are empty), 154 pairs -> 152
+# pairs + 4 single tiles, 160 pairs -> 152 + 16.  Every row is checked.
+@pytest.mark.parametrize("B,H,Nq,Nk,d", [
+    (1, 79, 300, 300, 64),
+    (1, 80, 260, 260, 64),
+    (1, 79, 384, 640, 128),    # Nq != Nk
+    (1, 77, 512, 512, 128),
+    (1, 77, 512, 512, 64),
+    (1, 79, 1000, 1000, 128),  # ragged last key tile
+    (1, 77, 300, 1024, 128),   # the tail tiles hold rows past Nq
+])
+def test_last_wave_single_tiles_match_oracle(B, H, Nq, Nk, d):
+    q, k, v = make_qkv(B, H, Nq, Nk, d, seed=23 + Nq + Nk + d, device=_dev())
+    _full_check(q, k, v, False, what=f"{(B, H, Nq, Nk, d)} split tail")
 
 
 def test_chunked_prefill_equals_prefill_at_once():
