@@ -312,13 +312,14 @@ def run_case(args):
     import torch
 
     from attention_flashattention_fwd_gb300 import binding
-    from attention_flashattention_fwd_gb300.inputs import WORKLOADS, Workload, make_workload
+    from attention_flashattention_fwd_gb300.inputs import (EXTRA_WORKLOADS, WORKLOADS, Workload,
+                                                           make_workload)
     if args.case == "custom":
         B, H, Nq, Nk, d, causal = (int(x) for x in args.shape.split(","))
         w = Workload(f"b{B}h{H}q{Nq}k{Nk}d{d}{'_causal' if causal else ''}", B, H, Nq, Nk, d,
                      bool(causal), seed=2000)
     else:
-        w = WORKLOADS[args.case]
+        w = WORKLOADS[args.case] if args.case in WORKLOADS else EXTRA_WORKLOADS[args.case]
     binding.load()
     dev = torch.device("cuda", 0)
     q, k, v = make_workload(w, device=dev)
