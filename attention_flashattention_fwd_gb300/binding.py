@@ -64,6 +64,8 @@ def _configure():
     lib.attn_bwd.restype = I
     lib.attn_fwd_ragged.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, P]
     lib.attn_fwd_ragged.restype = I
+    lib.attn_fwd_decode_mx.argtypes = [P, P, P, P, P, P, P, I, I, I, I, F, P, S, P]
+    lib.attn_fwd_decode_mx.restype = I
     lib.attn_fwd_decode_ragged.argtypes = [P, P, P, P, P, P, I, I, I, I, F, P, S, P]
     lib.attn_fwd_decode_ragged.restype = I
     lib.attn_merge.argtypes = [P, P, I, P, P, I, I, I, I, P]
@@ -229,6 +231,43 @@ def attn_fwd_decode(q, k, v, scale=None, out=None, lse=None, workspace=None, str
         st = load().attn_fwd_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nk,
                                     d, float(scale), ws_ptr, ws_bytes, _stream_ptr(stream))
     _check(st, "attn_fwd_decode")
+    return out, lse
+
+
+def attn_fwd_decode_mx(q, k8, k_scale, v8, v_scale, scale=None, out=None, lse=None,
+                       workspace=None, stream=None):
+    """The C entry point ``attn_fwd_decode_mx``: single-query attention with
+    MXFP8 keys and values.  q bf16 [B,H,1,d]; k8, v8 E4M3 codes [B,H,Nk,d]
+    (torch.float8_e4m3fn or uint8); k_scale, v_scale E8M0 codes [B,H,Nk,d/32]
+    (torch.float8_e8m0fnu or uint8).  Returns (o bf16 [B,H,1,d], lse fp32
+    [B,H,1])."""
+    if not q.is_cuda or q.dtype != torch.bfloat16 or q.dim() != 4 or not q.is_contiguous():
+        raise ValueError("q must be a contiguous bf16 CUDA tensor [B, H, 1, d]")
+    B, H, Nq, d = q.shape
+    if Nq != 1:
+        raise ValueError("attn_fwd_decode_mx takes a single query row (Nq = 1)")
+    Nk = k8.shape[2] if k8.dim() == 4 else -1
+    for name, t, shape, dts in (
+            ("k8", k8, (B, H, Nk, d), (torch.uint8, torch.float8_e4m3fn)),
+            ("v8", v8, (B, H, Nk, d), (torch.uint8, torch.float8_e4m3fn)),
+            ("k_scale", k_scale, (B, H, Nk, d // 32), (torch.uint8, torch.float8_e8m0fnu)),
+            ("v_scale", v_scale, (B, H, Nk, d // 32), (torch.uint8, torch.float8_e8m0fnu))):
+        if (t.device != q.device or t.dtype not in dts or tuple(t.shape) != shape
+                or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous {dts[0]} tensor of shape {shape} "
+                             f"on {q.device}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = _out(out, (B, H, 1, d), torch.bfloat16, q.device, "out")
+    lse = _out(lse, (B, H, 1), torch.float32, q.device, "lse")
+    workspace = _workspace(workspace, decode_workspace_bytes(B, H, Nk, d), q.device)
+    ws_ptr = _ptr(workspace) if workspace is not None else ctypes.c_void_p(0)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    with _on(q.device, stream):
+        st = load().attn_fwd_decode_mx(_ptr(q), _ptr(k8), _ptr(k_scale), _ptr(v8),
+                                       _ptr(v_scale), _ptr(out), _ptr(lse), B, H, Nk, d,
+                                       float(scale), ws_ptr, ws_bytes, _stream_ptr(stream))
+    _check(st, "attn_fwd_decode_mx")
     return out, lse
 
 

@@ -97,5 +97,7 @@ extern "C" int attn_fwd_decode_no_alloc(const void* q, const void* k, const void
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
     p.H = H;
     p.seqlens_k = nullptr;  // every sequence has all Nk keys
+    p.k_scale = nullptr;    // bf16 keys and values
+    p.v_scale = nullptr;
     return gbattn::launch_decode(d, p, static_cast<cudaStream_t>(stream));
 }

@@ -68,6 +68,57 @@ __device__ __forceinline__ void axpy8(float (&acc)[8], float p, uint4 v) {
     acc[7] = fmaf(p, bf_hi(v.w), acc[7]);
 }
 
+__device__ __forceinline__ uint32_t ld_stream_u8(const uint8_t* p) {
+    uint32_t r;
+    asm volatile("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+
+// Four E4M3 codes (lowest byte first) to fp32.  Every E4M3 value is an fp16
+// value, so both conversions (E4M3 pairs to fp16 pairs, fp16 to fp32) are exact.
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float (&f)[4]) {
+    asm("{\n\t.reg .b16 lo, hi, a0, a1, a2, a3;\n\t.reg .b32 h01, h23;\n\t"
+        "mov.b32 {lo, hi}, %4;\n\t"
+        "cvt.rn.f16x2.e4m3x2 h01, lo;\n\tcvt.rn.f16x2.e4m3x2 h23, hi;\n\t"
+        "mov.b32 {a0, a1}, h01;\n\tmov.b32 {a2, a3}, h23;\n\t"
+        "cvt.f32.f16 %0, a0;\n\tcvt.f32.f16 %1, a1;\n\tcvt.f32.f16 %2, a2;\n\t"
+        "cvt.f32.f16 %3, a3;\n\t}"
+        : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3])
+        : "r"(w));
+}
+
+// Value of an E8M0 scale code (OCP MX v1.0): 2^(code - 127), built from its
+// exponent bits; code 0 is 2^-127 (an fp32 subnormal), 0xFF is NaN.
+__device__ __forceinline__ float e8m0_to_f32(uint32_t code) {
+    return __uint_as_float(code == 0u ? 0x00400000u : code == 255u ? 0x7fc00000u : code << 23);
+}
+
+// sum over 16 E4M3 codes (a uint4) of q[c] * value(code c)
+__device__ __forceinline__ float dot16_e4m3(const float (&q)[16], uint4 k) {
+    const uint32_t w[4] = {k.x, k.y, k.z, k.w};
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float f[4];
+        e4m3x4_to_f32(w[i], f);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s = fmaf(q[4 * i + e], f[e], s);
+    }
+    return s;
+}
+
+// acc[c] += p * value(code c) over 16 E4M3 codes
+__device__ __forceinline__ void axpy16_e4m3(float (&acc)[16], float p, uint4 v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float f[4];
+        e4m3x4_to_f32(w[i], f);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[4 * i + e] = fmaf(p, f[e], acc[4 * i + e]);
+    }
+}
+
 }  // namespace
 
 // One CTA = one (b, h, split).  Lane group g (d/8 lanes) handles keys
@@ -194,6 +245,139 @@ __global__ void __launch_bounds__(kDecThreads)
     }
 }
 
+// MXFP8 keys and values (E4M3 codes, one E8M0 scale per 32 consecutive
+// elements of a row: the microscaling formats of the PDC course, Lecture 7,
+// section 7.14): the split kernel above with one byte per element.  A key row
+// of d codes is read by d/16 neighbouring lanes (16 codes per 16-byte load), so
+// a lane's slice lies in one scale block: the lane multiplies its partial dot
+// by the key's block scale before the lane group sums the slices, and folds
+// the value's block scale into the probability before its axpy.  Every code
+// is widened exactly (E4M3 -> fp16 -> fp32); the arithmetic is the bf16
+// kernel's, so the decode reads 1 + 1/32 bytes per K and V element instead of 2.
+template <int D>
+__global__ void __launch_bounds__(kDecThreads, 2)
+    attn_fwd_decode_mx_split_kernel(DecodeParams p) {
+    constexpr int kLanesPerRow = D / 16;             // 8 (d=128) or 4 (d=64)
+    constexpr int kGroupsPerWarp = 32 / kLanesPerRow;
+    constexpr int kGroups = (kDecThreads / 32) * kGroupsPerWarp;
+    constexpr int kNb = D / 32;                      // scale blocks per row
+
+    __shared__ float sm_m[kGroups];
+    __shared__ float sm_l[kGroups];
+    __shared__ float sm_acc[kGroups][D];
+
+    const int bh = blockIdx.x / p.splits;
+    const int split = blockIdx.x % p.splits;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = warp * kGroupsPerWarp + lane / kLanesPerRow;
+    const int sub = lane % kLanesPerRow;  // which 16-element slice of the row
+    const int ks = split * p.keys_per_split;
+    const int ke = min(p.Nk, ks + p.keys_per_split);
+
+    float q[16];
+    {
+        const uint4* qp = reinterpret_cast<const uint4*>(p.q + static_cast<size_t>(bh) * D + sub * 16);
+        const uint4 a = qp[0], b = qp[1];
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            // fold scale * log2(e) into q once
+            q[2 * i] = bf_lo(w[i]) * p.scale_log2;
+            q[2 * i + 1] = bf_hi(w[i]) * p.scale_log2;
+        }
+    }
+    const uint8_t* k8 = reinterpret_cast<const uint8_t*>(p.k);
+    const uint8_t* v8 = reinterpret_cast<const uint8_t*>(p.v);
+    const uint8_t* kbase = k8 + static_cast<size_t>(bh) * p.Nk * D + sub * 16;
+    const uint8_t* vbase = v8 + static_cast<size_t>(bh) * p.Nk * D + sub * 16;
+    const uint8_t* ksbase = p.k_scale + static_cast<size_t>(bh) * p.Nk * kNb + sub / 2;
+    const uint8_t* vsbase = p.v_scale + static_cast<size_t>(bh) * p.Nk * kNb + sub / 2;
+
+    float m = -INFINITY, l = 0.f;
+    float acc[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+
+    for (int base = ks; base < ke; base += kGroups * kUnroll) {
+        uint4 kr[kUnroll], vr[kUnroll];
+        uint32_t kx[kUnroll], vx[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int j = base + u * kGroups + g;
+            if (j < ke) {
+                kr[u] = ld_stream(kbase + static_cast<size_t>(j) * D);
+                vr[u] = ld_stream(vbase + static_cast<size_t>(j) * D);
+                kx[u] = ld_stream_u8(ksbase + static_cast<size_t>(j) * kNb);
+                vx[u] = ld_stream_u8(vsbase + static_cast<size_t>(j) * kNb);
+            } else {
+                kr[u] = make_uint4(0, 0, 0, 0);
+                vr[u] = make_uint4(0, 0, 0, 0);
+                kx[u] = 127u;
+                vx[u] = 127u;
+            }
+        }
+        float s[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) s[u] = dot16_e4m3(q, kr[u]) * e8m0_to_f32(kx[u]);
+        // sum the d/16 partial dots of each row across its lane group
+#pragma unroll
+        for (int off = kLanesPerRow / 2; off >= 1; off >>= 1)
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) s[u] += __shfl_xor_sync(0xffffffffu, s[u], off);
+        float mx = m;
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            if (base + u * kGroups + g >= ke) s[u] = -INFINITY;
+            mx = fmaxf(mx, s[u]);
+        }
+        if (mx == -INFINITY) continue;  // every key of this group is past the range
+        const float alpha = ex2_approx(m - mx);  // m = -inf on the first visit gives 0
+        l *= alpha;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc[e] *= alpha;
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const float pu = ex2_approx(s[u] - mx);
+            l += pu;
+            axpy16_e4m3(acc, pu * e8m0_to_f32(vx[u]), vr[u]);
+        }
+        m = mx;
+    }
+
+    // ---- merge the lane groups of the CTA (as in the bf16 kernel)
+#pragma unroll
+    for (int e = 0; e < 16; ++e) sm_acc[g][sub * 16 + e] = acc[e];
+    if (sub == 0) {
+        sm_m[g] = m;
+        sm_l[g] = l;
+    }
+    __syncthreads();
+    if (threadIdx.x < D) {
+        const int c = threadIdx.x;
+        float M = -INFINITY;
+#pragma unroll 4
+        for (int i = 0; i < kGroups; ++i) M = fmaxf(M, sm_m[i]);
+        float Lsum = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+            for (int i = 0; i < kGroups; ++i) {
+                if (sm_m[i] == -INFINITY) continue;
+                const float w = ex2_approx(sm_m[i] - M);
+                Lsum = fmaf(w, sm_l[i], Lsum);
+                O = fmaf(w, sm_acc[i][c], O);
+            }
+        }
+        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+        if (p.splits == 1) {
+            p.o[static_cast<size_t>(bh) * D + c] = __float2bfloat16_rn(O * inv);
+            if (c == 0) p.lse[bh] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
+        } else {
+            const size_t ps = static_cast<size_t>(bh) * p.splits + split;
+            p.part_o[ps * D + c] = O * inv;
+            if (c == 0) p.part_lse[ps] = Lsum > 0.f ? M + log2f(Lsum) : -INFINITY;
+        }
+    }
+}
+
 // Merge the splits of one (b, h): lse = log2 sum_s 2^{lse_s},
 // o = sum_s 2^{lse_s - lse} o_s.  One CTA per (b, h), one thread per column.
 template <int D>
@@ -257,6 +441,22 @@ int launch_decode(int d, const DecodeParams& p, cudaStream_t stream) {
             attn_fwd_decode_combine_kernel<128><<<p.BH, 128, 0, stream>>>(p);
     } else {
         attn_fwd_decode_split_kernel<64><<<static_cast<unsigned>(grid), kDecThreads, 0, stream>>>(p);
+        if (p.splits > 1)
+            attn_fwd_decode_combine_kernel<64><<<p.BH, 64, 0, stream>>>(p);
+    }
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int launch_decode_mx(int d, const DecodeParams& p, cudaStream_t stream) {
+    const long long grid = static_cast<long long>(p.BH) * p.splits;
+    if (d == 128) {
+        attn_fwd_decode_mx_split_kernel<128>
+            <<<static_cast<unsigned>(grid), kDecThreads, 0, stream>>>(p);
+        if (p.splits > 1)
+            attn_fwd_decode_combine_kernel<128><<<p.BH, 128, 0, stream>>>(p);
+    } else {
+        attn_fwd_decode_mx_split_kernel<64>
+            <<<static_cast<unsigned>(grid), kDecThreads, 0, stream>>>(p);
         if (p.splits > 1)
             attn_fwd_decode_combine_kernel<64><<<p.BH, 64, 0, stream>>>(p);
     }

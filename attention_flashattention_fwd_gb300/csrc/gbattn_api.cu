@@ -317,9 +317,11 @@ size_t attn_fwd_decode_workspace_bytes(int B, int H, int Nk, int d) {
 
 namespace {
 
+// k_scale / v_scale non-null: k and v are MXFP8 codes with these block scales.
 int decode_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                 int Nk, int d, float scale, void* workspace, size_t workspace_bytes,
-                const int* seqlens_k, void* stream) {
+                const int* seqlens_k, void* stream, const void* k_scale = nullptr,
+                const void* v_scale = nullptr) {
     if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
     if (B <= 0 || H <= 0 || Nk <= 0) return ATTN_ERR_INVALID_ARG;
     if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
@@ -352,6 +354,9 @@ int decode_impl(const void* q, const void* k, const void* v, void* o, float* lse
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
     p.H = H;
     p.seqlens_k = seqlens_k;
+    p.k_scale = static_cast<const uint8_t*>(k_scale);
+    p.v_scale = static_cast<const uint8_t*>(v_scale);
+    if (k_scale) return launch_decode_mx(d, p, static_cast<cudaStream_t>(stream));
     return launch_decode(d, p, static_cast<cudaStream_t>(stream));
 }
 
@@ -364,6 +369,14 @@ int attn_fwd_decode(const void* q, const void* k, const void* v, void* o, float*
                     void* stream) {
     return decode_impl(q, k, v, o, lse, B, H, Nk, d, scale, workspace, workspace_bytes, nullptr,
                        stream);
+}
+
+int attn_fwd_decode_mx(const void* q, const void* k8, const void* k_scale, const void* v8,
+                       const void* v_scale, void* o, float* lse, int B, int H, int Nk, int d,
+                       float scale, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!k_scale || !v_scale) return ATTN_ERR_INVALID_ARG;
+    return decode_impl(q, k8, v8, o, lse, B, H, Nk, d, scale, workspace, workspace_bytes,
+                       nullptr, stream, k_scale, v_scale);
 }
 
 int attn_fwd_decode_ragged(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -44,6 +44,10 @@ struct DecodeParams {
     float scale_log2;
     int H;
     const int* seqlens_k;    // [B] per-sequence key counts, or null (all Nk)
+    // MXFP8 keys and values (attn_fwd_decode_mx): k and v then point at E4M3
+    // codes [BH, Nk, d] and these at the E8M0 block scales [BH, Nk, d / 32]
+    const uint8_t* k_scale;
+    const uint8_t* v_scale;
 };
 
 // Arguments of the backward preprocessing kernel.
@@ -118,6 +122,8 @@ size_t decode_partials_bytes(long long BH, int splits, int d);
 // takes for these sizes (depends on the sizes alone).
 size_t decode_workspace_bytes(long long BH, int Nk, int d);
 int launch_decode(int d, const DecodeParams& p, cudaStream_t stream);
+// the same split + combine kernels on MXFP8 keys and values
+int launch_decode_mx(int d, const DecodeParams& p, cudaStream_t stream);
 unsigned read_and_clear_decode_error();
 
 // selftest_sm103.cu

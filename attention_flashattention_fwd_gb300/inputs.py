@@ -117,3 +117,42 @@ def make_workload_fp8(w: Workload, device="cpu", seed=None):
 def bf16_bits(t: torch.Tensor):
     """The raw 16-bit patterns of a bf16 tensor as a numpy uint16 array (CPU copy)."""
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view("uint16")
+
+
+def mx_quantize(x: torch.Tensor, block: int = 32):
+    """MXFP8 quantisation of the last dimension of an fp32 tensor, following the
+    OCP Microscaling (MX) v1.0 conversion: each block of ``block`` consecutive
+    elements shares the E8M0 scale 2^(floor(log2 amax) - 8) (8 = the largest
+    E4M3 exponent), the elements divided by it are rounded to E4M3 by torch,
+    saturating at +-448.  Returns (codes uint8 [..., d], scales uint8
+    [..., d / block])."""
+    shp = x.shape
+    xb = x.reshape(*shp[:-1], shp[-1] // block, block).to(torch.float32)
+    amax = xb.abs().amax(dim=-1)
+    e = torch.floor(torch.log2(torch.where(amax > 0, amax, torch.ones_like(amax)))) - 8
+    X = torch.clamp(e + 127, 0, 254)  # biased E8M0 exponent
+    y = xb / torch.exp2(X - 127)[..., None]
+    codes = torch.clamp(y, -E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes.reshape(shp), X.to(torch.uint8)
+
+
+def make_qkv_mx(B, H, Nk, d, seed, device="cpu", sigma_qk=1.0, sigma_v=1.0):
+    """A decode step with MXFP8 keys and values: the Gaussian draws of
+    :func:`make_qkv` for Nq = 1 (same seed and order), q rounded to bf16 and K, V
+    quantised by :func:`mx_quantize`.  Returns (q bf16 [B,H,1,d], k8, k_scale,
+    v8, v_scale) with codes uint8 [B,H,Nk,d] and scales uint8 [B,H,Nk,d/32]."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    q = (torch.randn((B, H, 1, d), generator=g, device=device, dtype=torch.float32)
+         * sigma_qk).to(torch.bfloat16)
+    k = torch.randn((B, H, Nk, d), generator=g, device=device, dtype=torch.float32) * sigma_qk
+    v = torch.randn((B, H, Nk, d), generator=g, device=device, dtype=torch.float32) * sigma_v
+    k8, ks = mx_quantize(k)
+    del k
+    v8, vs = mx_quantize(v)
+    return q, k8.contiguous(), ks.contiguous(), v8.contiguous(), vs.contiguous()
+
+
+def make_workload_mx(w: Workload, device="cpu", seed=None):
+    return make_qkv_mx(w.B, w.H, w.Nk, w.d, w.seed if seed is None else seed, device,
+                       sigma_qk=w.sigma_qk)

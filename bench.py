@@ -57,9 +57,9 @@ def parse_args():
                     help="run only this workload's kernel(s) (profiling runs); prints its time")
     ap.add_argument("--shape", default=None,
                     help="with --case custom: B,H,Nq,Nk,d,causal of a profiling workload")
-    ap.add_argument("--pass", dest="which", choices=["fwd", "bwd", "fp8"], default="fwd",
-                    help="with --case: time the forward (default), the backward call or the "
-                         "forward on FP8 (E4M3) operands")
+    ap.add_argument("--pass", dest="which", choices=["fwd", "bwd", "fp8", "mx"], default="fwd",
+                    help="with --case: time the forward (default), the backward call, the "
+                         "forward on FP8 (E4M3) operands or (decode) MXFP8 keys and values")
     a = ap.parse_args()
     a.warmup = max(3, a.warmup)
     a.steps = max(1, a.steps)
@@ -350,6 +350,17 @@ def run_case(args):
         def launch():  # noqa: F811  (the timed call is the backward)
             binding.attn_bwd(q, k, v, o, lse, dout, causal=w.causal, scale=w.scale, dq=dq, dk=dk,
                              dv=dv, workspace=bws)
+    elif args.which == "mx":
+        if not w.decode:
+            raise SystemExit("--pass mx needs a decode workload")
+        from attention_flashattention_fwd_gb300.inputs import make_workload_mx
+        del q, k, v
+        qx, k8x, ksx, v8x, vsx = make_workload_mx(w, device=dev)
+        mx_bytes = sum(t.nbytes for t in (qx, k8x, ksx, v8x, vsx, o, lse))
+
+        def launch():  # noqa: F811  (the timed call is the MX decode)
+            binding.attn_fwd_decode_mx(qx, k8x, ksx, v8x, vsx, scale=w.scale, out=o, lse=lse,
+                                       workspace=ws)
     elif args.which == "fp8":
         if w.decode or w.d != 128:
             raise SystemExit("--pass fp8 needs a d = 128 prefill workload")
@@ -374,7 +385,10 @@ def run_case(args):
     ms = e0.elapsed_time(e1) / args.steps
     if binding.device_error() != 0:
         raise RuntimeError("a kernel reported a device-side error")
-    val = (w.algorithmic_bytes() / ms / 1e6, "GB/s") if w.decode else (
+    if args.which == "mx":
+        val = (mx_bytes / ms / 1e6, "GB/s")
+    else:
+        val = (w.algorithmic_bytes() / ms / 1e6, "GB/s") if w.decode else (
         flop_ratio * w.flops() / ms / 1e9, "TFLOP/s")
     print(json.dumps({"case": w.name, "pass": args.which, "ms_per_launch": ms, "value": val[0],
                       "unit": val[1], "steps": args.steps, "warmup": args.warmup,
@@ -637,6 +651,46 @@ def run_gpu(args):
     }
     del q8, k8, vt8, o8, l8
 
+    # ---- the decode workload with MXFP8 keys and values (not part of the timed
+    # step): E4M3 codes with one E8M0 scale per 32 elements, half the bytes
+    from attention_flashattention_fwd_gb300.inputs import make_workload_mx
+    qx, k8x, ksx, v8x, vsx = make_workload_mx(w5, device=dev)
+    ox, lx = torch.empty_like(o5), torch.empty_like(l5)
+
+    def mx_call():
+        binding.attn_fwd_decode_mx(qx, k8x, ksx, v8x, vsx, scale=w5.scale, out=ox, lse=lx,
+                                   workspace=ws5, stream=stream)
+
+    for _ in range(3):
+        mx_call()
+    torch.cuda.synchronize()
+    x_ms = 0.0
+    for _ in range(bwd_reps):
+        flush_l2()
+        torch.cuda._sleep(LAUNCH_COVER_CYCLES)
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        mx_call()
+        b1.record(stream)
+        torch.cuda.synchronize()
+        x_ms += b0.elapsed_time(b1)
+    if binding.device_error() != 0:
+        raise RuntimeError("a kernel reported a device-side error in the MX decode")
+    (x_ms,) = max_over_ranks([x_ms], world, device=dev)
+    x_per = x_ms / bwd_reps
+    x_bytes = sum(t.nbytes for t in (qx, k8x, ksx, v8x, vsx, ox, lx))
+    x_gbs = x_bytes / (x_per * 1e-3) / 1e9
+    decode_mx = {
+        "workload": w5.name, "operands": "K, V MXFP8 (E4M3 + one E8M0 scale per 32)",
+        "value": world * x_gbs, "unit": "GB/s", "ms_per_call": x_per, "calls": bwd_reps,
+        "bytes_per_call": x_bytes, "speedup_vs_bf16_decode": per5 / x_per,
+        "roofline": {"bound": "hbm", "achieved": x_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": x_gbs / peaks["hbm_gbs"],
+                     "traffic": profiled_traffic("ncu_decode_mx_" + DECODE, DECODE_SOURCES),
+                     "peak_source": f"{peak_src} HBM copy"},
+    }
+    del qx, k8x, ksx, v8x, vsx, ox, lx
+
     # ---- the exchange step of key-sharded attention (not part of the timed step):
     # attn_merge of MERGE_PARTS shard results of the headline shape
     o_parts = torch.stack([o3] * MERGE_PARTS).contiguous()
@@ -685,6 +739,7 @@ def run_gpu(args):
         "parts": {HEADLINE: p3, LONG: p4, DECODE: p5},
         "noncausal": noncausal,
         "fp8": fp8,
+        "decode_mx": decode_mx,
         "backward": backward,
         "merge": merge,
     }
@@ -709,6 +764,7 @@ def run_gpu(args):
         "prefill_" + HEADLINE: brief(p3, "ms_per_launch"),
         "prefill_" + wn.name: brief(noncausal, "ms_per_launch"),
         "decode_" + w5.name.replace("decode_", ""): brief(p5, "ms_per_call"),
+        "decode_mx_" + w5.name.replace("decode_", ""): brief(decode_mx, "ms_per_call"),
         "fp8_" + w3.name: brief(fp8, "ms_per_call"),
         "backward_" + w3.name: brief(backward, "ms_per_call"),
         "merge4_" + w3.name: brief(merge, "ms_per_call"),

@@ -160,6 +160,33 @@ int attn_fwd_decode(const void *q, const void *k, const void *v, void *o, float 
                     void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * attn_fwd_decode_mx -- attn_fwd_decode with MXFP8 keys and values.
+ *
+ * The microscaling (MX) formats give every block of 32 consecutive elements
+ * its own power-of-two scale (the fine-grained quantisation of PDC course
+ * Lecture 7, section 7.14; the bits follow the OCP Microscaling Formats v1.0
+ * specification): an element's value is 2^(X - 127) * E4M3(code), X the E8M0
+ * code of its block (0xFF is NaN).  Decode reads every key and value once, so
+ * storing the KV cache this way halves the bytes it streams.  Computes what
+ * attn_fwd_decode computes on the dequantised keys and values:
+ *   s_j = scale * q . K_j,  o = softmax(s) V (bf16),  lse = log sum_j e^{s_j}.
+ *
+ *   q        device bf16 [B,H,1,d].
+ *   k8, v8   device, E4M3 codes (one byte each) [B,H,Nk,d]; read only.
+ *   k_scale, v_scale  device, E8M0 codes [B,H,Nk,d/32]: the scale of elements
+ *            32 b .. 32 b + 31 of a key's (value's) row is its entry b; read only.
+ *   o, lse, workspace, stream, B, H, Nk, scale  as attn_fwd_decode (the same
+ *            workspace size: attn_fwd_decode_workspace_bytes(B, H, Nk, d)).
+ *   d in {64, 128}.  q, k8, v8, o, lse and the workspace 16-byte aligned.
+ * Internal arithmetic: codes widened exactly to fp32, fp32 dot products and
+ * accumulators, scales applied per block (exact powers of two).
+ * Returns as attn_fwd_decode; a NULL scale pointer is ATTN_ERR_INVALID_ARG.
+ */
+int attn_fwd_decode_mx(const void *q, const void *k8, const void *k_scale, const void *v8,
+                       const void *v_scale, void *o, float *lse, int B, int H, int Nk, int d,
+                       float scale, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * attn_fwd_from_host -- attn_fwd on HOST buffers, end to end.
  *
  * Host->device copies of q, k, v into the caller's device buffers dq, dk,

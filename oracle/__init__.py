@@ -21,6 +21,9 @@ Functions (each follows a passage of the lecture pages, cited in the C file):
   (CS336 L5 6.2; PDC L7 section 7.14).
 * :func:`fp8_operands` / :func:`attention_fp8` -- attention of per-tensor
   scaled FP8 operands: decode, then the naive attention above.
+* :func:`decode_mx` / :func:`attention_mx` -- MXFP8 (E4M3 elements, one E8M0
+  scale per 32 consecutive elements of a row; PDC L7 section 7.14, OCP MX
+  v1.0) keys and values: decode, then the naive attention above.
 
 Inputs are numpy arrays, either float64 or bfloat16 bit patterns (uint16).
 """
@@ -57,6 +60,10 @@ def _declare(lib):
     lib.oracle_attention_bwd_dkdv_keys.restype = I
     lib.oracle_decode_e4m3.argtypes = [P, P, L, D]
     lib.oracle_decode_e4m3.restype = None
+    lib.oracle_decode_mx.argtypes = [P, P, P, L, L, L]
+    lib.oracle_decode_mx.restype = I
+    lib.oracle_widen_bf16.argtypes = [P, P, L]
+    lib.oracle_widen_bf16.restype = None
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = I
     return lib
@@ -247,4 +254,33 @@ def attention_fp8(q8, k8, vt8, causal=False, scale=None, descale_q=1.0, descale_
     S = scale (descale_q Q8)(descale_k K8)^T, O = softmax(S) (descale_v V8).
     Returns (o [B,H,Nq,d], lse [B,H,Nq]) in float64."""
     q, k, v = fp8_operands(q8, k8, vt8, descale_q, descale_k, descale_v)
+    return attention(q, k, v, causal=causal, scale=scale)
+
+
+def decode_mx(codes, scales, block=32):
+    """float64 values of MXFP8 data: codes uint8 [..., d] (E4M3), scales uint8
+    [..., d / block] (E8M0), element c of a row scaled by its block's scale."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    d = codes.shape[-1]
+    if d % block or scales.shape != codes.shape[:-1] + (d // block,):
+        raise ValueError("scales must be [..., d / block]")
+    out = np.empty(codes.shape, np.float64)
+    rows = codes.size // d if d else 0
+    if _load().oracle_decode_mx(_ptr(codes), _ptr(scales), _ptr(out), rows, d, block) != 0:
+        raise ValueError("oracle_decode_mx rejected its arguments")
+    return out
+
+
+def attention_mx(q, k8, k_scale, v8, v_scale, causal=False, scale=None, block=32):
+    """Attention with MXFP8 keys and values (see :func:`decode_mx`): q [B,H,Nq,d]
+    (float64 or bf16 bits), k8 / v8 [B,H,Nk,d] E4M3 codes, k_scale / v_scale
+    [B,H,Nk,d/32] E8M0 codes.  Returns (o, lse) in float64."""
+    q = np.ascontiguousarray(q)
+    if q.dtype == np.uint16:  # bf16 bits: widen exactly, like the other inputs
+        qd = np.empty(q.shape, np.float64)
+        _load().oracle_widen_bf16(_ptr(q), _ptr(qd), q.size)
+        q = qd
+    k = decode_mx(k8, k_scale, block)
+    v = decode_mx(v8, v_scale, block)
     return attention(q, k, v, causal=causal, scale=scale)

@@ -67,6 +67,13 @@ static double widen_bf16(uint16_t bits)
     return (double)f;
 }
 
+/* dst[i] = the binary64 value of bfloat16 bit pattern src[i] (exact) */
+ORACLE_ABI void oracle_widen_bf16(const uint16_t *src, double *dst, long n)
+{
+    for (long i = 0; i < n; ++i)
+        dst[i] = widen_bf16(src[i]);
+}
+
 /* element `idx` of an input array that is binary64 (is_bf16 == 0) or bfloat16 */
 static double load_elem(const void *p, size_t idx, int is_bf16)
 {
@@ -637,4 +644,40 @@ ORACLE_ABI void oracle_decode_e4m3(const uint8_t *src, double *dst, long n, doub
 {
     for (long i = 0; i < n; ++i)
         dst[i] = descale * e4m3_value(src[i]);
+}
+
+/* ---- MX (microscaling) FP8 inputs --------------------------------------- */
+
+/*
+ * Value of one E8M0 block-scale code.  PDC course Lecture 7, section 7.14
+ * names the MX ("microscaling") formats for fine-grained quantisation on
+ * Blackwell without spelling out their bits; the definition followed here is
+ * the OCP Microscaling Formats (MX) v1.0 specification's E8M0: an unsigned
+ * 8-bit exponent with bias 127, value 2^(code - 127), no sign and no mantissa;
+ * the code 0xFF is NaN.
+ */
+static double e8m0_value(uint8_t code)
+{
+    if (code == 0xFF)
+        return NAN;
+    return ldexp(1.0, (int)code - 127);
+}
+
+/*
+ * MXFP8 dequantisation (same specification): `rows` rows of `d` E4M3 codes,
+ * the elements c of a row in blocks of `block` consecutive ones (32 for the
+ * MX formats), block b of row r sharing the scale scales[r * (d / block) + b]:
+ *   dst[r * d + c] = E8M0(scales[r * nb + c / block]) * E4M3(codes[r * d + c]).
+ * Returns 0, or -1 when d is not a multiple of block.
+ */
+ORACLE_ABI int oracle_decode_mx(const uint8_t *codes, const uint8_t *scales, double *dst,
+                                long rows, long d, long block)
+{
+    if (block <= 0 || d % block != 0)
+        return -1;
+    const long nb = d / block;
+    for (long r = 0; r < rows; ++r)
+        for (long c = 0; c < d; ++c)
+            dst[r * d + c] = e8m0_value(scales[r * nb + c / block]) * e4m3_value(codes[r * d + c]);
+    return 0;
 }

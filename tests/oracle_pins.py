@@ -447,6 +447,74 @@ def pin_fp8_descales(orc):
     assert np.max(np.abs(o3 - o4)) <= 1e-13 and np.max(np.abs(l3 - l4)) <= 1e-13
 
 
+# -- MX (microscaling) FP8 keys and values ----------------------------------
+
+def pin_e8m0_spec_values(orc):
+    """OCP MX v1.0 E8M0: value 2^(code - 127); 0xFF is NaN (decoded on E4M3
+    elements equal to 1.0, code 0x38)."""
+    codes = np.full((1, 7 * 32), 0x38, np.uint8)
+    scales = np.array([[0, 1, 126, 127, 128, 254, 255]], np.uint8)
+    got = orc.decode_mx(codes, scales).reshape(7, 32)
+    want = [2.0 ** -127, 2.0 ** -126, 0.5, 1.0, 2.0, 2.0 ** 127]
+    assert np.array_equal(got[:6], np.repeat(np.array(want)[:, None], 32, axis=1))
+    assert np.all(np.isnan(got[6]))
+
+
+def pin_e8m0_torch(orc):
+    """Every E8M0 code decodes to torch's float8_e8m0fnu value."""
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    got = orc.decode_mx(np.full((256, 32), 0x38, np.uint8), codes[:, None])[:, 0]
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan) and np.array_equal(got[~nan], ref[~nan])
+
+
+def _mx_codes(rows, d, seed):
+    """Seeded E4M3 element codes and E8M0 scale codes (scales 2^-6 .. 2^5)."""
+    rng = np.random.default_rng(seed)
+    codes = _fp8_codes((rows, d), seed)
+    scales = rng.integers(121, 133, size=(rows, d // 32)).astype(np.uint8)
+    return codes, scales
+
+
+def pin_mx_block_layout(orc):
+    """Element c of a row takes the scale of its block c // 32 of that row: the
+    decode equals torch's E4M3 value times torch's E8M0 value of that block."""
+    import torch
+    codes, scales = _mx_codes(5, 128, 50)
+    e = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    x = torch.from_numpy(scales.copy()).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    want = e * np.repeat(x, 32, axis=1)
+    got = orc.decode_mx(codes, scales)
+    assert np.array_equal(got, want)
+
+
+def pin_mx_attention_dequantised(orc):
+    """MX attention equals fp64 attention of the keys and values dequantised
+    block by block (numpy composition of the E4M3 and E8M0 decodes)."""
+    B, H, nk, d = 1, 3, 45, 64
+    rng = np.random.default_rng(51)
+    q = rng.standard_normal((B, H, 1, d))
+    k8, ks = _mx_codes(B * H * nk, d, 52)
+    v8, vs = _mx_codes(B * H * nk, d, 53)
+    k = (orc.decode_e4m3(k8) * np.repeat(2.0 ** (ks.astype(np.float64) - 127), 32, axis=1))
+    v = (orc.decode_e4m3(v8) * np.repeat(2.0 ** (vs.astype(np.float64) - 127), 32, axis=1))
+    shp, sshp = (B, H, nk, d), (B, H, nk, d // 32)
+    o1, l1 = orc.attention_mx(q, k8.reshape(shp), ks.reshape(sshp), v8.reshape(shp),
+                              vs.reshape(sshp), scale=0.2)
+    o2, l2 = orc.attention(q, k.reshape(shp), v.reshape(shp), scale=0.2)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    # a bf16 query (bit patterns) is widened exactly, as attention() widens it
+    import torch
+    qb = torch.from_numpy(q).to(torch.bfloat16)
+    bits = qb.view(torch.int16).numpy().view(np.uint16)
+    o3, l3 = orc.attention_mx(bits, k8.reshape(shp), ks.reshape(sshp), v8.reshape(shp),
+                              vs.reshape(sshp), scale=0.2)
+    o4, l4 = orc.attention(qb.to(torch.float64).numpy(), k.reshape(shp), v.reshape(shp), scale=0.2)
+    assert np.array_equal(o3, o4) and np.array_equal(l3, l4)
+
+
 ALL_PINS = [
     pin_exercise8_online_softmax,
     pin_rows_sum_to_one,
@@ -472,4 +540,8 @@ ALL_PINS = [
     pin_e4m3_torch,
     pin_fp8_attention_dequantised,
     pin_fp8_descales,
+    pin_e8m0_spec_values,
+    pin_e8m0_torch,
+    pin_mx_block_layout,
+    pin_mx_attention_dequantised,
 ]

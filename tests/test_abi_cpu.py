@@ -100,6 +100,25 @@ def test_decode_rejects_before_launch(lib):
     assert dec(ws=FAKE + 4) == MISALIGNED
 
 
+def test_decode_mx_rejects_before_launch(lib):
+    P = ctypes.c_void_p
+    lib.attn_fwd_decode_mx.argtypes = [P] * 7 + [ctypes.c_int] * 4 + [ctypes.c_float, P,
+                                                                      ctypes.c_size_t, P]
+    lib.attn_fwd_decode_mx.restype = ctypes.c_int
+    need = lib.attn_fwd_decode_workspace_bytes(1, 1, 8192, 128)
+
+    def dec(ks=FAKE, vs=FAKE, k8=FAKE, d=128, Nk=8192, ws_bytes=need):
+        return lib.attn_fwd_decode_mx(P(FAKE), P(k8), P(ks), P(FAKE), P(vs), P(FAKE), P(FAKE),
+                                      1, 1, Nk, d, 0.1, P(FAKE), ws_bytes, P(0))
+
+    assert dec(ks=0) == INVALID
+    assert dec(vs=0) == INVALID
+    assert dec(ws_bytes=need - 1) == INVALID
+    assert dec(d=96) == UNSUPPORTED
+    assert dec(k8=FAKE + 8) == MISALIGNED
+    assert dec(ks=FAKE + 1, vs=FAKE + 3, k8=FAKE + 8) == MISALIGNED  # scales: any alignment
+
+
 def test_from_host_rejects_before_launch(lib):
     P = ctypes.c_void_p
     args = [P(FAKE)] * 10

@@ -49,6 +49,11 @@ MUTANTS = [
     ("bwd_keys_top_left", "if (causal && j > i + (Nk - Nq))\n                    continue;",
      "if (causal && j > i)\n                    continue;"),
     ("bwd_keys_dv_uses_q", "dvj[c] += p * load_elem(dout,", "dvj[c] += p * load_elem(q,"),
+    ("mx_scale_bias", "return ldexp(1.0, (int)code - 127);", "return ldexp(1.0, (int)code - 128);"),
+    ("mx_block_index", "e8m0_value(scales[r * nb + c / block])", "e8m0_value(scales[r * nb + c % nb])"),
+    ("mx_scale_dropped", "e8m0_value(scales[r * nb + c / block]) * e4m3_value",
+     "1.0 * e4m3_value"),
+    ("mx_nan_code", "if (code == 0xFF)\n        return NAN;", "if (code == 0xFE)\n        return NAN;"),
 ]
 
 
