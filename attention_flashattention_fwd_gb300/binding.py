@@ -15,7 +15,10 @@ import threading
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libgbattn.so")
+# GBATTN_DEBUG=1 in the environment selects the debug build, whose kernels
+# check every direct global-memory index (see include/gbattn.h)
+LIB_PATH = os.path.join(_HERE, "libgbattn_debug.so" if os.environ.get("GBATTN_DEBUG") == "1"
+                        else "libgbattn.so")
 
 ATTN_OK = 0
 _lib = None
@@ -78,6 +81,10 @@ def _configure():
     lib.attn_selftest_timeout.restype = I
     lib.attn_version.argtypes = []
     lib.attn_version.restype = I
+    lib.attn_selftest_bounds.argtypes = [P]
+    lib.attn_selftest_bounds.restype = I
+    lib.attn_debug_build.argtypes = []
+    lib.attn_debug_build.restype = I
     return lib
 
 

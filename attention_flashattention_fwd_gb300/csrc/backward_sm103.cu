@@ -284,8 +284,10 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(BwdPrepParams a) {
         const long long bh = row / a.Nq_pad;
         const int i = static_cast<int>(row % a.Nq_pad);
         float acc = 0.f;
-        if (valid && i < a.Nq) {
-            const size_t off = (static_cast<size_t>(bh) * a.Nq + i) * D + c * 8;
+        const long long n_rows_q = a.rows / a.Nq_pad * a.Nq;  // B H Nq rows of o, dO, lse
+        const long long off_q = (bh * a.Nq + i) * D + c * 8;
+        if (valid && i < a.Nq && gb_index_ok(&g_bwd_error, off_q, off_q + 7, n_rows_q * D)) {
+            const size_t off = static_cast<size_t>(off_q);
             const uint4 ov = *reinterpret_cast<const uint4*>(a.o + off);
             const uint4 dv = *reinterpret_cast<const uint4*>(a.dout + off);
             const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
@@ -300,13 +302,15 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(BwdPrepParams a) {
         }
 #pragma unroll
         for (int sh = kLanes / 2; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
-        if (valid) {
+        if (valid && gb_index_ok(&g_bwd_error, row * D + c * 8, row * D + c * 8 + 7, a.rows * D)) {
             float4* z = reinterpret_cast<float4*>(a.dq_acc + row * D + c * 8);
             z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
             z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (c == 0) {
                 a.nD[row] = -acc;
-                a.nl2[row] = i < a.Nq
+                const bool lse_ok = i < a.Nq && gb_index_ok(&g_bwd_error, bh * a.Nq + i,
+                                                            bh * a.Nq + i, n_rows_q);
+                a.nl2[row] = lse_ok
                                  ? a.lse[static_cast<size_t>(bh) * a.Nq + i] * -1.4426950408889634f
                                  : -INFINITY;
             }
@@ -420,8 +424,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t dst = sRing + s * 2 * C::kTileBytes;
                 const int y = (i_first + it) * kTile;
                 const size_t row0 = static_cast<size_t>(bh) * p.Nq_pad + y;
-                bulk_load(sLd + s * 1024, p.nl2 + row0, 512, bars.q_full(s));
-                bulk_load(sLd + s * 1024 + 512, p.nD + row0, 512, bars.q_full(s));
+                // (debug builds: an out-of-range tile is not loaded; its stage
+                // then never completes and the consumers' bounded waits report it)
+                if (gb_index_ok(&g_bwd_error, static_cast<long long>(row0),
+                                static_cast<long long>(row0) + 127,
+                                static_cast<long long>(p.BH) * p.Nq_pad)) {
+                    bulk_load(sLd + s * 1024, p.nl2 + row0, 512, bars.q_full(s));
+                    bulk_load(sLd + s * 1024 + 512, p.nD + row0, 512, bars.q_full(s));
+                }
                 for (int sub = 0; sub < C::kSub; ++sub) {
                     tma_load_3d(dst + sub * C::kSubBytes, &tm_q, bars.q_full(s), sub * 64, y, bh);
                     tma_load_3d(dst + C::kTileBytes + sub * C::kSubBytes, &tm_do, bars.q_full(s),
@@ -666,7 +676,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t v[32];
                     tmem_ld32(tmem + lane_off + col + ch * 32, v);
                     tmem_wait_ld_into(v);
-                    if (key_ok) {
+                    const long long oe = static_cast<long long>(row_off) + ch * 32;
+                    if (key_ok && gb_index_ok(&g_bwd_error, oe, oe + 31,
+                                              static_cast<long long>(p.BH) * p.Nk * D)) {
                         float f[32];
 #pragma unroll
                         for (int c = 0; c < 32; ++c) f[c] = __uint_as_float(v[c]) * mul;
@@ -762,8 +774,11 @@ __global__ void __launch_bounds__(256) attn_bwd_dq_kernel(const float* __restric
         const int col = static_cast<int>(e % D);
         const long long bh = row / Nq;
         const int i = static_cast<int>(row % Nq);
-        const float4* src =
-            reinterpret_cast<const float4*>(dq_acc + (static_cast<size_t>(bh) * Nq_pad + i) * D + col);
+        const long long acc_e = (bh * Nq_pad + i) * D + col;
+        if (!gb_index_ok(&g_bwd_error, acc_e, acc_e + 7, n8 / Nq * Nq_pad * 8) ||
+            !gb_index_ok(&g_bwd_error, e, e + 7, n8 * 8))
+            continue;
+        const float4* src = reinterpret_cast<const float4*>(dq_acc + acc_e);
         const float4 a = src[0], b = src[1];
         const float f[8] = {a.x * scale, a.y * scale, a.z * scale, a.w * scale,
                             b.x * scale, b.y * scale, b.z * scale, b.w * scale};

@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kDecThreads)
     // of range is reported and gives the sequence no keys: o = 0, lse = -inf)
     int nk = p.Nk;
     if (p.seqlens_k) {
-        nk = p.seqlens_k[bh / p.H];
+        nk = gb_index_ok(&g_decode_error, bh / p.H, bh / p.H, p.BH / p.H) ? p.seqlens_k[bh / p.H] : 0;
         if (nk < 1 || nk > p.Nk) {
             if (threadIdx.x == 0) atomicOr(&g_decode_error, kErrBitLengths);
             nk = 0;
@@ -153,9 +153,13 @@ __global__ void __launch_bounds__(kDecThreads)
     const int ks = split * p.keys_per_split;
     const int ke = min(nk, ks + p.keys_per_split);
 
+    const long long n_kv = static_cast<long long>(p.BH) * p.Nk * D;  // elements of k, v
     float q[8];
     {
-        const uint4 qr = *reinterpret_cast<const uint4*>(p.q + static_cast<size_t>(bh) * D + sub * 8);
+        const long long qi = static_cast<long long>(bh) * D + sub * 8;
+        const uint4 qr = gb_index_ok(&g_decode_error, qi, qi + 7, static_cast<long long>(p.BH) * D)
+                             ? *reinterpret_cast<const uint4*>(p.q + qi)
+                             : make_uint4(0, 0, 0, 0);
         q[0] = bf_lo(qr.x); q[1] = bf_hi(qr.x); q[2] = bf_lo(qr.y); q[3] = bf_hi(qr.y);
         q[4] = bf_lo(qr.z); q[5] = bf_hi(qr.z); q[6] = bf_lo(qr.w); q[7] = bf_hi(qr.w);
         // fold scale * log2(e) into q once
@@ -175,7 +179,8 @@ __global__ void __launch_bounds__(kDecThreads)
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int j = base + u * kGroups + g;
-            if (j < ke) {
+            const long long e0 = (static_cast<long long>(bh) * p.Nk + j) * D + sub * 8;
+            if (j < ke && gb_index_ok(&g_decode_error, e0, e0 + 7, n_kv)) {
                 kr[u] = ld_stream(kbase + static_cast<size_t>(j) * D);
                 vr[u] = ld_stream(vbase + static_cast<size_t>(j) * D);
             } else {
@@ -235,12 +240,18 @@ __global__ void __launch_bounds__(kDecThreads)
         }
         const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
         if (p.splits == 1) {
-            p.o[static_cast<size_t>(bh) * D + c] = __float2bfloat16_rn(O * inv);
-            if (c == 0) p.lse[bh] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
+            const long long oi = static_cast<long long>(bh) * D + c;
+            if (gb_index_ok(&g_decode_error, oi, oi, static_cast<long long>(p.BH) * D))
+                p.o[oi] = __float2bfloat16_rn(O * inv);
+            if (c == 0 && gb_index_ok(&g_decode_error, bh, bh, p.BH))
+                p.lse[bh] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
         } else {
-            const size_t ps = static_cast<size_t>(bh) * p.splits + split;
-            p.part_o[ps * D + c] = O * inv;
-            if (c == 0) p.part_lse[ps] = Lsum > 0.f ? M + log2f(Lsum) : -INFINITY;
+            const long long ps = static_cast<long long>(bh) * p.splits + split;
+            const long long n_ps = static_cast<long long>(p.BH) * p.splits;
+            if (gb_index_ok(&g_decode_error, ps * D + c, ps * D + c, n_ps * D))
+                p.part_o[ps * D + c] = O * inv;
+            if (c == 0 && gb_index_ok(&g_decode_error, ps, ps, n_ps))
+                p.part_lse[ps] = Lsum > 0.f ? M + log2f(Lsum) : -INFINITY;
         }
     }
 }
@@ -274,10 +285,14 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     const int ks = split * p.keys_per_split;
     const int ke = min(p.Nk, ks + p.keys_per_split);
 
+    const long long n_kv = static_cast<long long>(p.BH) * p.Nk * D;  // codes of k8, v8
     float q[16];
     {
-        const uint4* qp = reinterpret_cast<const uint4*>(p.q + static_cast<size_t>(bh) * D + sub * 16);
-        const uint4 a = qp[0], b = qp[1];
+        const long long qi = static_cast<long long>(bh) * D + sub * 16;
+        const uint4* qp = reinterpret_cast<const uint4*>(p.q + qi);
+        const bool q_ok = gb_index_ok(&g_decode_error, qi, qi + 15, static_cast<long long>(p.BH) * D);
+        const uint4 a = q_ok ? qp[0] : make_uint4(0, 0, 0, 0);
+        const uint4 b = q_ok ? qp[1] : make_uint4(0, 0, 0, 0);
         const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -304,7 +319,10 @@ __global__ void __launch_bounds__(kDecThreads, 2)
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int j = base + u * kGroups + g;
-            if (j < ke) {
+            const long long e0 = (static_cast<long long>(bh) * p.Nk + j) * D + sub * 16;
+            const long long x0 = (static_cast<long long>(bh) * p.Nk + j) * kNb + sub / 2;
+            if (j < ke && gb_index_ok(&g_decode_error, e0, e0 + 15, n_kv) &&
+                gb_index_ok(&g_decode_error, x0, x0, n_kv / 32)) {
                 kr[u] = ld_stream(kbase + static_cast<size_t>(j) * D);
                 vr[u] = ld_stream(vbase + static_cast<size_t>(j) * D);
                 kx[u] = ld_stream_u8(ksbase + static_cast<size_t>(j) * kNb);
@@ -368,12 +386,18 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         }
         const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
         if (p.splits == 1) {
-            p.o[static_cast<size_t>(bh) * D + c] = __float2bfloat16_rn(O * inv);
-            if (c == 0) p.lse[bh] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
+            const long long oi = static_cast<long long>(bh) * D + c;
+            if (gb_index_ok(&g_decode_error, oi, oi, static_cast<long long>(p.BH) * D))
+                p.o[oi] = __float2bfloat16_rn(O * inv);
+            if (c == 0 && gb_index_ok(&g_decode_error, bh, bh, p.BH))
+                p.lse[bh] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
         } else {
-            const size_t ps = static_cast<size_t>(bh) * p.splits + split;
-            p.part_o[ps * D + c] = O * inv;
-            if (c == 0) p.part_lse[ps] = Lsum > 0.f ? M + log2f(Lsum) : -INFINITY;
+            const long long ps = static_cast<long long>(bh) * p.splits + split;
+            const long long n_ps = static_cast<long long>(p.BH) * p.splits;
+            if (gb_index_ok(&g_decode_error, ps * D + c, ps * D + c, n_ps * D))
+                p.part_o[ps * D + c] = O * inv;
+            if (c == 0 && gb_index_ok(&g_decode_error, ps, ps, n_ps))
+                p.part_lse[ps] = Lsum > 0.f ? M + log2f(Lsum) : -INFINITY;
         }
     }
 }
@@ -386,6 +410,11 @@ __global__ void __launch_bounds__(D) attn_fwd_decode_combine_kernel(DecodeParams
     const int c = threadIdx.x;
     const float* pl = p.part_lse + static_cast<size_t>(bh) * p.splits;
     const float* po = p.part_o + static_cast<size_t>(bh) * p.splits * D;
+    const long long n_ps = static_cast<long long>(p.BH) * p.splits;
+    const long long ps0 = static_cast<long long>(bh) * p.splits;
+    if (!gb_index_ok(&g_decode_error, ps0, ps0 + p.splits - 1, n_ps) ||
+        !gb_index_ok(&g_decode_error, bh, bh, p.BH))
+        return;
     float M = -INFINITY;
     for (int s = 0; s < p.splits; ++s) M = fmaxf(M, pl[s]);
     float Lsum = 0.f, O = 0.f;

@@ -562,6 +562,8 @@ const char* attn_status_string(int status) {
         case ATTN_ERR_MISALIGNED: return "ATTN_ERR_MISALIGNED: pointer not 16-byte aligned";
         case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: CUDA call failed";
         case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: kernel abandoned a barrier wait";
+        case ATTN_ERR_OUT_OF_RANGE:
+            return "ATTN_ERR_OUT_OF_RANGE: debug build skipped an access outside its buffer";
         default: return "unknown status";
     }
 }
@@ -569,9 +571,11 @@ const char* attn_status_string(int status) {
 int attn_device_error(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
     const unsigned e = read_and_clear_prefill_error() | read_and_clear_bwd_error() |
-                       read_and_clear_decode_error() | read_and_clear_selftest_error();
+                       read_and_clear_decode_error() | read_and_clear_selftest_error() |
+                       read_and_clear_merge_error();
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     if (e & kErrBitTimeout) return ATTN_ERR_TIMEOUT;
+    if (e & kErrBitBounds) return ATTN_ERR_OUT_OF_RANGE;
     return e ? ATTN_ERR_INVALID_ARG : ATTN_OK;
 }
 
@@ -579,6 +583,18 @@ int attn_version(void) { return kVersion; }
 
 int attn_selftest_timeout(void* stream) {
     return launch_selftest_timeout(static_cast<cudaStream_t>(stream));
+}
+
+int attn_selftest_bounds(void* stream) {
+    return launch_selftest_bounds(static_cast<cudaStream_t>(stream));
+}
+
+int attn_debug_build(void) {
+#ifdef GBATTN_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
 }
 
 }  // extern "C"

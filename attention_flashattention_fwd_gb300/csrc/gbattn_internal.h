@@ -110,6 +110,28 @@ unsigned read_and_clear_prefill_error();
 // Device error bits (shared by the kernels' error words)
 constexpr unsigned kErrBitTimeout = 1u;  // a bounded barrier wait ran out
 constexpr unsigned kErrBitLengths = 4u;  // a per-sequence length was out of range
+constexpr unsigned kErrBitBounds = 8u;   // debug builds: an out-of-range access was skipped
+
+// Debug builds (-DGBATTN_DEBUG: libgbattn_debug.so) check every direct global
+// memory access of the kernels -- the ones a TMA tensor map does not bound --
+// against its buffer: elements first .. last of an n-element buffer.  Out of
+// range, the kernel sets kErrBitBounds in its error word and skips the access
+// (attn_device_error reports ATTN_ERR_OUT_OF_RANGE); nothing traps.  Release
+// builds compile the check away.
+__device__ __forceinline__ bool gb_index_ok(unsigned int* err, long long first, long long last,
+                                            long long n) {
+#ifdef GBATTN_DEBUG
+    if (first >= 0 && last < n) return true;
+    atomicOr(err, kErrBitBounds);
+    return false;
+#else
+    (void)err;
+    (void)first;
+    (void)last;
+    (void)n;
+    return true;
+#endif
+}
 
 // decode_sm103.cu
 // Splits of each (b, h)'s keys for a device with num_sms SMs (at most
@@ -128,10 +150,13 @@ unsigned read_and_clear_decode_error();
 
 // selftest_sm103.cu
 int launch_selftest_timeout(cudaStream_t stream);
+// debug builds: a kernel whose index check fails on purpose (no access made)
+int launch_selftest_bounds(cudaStream_t stream);
 unsigned read_and_clear_selftest_error();
 
 // merge_sm103.cu
 int launch_merge(int d, const MergeParams& p, int num_sms, cudaStream_t stream);
+unsigned read_and_clear_merge_error();
 
 // backward_sm103.cu
 int bwd_set_attributes();

@@ -28,6 +28,8 @@
 
 namespace gbattn {
 
+__device__ unsigned int g_merge_error = 0;  // debug builds: kErrBitBounds
+
 namespace {
 
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
@@ -76,8 +78,10 @@ __device__ __forceinline__ void merge_unit(const MergeParams& p, long long g, co
     out.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
     out.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
     out.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-    *reinterpret_cast<uint4*>(p.o + row * D + c) = out;
-    if (c == 0) p.lse[row] = L > 0.f ? M + logf(L) : -INFINITY;
+    if (gb_index_ok(&g_merge_error, row * D + c, row * D + c + 7, p.rows * D))
+        *reinterpret_cast<uint4*>(p.o + row * D + c) = out;
+    if (c == 0 && gb_index_ok(&g_merge_error, row, row, p.rows))
+        p.lse[row] = L > 0.f ? M + logf(L) : -INFINITY;
 }
 
 // At most 4 parts: every load of two units (2 x 4 parts) in flight before any
@@ -103,9 +107,12 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeCtasPerSm)
             for (int s = 0; s < kParts; ++s) {
                 ls[u][s] = -INFINITY;
                 raw[u][s] = make_uint4(0u, 0u, 0u, 0u);
-                if (g < total && s < p.n_parts) {
-                    ls[u][s] = p.lse_parts[s * part_rows + row];
-                    raw[u][s] = ld_stream(p.o_parts + (s * part_rows + row) * D + c);
+                const long long pr = s * static_cast<long long>(part_rows) + row;
+                if (g < total && s < p.n_parts &&
+                    gb_index_ok(&g_merge_error, pr * D + c, pr * D + c + 7,
+                                p.n_parts * p.rows * D)) {
+                    ls[u][s] = p.lse_parts[pr];
+                    raw[u][s] = ld_stream(p.o_parts + pr * D + c);
                 }
             }
         }
@@ -138,9 +145,11 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeCtasPerSm) attn_merge_ker
                 const int s = s0 + b;
                 ls[b] = -INFINITY;
                 raw[b] = make_uint4(0u, 0u, 0u, 0u);
-                if (s < p.n_parts) {
-                    ls[b] = p.lse_parts[s * part_rows + row];
-                    raw[b] = ld_stream(p.o_parts + (s * part_rows + row) * D + c);
+                const long long pr = s * static_cast<long long>(part_rows) + row;
+                if (s < p.n_parts && gb_index_ok(&g_merge_error, pr * D + c, pr * D + c + 7,
+                                                 p.n_parts * p.rows * D)) {
+                    ls[b] = p.lse_parts[pr];
+                    raw[b] = ld_stream(p.o_parts + pr * D + c);
                 }
             }
 #pragma unroll
@@ -166,8 +175,10 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeCtasPerSm) attn_merge_ker
         out.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
         out.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
         out.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-        *reinterpret_cast<uint4*>(p.o + row * D + c) = out;
-        if (c == 0) p.lse[row] = L > 0.f ? M + logf(L) : -INFINITY;
+        if (gb_index_ok(&g_merge_error, row * D + c, row * D + c + 7, p.rows * D))
+            *reinterpret_cast<uint4*>(p.o + row * D + c) = out;
+        if (c == 0 && gb_index_ok(&g_merge_error, row, row, p.rows))
+            p.lse[row] = L > 0.f ? M + logf(L) : -INFINITY;
     }
 }
 
@@ -189,6 +200,13 @@ int launch_merge(int d, const MergeParams& p, int num_sms, cudaStream_t stream) 
     else
         launch_merge_d<64>(p, static_cast<unsigned>(blocks), stream);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+unsigned read_and_clear_merge_error() {
+    unsigned v = 0, zero = 0;
+    cudaMemcpyFromSymbol(&v, g_merge_error, sizeof v);
+    cudaMemcpyToSymbol(g_merge_error, &zero, sizeof zero);
+    return v;
 }
 
 }  // namespace gbattn

@@ -150,8 +150,9 @@ __device__ __forceinline__ Item item_at(const PrefillParams& p, int idx) {
     it.nk = p.Nk;
     if constexpr (kRagged) {
         const int b = it.bh / p.H;
-        if (p.seqlens_q) it.nq = p.seqlens_q[b];
-        if (p.seqlens_k) it.nk = p.seqlens_k[b];
+        const bool b_ok = gb_index_ok(&g_prefill_error, b, b, p.BH / p.H);
+        if (p.seqlens_q) it.nq = b_ok ? p.seqlens_q[b] : 0;
+        if (p.seqlens_k) it.nk = b_ok ? p.seqlens_k[b] : 0;
         if (it.nq < 1 || it.nq > p.Nq || it.nk < 1 || it.nk > p.Nk || (p.causal && it.nq > it.nk)) {
             atomicOr(&g_prefill_error, kErrBitLengths);  // the sequence is skipped
             it.nq = 0;  // skip the sequence
@@ -686,7 +687,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t o[32];
                     tmem_ld32(tO + ch * 32, o);
                     tmem_wait_ld();
-                    if (row < it.nq) {
+                    const long long oi = (static_cast<long long>(it.bh) * p.Nq + row) * D + ch * 32;
+                    if (row < it.nq && gb_index_ok(&g_prefill_error, oi, oi + 31,
+                                                   static_cast<long long>(p.BH) * p.Nq * D)) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int c = 0; c < 16; ++c)
@@ -743,7 +746,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // O_t has been read (each load above was waited for): the MMA thread
             // learns it from this warp's next p_ready arrival, which follows
-            if (row < it.nq)
+            if (row < it.nq && gb_index_ok(&g_prefill_error,
+                                           static_cast<long long>(it.bh) * p.Nq + row,
+                                           static_cast<long long>(it.bh) * p.Nq + row,
+                                           static_cast<long long>(p.BH) * p.Nq))
                 p.lse[static_cast<size_t>(it.bh) * p.Nq + row] =
                     (m_ref + log2f(l)) * 0.69314718055994530942f;
             ++kp;

@@ -24,6 +24,24 @@ __global__ void attn_selftest_timeout_kernel() {
     if (!mbar_wait(b, 0)) atomicOr(&g_selftest_error, kErrBitTimeout);  // nothing arrives
 }
 
+// The index check of the debug builds on an index one past the end of a
+// one-element buffer: the check fails, sets kErrBitBounds and the kernel makes
+// no access at all (in either build: the access is not written).
+__global__ void attn_selftest_bounds_kernel(long long n) {
+    if (threadIdx.x != 0) return;
+    (void)gb_index_ok(&g_selftest_error, n, n, n);
+}
+
+int launch_selftest_bounds(cudaStream_t stream) {
+#ifdef GBATTN_DEBUG
+    attn_selftest_bounds_kernel<<<1, 32, 0, stream>>>(1);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+#else
+    (void)stream;
+    return ATTN_ERR_UNSUPPORTED;  // release builds carry no index checks
+#endif
+}
+
 int launch_selftest_timeout(cudaStream_t stream) {
     attn_selftest_timeout_kernel<<<1, 32, 0, stream>>>();
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;

@@ -56,9 +56,12 @@ typedef enum {
                                   sizes beyond the index range of the kernels */
     ATTN_ERR_MISALIGNED = 3,   /* a device pointer is not 16-byte aligned */
     ATTN_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
-    ATTN_ERR_TIMEOUT = 5       /* a kernel gave up waiting on one of its own
+    ATTN_ERR_TIMEOUT = 5,      /* a kernel gave up waiting on one of its own
                                   pipeline barriers (reported by
                                   attn_device_error, never by a launch) */
+    ATTN_ERR_OUT_OF_RANGE = 6  /* debug builds only: a kernel found an index
+                                  outside its buffer and skipped the access (a
+                                  library bug; reported by attn_device_error) */
 } attn_status_t;
 
 /*
@@ -389,6 +392,24 @@ int attn_version(void);
  * faults; the context stays usable.  Returns ATTN_OK or ATTN_ERR_CUDA.
  */
 int attn_selftest_timeout(void *stream);
+
+/*
+ * Debug builds.  The library also builds as libgbattn_debug.so (compiled with
+ * GBATTN_DEBUG), whose kernels check the index of every direct global-memory
+ * access (those a TMA tensor map does not bound) against its buffer; an index
+ * out of range sets a bit of the device error word and the access is skipped,
+ * so attn_device_error returns ATTN_ERR_OUT_OF_RANGE instead of the kernel
+ * touching memory it does not own.  Nothing traps.  The lecture pages have no
+ * counterpart; this is the library's own stand-in for a memory checker.
+ *
+ * attn_debug_build -- 1 in the debug build, 0 in the release build.
+ * attn_selftest_bounds -- debug builds: enqueue a kernel whose index check
+ * fails on purpose (it makes no access); the next attn_device_error returns
+ * ATTN_ERR_OUT_OF_RANGE and clears it.  Release builds return
+ * ATTN_ERR_UNSUPPORTED and enqueue nothing.
+ */
+int attn_debug_build(void);
+int attn_selftest_bounds(void *stream);
 
 #ifdef __cplusplus
 }

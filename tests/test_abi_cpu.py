@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_version_and_status_strings(lib):
     assert lib.attn_version() >= 100
-    for st in range(6):
+    for st in range(7):
         assert binding.status_string(st).startswith("ATTN_")
     assert binding.status_string(99) == "unknown status"
 
@@ -217,3 +217,23 @@ def test_fp8_entry_point_rejects_before_launch(lib):
     assert f8(Nk=120) == UNSUPPORTED                        # V^T rows of 120 bytes
     assert f8(causal=1, Nq=256, Nk=128) == UNSUPPORTED
     assert f8(vt=FAKE + 8) == MISALIGNED and f8(o=FAKE + 2) == MISALIGNED
+
+
+def test_release_and_debug_builds_identify_themselves(lib):
+    """attn_debug_build tells the builds apart; the release build has no index
+    checks, so its bounds self-test is refused before any CUDA call."""
+    import ctypes as C
+    import os
+    from attention_flashattention_fwd_gb300 import build_lib
+    lib.attn_debug_build.restype = C.c_int
+    lib.attn_selftest_bounds.argtypes = [C.c_void_p]
+    lib.attn_selftest_bounds.restype = C.c_int
+    if not binding.LIB_PATH.endswith("_debug.so"):
+        assert lib.attn_debug_build() == 0
+        assert lib.attn_selftest_bounds(C.c_void_p(0)) == UNSUPPORTED
+    build_lib.build(debug=True)
+    dbg = C.CDLL(build_lib.LIB_DEBUG)
+    dbg.attn_debug_build.restype = C.c_int
+    assert dbg.attn_debug_build() == 1
+    for name in declared_functions():
+        assert hasattr(dbg, name), f"libgbattn_debug.so does not export {name}"
