@@ -93,29 +93,31 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t code) {
     return __uint_as_float(code == 0u ? 0x00400000u : code == 255u ? 0x7fc00000u : code << 23);
 }
 
-// sum over 16 E4M3 codes (a uint4) of q[c] * value(code c)
-__device__ __forceinline__ float dot16_e4m3(const float (&q)[16], uint4 k) {
+// sum over 16 E4M3 codes (a uint4) of q[c] * value(code c), two lanes of
+// work per instruction (packed fp32 FMA on (even, odd) element pairs)
+__device__ __forceinline__ float dot16_e4m3(const float2 (&q)[8], uint4 k) {
     const uint32_t w[4] = {k.x, k.y, k.z, k.w};
-    float s = 0.f;
+    float2 s = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         float f[4];
         e4m3x4_to_f32(w[i], f);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) s = fmaf(q[4 * i + e], f[e], s);
+        s = ffma2(q[2 * i], make_float2(f[0], f[1]), s);
+        s = ffma2(q[2 * i + 1], make_float2(f[2], f[3]), s);
     }
-    return s;
+    return s.x + s.y;
 }
 
-// acc[c] += p * value(code c) over 16 E4M3 codes
-__device__ __forceinline__ void axpy16_e4m3(float (&acc)[16], float p, uint4 v) {
+// acc[c] += p * value(code c) over 16 E4M3 codes, acc as (even, odd) pairs
+__device__ __forceinline__ void axpy16_e4m3(float2 (&acc)[8], float p, uint4 v) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const float2 p2 = make_float2(p, p);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         float f[4];
         e4m3x4_to_f32(w[i], f);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[4 * i + e] = fmaf(p, f[e], acc[4 * i + e]);
+        acc[2 * i] = ffma2(p2, make_float2(f[0], f[1]), acc[2 * i]);
+        acc[2 * i + 1] = ffma2(p2, make_float2(f[2], f[3]), acc[2 * i + 1]);
     }
 }
 
@@ -286,7 +288,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     const int ke = min(p.Nk, ks + p.keys_per_split);
 
     const long long n_kv = static_cast<long long>(p.BH) * p.Nk * D;  // codes of k8, v8
-    float q[16];
+    float2 q[8];  // the lane's 16 elements as (even, odd) pairs
     {
         const long long qi = static_cast<long long>(bh) * D + sub * 16;
         const uint4* qp = reinterpret_cast<const uint4*>(p.q + qi);
@@ -295,11 +297,8 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         const uint4 b = q_ok ? qp[1] : make_uint4(0, 0, 0, 0);
         const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            // fold scale * log2(e) into q once
-            q[2 * i] = bf_lo(w[i]) * p.scale_log2;
-            q[2 * i + 1] = bf_hi(w[i]) * p.scale_log2;
-        }
+        for (int i = 0; i < 8; ++i)  // fold scale * log2(e) into q once
+            q[i] = make_float2(bf_lo(w[i]) * p.scale_log2, bf_hi(w[i]) * p.scale_log2);
     }
     const uint8_t* k8 = reinterpret_cast<const uint8_t*>(p.k);
     const uint8_t* v8 = reinterpret_cast<const uint8_t*>(p.v);
@@ -309,9 +308,9 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     const uint8_t* vsbase = p.v_scale + static_cast<size_t>(bh) * p.Nk * kNb + sub / 2;
 
     float m = -INFINITY, l = 0.f;
-    float acc[16];
+    float2 acc[8];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+    for (int e = 0; e < 8; ++e) acc[e] = make_float2(0.f, 0.f);
 
     for (int base = ks; base < ke; base += kGroups * kUnroll) {
         uint4 kr[kUnroll], vr[kUnroll];
@@ -352,7 +351,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         const float alpha = ex2_approx(m - mx);  // m = -inf on the first visit gives 0
         l *= alpha;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) acc[e] *= alpha;
+        for (int e = 0; e < 8; ++e) acc[e] = make_float2(acc[e].x * alpha, acc[e].y * alpha);
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const float pu = ex2_approx(s[u] - mx);
@@ -364,7 +363,10 @@ __global__ void __launch_bounds__(kDecThreads, 2)
 
     // ---- merge the lane groups of the CTA (as in the bf16 kernel)
 #pragma unroll
-    for (int e = 0; e < 16; ++e) sm_acc[g][sub * 16 + e] = acc[e];
+    for (int e = 0; e < 8; ++e) {
+        sm_acc[g][sub * 16 + 2 * e] = acc[e].x;
+        sm_acc[g][sub * 16 + 2 * e + 1] = acc[e].y;
+    }
     if (sub == 0) {
         sm_m[g] = m;
         sm_l[g] = l;
