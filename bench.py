@@ -57,9 +57,11 @@ def parse_args():
                     help="run only this workload's kernel(s) (profiling runs); prints its time")
     ap.add_argument("--shape", default=None,
                     help="with --case custom: B,H,Nq,Nk,d,causal of a profiling workload")
-    ap.add_argument("--pass", dest="which", choices=["fwd", "bwd", "fp8", "mx"], default="fwd",
+    ap.add_argument("--pass", dest="which", choices=["fwd", "bwd", "fp8", "mx", "merge"],
+                    default="fwd",
                     help="with --case: time the forward (default), the backward call, the "
-                         "forward on FP8 (E4M3) operands or (decode) MXFP8 keys and values")
+                         "forward on FP8 (E4M3) operands, (decode) MXFP8 keys and values, or "
+                         "attn_merge of 4 shard results of the workload's shape")
     a = ap.parse_args()
     a.warmup = max(3, a.warmup)
     a.steps = max(1, a.steps)
@@ -350,6 +352,17 @@ def run_case(args):
         def launch():  # noqa: F811  (the timed call is the backward)
             binding.attn_bwd(q, k, v, o, lse, dout, causal=w.causal, scale=w.scale, dq=dq, dk=dk,
                              dv=dv, workspace=bws)
+    elif args.which == "merge":
+        if w.decode:
+            raise SystemExit("--pass merge needs a prefill workload")
+        launch()  # o, lse of these inputs, as the shards' results
+        o_parts = torch.stack([o] * MERGE_PARTS).contiguous()
+        l_parts = torch.stack([lse - float(s) for s in range(MERGE_PARTS)]).contiguous()
+        om, lm = torch.empty_like(o), torch.empty_like(lse)
+        merge_bytes = (MERGE_PARTS + 1) * (o.nbytes + lse.nbytes)
+
+        def launch():  # noqa: F811  (the timed call is the merge)
+            binding.attn_merge(o_parts, l_parts, out=om, lse=lm)
     elif args.which == "mx":
         if not w.decode:
             raise SystemExit("--pass mx needs a decode workload")
@@ -387,6 +400,8 @@ def run_case(args):
         raise RuntimeError("a kernel reported a device-side error")
     if args.which == "mx":
         val = (mx_bytes / ms / 1e6, "GB/s")
+    elif args.which == "merge":
+        val = (merge_bytes / ms / 1e6, "GB/s")
     else:
         val = (w.algorithmic_bytes() / ms / 1e6, "GB/s") if w.decode else (
         flop_ratio * w.flops() / ms / 1e9, "TFLOP/s")
