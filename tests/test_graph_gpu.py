@@ -15,7 +15,7 @@ import torch
 
 import oracle
 from attention_flashattention_fwd_gb300 import binding
-from attention_flashattention_fwd_gb300.inputs import bf16_bits, make_qkv, make_qkv_fp8
+from attention_flashattention_fwd_gb300.inputs import bf16_bits, make_qkv, make_qkv_fp8, make_qkv_mx
 from tests.conftest import nan_full
 
 pytestmark = pytest.mark.gpu
@@ -42,6 +42,9 @@ def _fill(bufs, seed):
     bufs["vt8"].copy_(vt8.view(torch.uint8))
     g = torch.Generator(device="cpu").manual_seed(seed + 2)
     bufs["dout"].copy_(torch.randn(B, H, NQ, D, generator=g).to(torch.bfloat16))
+    _, kx, ksx, vx, vsx = make_qkv_mx(B, H, NK, D, seed=seed + 3, device=dev)
+    for n, t in (("kx", kx), ("ksx", ksx), ("vx", vx), ("vsx", vsx)):
+        bufs[n].copy_(t)
 
 
 def _buffers(dev):
@@ -55,6 +58,9 @@ def _buffers(dev):
         "qd": z((B, H, 1, D), bf),
         "q8": z((B, H, NQ, D), u8), "k8": z((B, H, NK, D), u8), "vt8": z((B, H, D, NK), u8),
         "dout": z((B, H, NQ, D), bf),
+        "kx": z((B, H, NK, D), u8), "ksx": z((B, H, NK, D // 32), u8),
+        "vx": z((B, H, NK, D), u8), "vsx": z((B, H, NK, D // 32), u8),
+        "ox": z((B, H, 1, D), bf), "lx": z((B, H, 1), f32),
         # outputs
         "o": z((B, H, NQ, D), bf), "lse": z((B, H, NQ), f32),
         "o8": z((B, H, NQ, D), bf), "lse8": z((B, H, NQ), f32),
@@ -67,12 +73,13 @@ def _buffers(dev):
     }
 
 
-OUTPUTS = ("o", "lse", "o8", "lse8", "op", "lp", "om", "lm", "od", "ld", "dk", "dv")
+OUTPUTS = ("o", "lse", "o8", "lse8", "op", "lp", "om", "lm", "od", "ld", "ox", "lx", "dk", "dv")
 
 
 def _step(b):
     """One pass over the entry points: causal prefill, FP8 prefill, two key
-    shards merged, one decode row, and the backward of the causal prefill."""
+    shards merged, one decode row (bf16 and MXFP8 keys and values), and the
+    backward of the causal prefill."""
     binding.attn_fwd(b["q"], b["k"], b["v"], causal=True, out=b["o"], lse=b["lse"])
     binding.attn_fwd_fp8(b["q8"], b["k8"], b["vt8"], 0.05, 0.05, 0.05, causal=True,
                          out=b["o8"], lse=b["lse8"])
@@ -81,6 +88,8 @@ def _step(b):
     binding.attn_merge(b["op"], b["lp"], out=b["om"], lse=b["lm"])
     binding.attn_fwd_decode(b["qd"], b["k"], b["v"], out=b["od"], lse=b["ld"],
                             workspace=b["ws_dec"])
+    binding.attn_fwd_decode_mx(b["qd"], b["kx"], b["ksx"], b["vx"], b["vsx"], out=b["ox"],
+                               lse=b["lx"], workspace=b["ws_dec"])
     binding.attn_bwd(b["q"], b["k"], b["v"], o=b["o"], lse=b["lse"], dout=b["dout"],
                      causal=True, dq=b["dq"], dk=b["dk"], dv=b["dv"], workspace=b["ws_bwd"])
 
