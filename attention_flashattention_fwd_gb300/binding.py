@@ -85,6 +85,10 @@ def _configure():
     lib.attn_selftest_bounds.restype = I
     lib.attn_debug_build.argtypes = []
     lib.attn_debug_build.restype = I
+    lib.attn_pair_product.argtypes = [P, P, P, P]
+    lib.attn_pair_product.restype = I
+    lib.attn_bench_mma_rate.argtypes = [I, I, I, I, I, P, P, P, P]
+    lib.attn_bench_mma_rate.restype = I
     return lib
 
 
@@ -425,3 +429,35 @@ def attn_bwd(q, k, v, o, lse, dout, causal=False, scale=None, dq=None, dk=None, 
 def device_error() -> int:
     """Synchronise and read/clear the kernels' device error word (0 = none)."""
     return int(load().attn_device_error())
+
+
+def attn_pair_product(a, b, d=None, stream=None):
+    """D = A Bᵀ through the CTA-pair product (``attn_pair_product``): a is a
+    256 x 64 and b a 128 x 64 bfloat16 CUDA tensor; returns the 256 x 128
+    float32 D.  Blocks until the product is done."""
+    for name, t, shape in (("a", a, (256, 64)), ("b", b, (128, 64))):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or tuple(t.shape) != shape \
+                or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bfloat16 CUDA tensor of shape {shape}")
+    if b.device != a.device:
+        raise ValueError("a and b must be on the same device")
+    with _on(a.device, stream):
+        d = _out(d, (256, 128), torch.float32, a.device, "d")
+        _check(load().attn_pair_product(_ptr(a), _ptr(b), _ptr(d), _stream_ptr(stream)),
+               "attn_pair_product")
+    return d
+
+
+def bench_mma_rate(form, busy=0, waits=0, steps=4096, reps=5, device=None, stream=None):
+    """Time one issuing thread's products (``attn_bench_mma_rate``): form 1 is
+    the single-CTA 128 x 128 x 16 product, form 2 the CTA-pair 256 x 128 x 16
+    one.  Returns {"ms": mean launch time, "cycles": mean issuing-thread
+    cycles, "sms": SMs used}."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    ms, cyc, sms = ctypes.c_float(), ctypes.c_double(), ctypes.c_int()
+    with _on(dev, stream):
+        _check(load().attn_bench_mma_rate(int(form), int(busy), int(waits), int(steps), int(reps),
+                                          ctypes.byref(ms), ctypes.byref(cyc), ctypes.byref(sms),
+                                          _stream_ptr(stream)),
+               "attn_bench_mma_rate")
+    return {"ms": ms.value, "cycles": cyc.value, "sms": sms.value}

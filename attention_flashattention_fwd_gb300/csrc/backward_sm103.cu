@@ -125,6 +125,13 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
     }
 }
 
+// The same wait run by every lane of the MMA warp, its result made
+// warp-uniform so that no lane leaves the warp's loops alone.
+__device__ __forceinline__ bool wait_uniform(uint32_t bar, uint32_t parity,
+                                             volatile int* abort_flag) {
+    return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag));
+}
+
 // Wait for this thread's Tensor Memory loads into `a` and `b`; the registers
 // are tied to the wait so no use of them can be scheduled before it.
 __device__ __forceinline__ void tmem_wait_ld_into(uint32_t (&a)[32], uint32_t (&b)[32]) {
@@ -459,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // them, S^T(i+1) in the S^T columns after the dV product has read P^T
         // (one thread's MMAs run in issue order); only dP^T(i+1) waits for the
         // dQ warpgroup to have taken dQ_i.
-        if (lane == 0) {
+        {  // the whole warp; elect_one() issues
             const uint32_t id_s = umma_idesc_bf16(kTile, kTile, false);  // both K-major
             const uint32_t id_acc = umma_idesc_bf16(kTile, D, true);     // B MN-major
             const uint32_t id_dq = idesc_bf16_a_mn(kTile, D);            // A and B MN-major
@@ -476,62 +483,77 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 umma_commit(bars.s_full());
             };
-            bool ok = wait_or_abort(bars.kv_full(), 0, abort_flag) &&
-                      wait_or_abort(bars.q_full(0), 0, abort_flag);
+            bool ok = wait_uniform(bars.kv_full(), 0, abort_flag) &&
+                      wait_uniform(bars.q_full(0), 0, abort_flag);
             if (ok) {
                 tc_fence_after();
-                issue_s(0);
+                if (elect_one()) issue_s(0);
+                __syncwarp();
             }
             for (int it = 0; it < n_iter && ok; ++it) {
                 const int s = it & 1;
-                if (it > 0 && !(ok = wait_or_abort(bars.dq_free(), (it - 1) & 1, abort_flag)))
+                if (it > 0 && !(ok = wait_uniform(bars.dq_free(), (it - 1) & 1, abort_flag)))
                     break;
                 tc_fence_after();
                 const uint32_t sq = sRing + s * 2 * C::kTileBytes;
                 const uint32_t sdo = sq + C::kTileBytes;
                 const uint64_t ddo_k = umma_desc_sw128(sdo, 16, 1024);
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V_j dO_i^T
-                    const uint32_t off = ((kk >> 2) * C::kSubBytes + (kk & 3) * 32) >> 4;
-                    umma_ss(tmem + C::kColDP, dv_k + off, ddo_k + off, id_s, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V_j dO_i^T
+                        const uint32_t off = ((kk >> 2) * C::kSubBytes + (kk & 3) * 32) >> 4;
+                        umma_ss(tmem + C::kColDP, dv_k + off, ddo_k + off, id_s, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(bars.dp_full());
                 }
-                umma_commit(bars.dp_full());
+                __syncwarp();
                 const uint64_t dq_mn = umma_desc_sw128(sq, C::kSubBytes, 1024);
                 const uint64_t ddo_mn = umma_desc_sw128(sdo, C::kSubBytes, 1024);
                 // K = 128 queries in steps of 16: 8 packed P / dS columns, 16 rows of 128 B
-                if (!(ok = wait_or_abort(bars.pa_ready(), it & 1, abort_flag))) break;
+                if (!(ok = wait_uniform(bars.pa_ready(), it & 1, abort_flag))) break;
                 tc_fence_after();
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)
-                    umma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8, ddo_mn + ((kk * 2048) >> 4),
-                            id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kTile / 16; ++kk)
+                        umma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8,
+                                ddo_mn + ((kk * 2048) >> 4), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+                }
+                __syncwarp();
                 // S^T(i+1) right behind the dV product that read P^T(i): the key-row
                 // warps start on it as soon as they are done with dS(i)
                 if (it + 1 < n_iter) {
-                    if (!(ok = wait_or_abort(bars.q_full((it + 1) & 1), ((it + 1) >> 1) & 1,
-                                             abort_flag)))
+                    if (!(ok = wait_uniform(bars.q_full((it + 1) & 1), ((it + 1) >> 1) & 1,
+                                            abort_flag)))
                         break;
                     tc_fence_after();
-                    issue_s(it + 1);
+                    if (elect_one()) issue_s(it + 1);
+                    __syncwarp();
                 }
-                if (!(ok = wait_or_abort(bars.pb_tmem(), it & 1, abort_flag))) break;
+                if (!(ok = wait_uniform(bars.pb_tmem(), it & 1, abort_flag))) break;
                 tc_fence_after();
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)
-                    umma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8, dq_mn + ((kk * 2048) >> 4),
-                            id_acc, (it > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(bars.q_empty(s));
-                if (!(ok = wait_or_abort(bars.pb_smem(), it & 1, abort_flag))) break;
+                    for (int kk = 0; kk < kTile / 16; ++kk)
+                        umma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8,
+                                dq_mn + ((kk * 2048) >> 4), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(bars.q_empty(s));
+                }
+                __syncwarp();
+                if (!(ok = wait_uniform(bars.pb_smem(), it & 1, abort_flag))) break;
                 tc_fence_after();
-                // K = 128 keys in steps of 16 rows of the dS and K_j tiles
+                if (elect_one()) {
+                    // K = 128 keys in steps of 16 rows of the dS and K_j tiles
 #pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)
-                    umma_ss(tmem + C::kColDQ, dds_mn + ((kk * 2048) >> 4), dk_mn + ((kk * 2048) >> 4),
-                            id_dq, kk > 0 ? 1u : 0u);
-                umma_commit(bars.dq_full());
+                    for (int kk = 0; kk < kTile / 16; ++kk)
+                        umma_ss(tmem + C::kColDQ, dds_mn + ((kk * 2048) >> 4),
+                                dk_mn + ((kk * 2048) >> 4), id_dq, kk > 0 ? 1u : 0u);
+                    umma_commit(bars.dq_full());
+                }
+                __syncwarp();
             }
-            // every MMA this thread issued has completed once `done` flips
-            umma_commit(bars.done());
+            // every MMA the elected lane issued has completed once `done` flips
+            if (elect_one()) umma_commit(bars.done());
+            __syncwarp();
             mbar_wait(bars.done(), 0);
         }
         __syncwarp();

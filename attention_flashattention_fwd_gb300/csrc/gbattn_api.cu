@@ -589,6 +589,21 @@ int attn_selftest_bounds(void* stream) {
     return launch_selftest_bounds(static_cast<cudaStream_t>(stream));
 }
 
+int attn_pair_product(const void* a, const void* b, float* d, void* stream) {
+    if (!a || !b || !d) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(d)) return ATTN_ERR_MISALIGNED;
+    return launch_pair_product(a, b, d, static_cast<cudaStream_t>(stream));
+}
+
+int attn_bench_mma_rate(int form, int busy, int waits, int steps, int reps, float* ms_out,
+                        double* cycles_out, int* sms_out, void* stream) {
+    if ((form != 1 && form != 2) || (busy != 0 && busy != 1) || (waits != 0 && waits != 1) ||
+        steps < 1 || steps > (1 << 16) || reps < 1 || reps > 1000 || !ms_out)
+        return ATTN_ERR_INVALID_ARG;
+    return run_mma_rate(form, busy, waits, steps, reps, ms_out, cycles_out, sms_out,
+                        static_cast<cudaStream_t>(stream));
+}
+
 int attn_debug_build(void) {
 #ifdef GBATTN_DEBUG
     return 1;

@@ -112,6 +112,20 @@ constexpr unsigned kErrBitTimeout = 1u;  // a bounded barrier wait ran out
 constexpr unsigned kErrBitLengths = 4u;  // a per-sequence length was out of range
 constexpr unsigned kErrBitBounds = 8u;   // debug builds: an out-of-range access was skipped
 
+// One lane of a converged warp: elect.sync picks the same lane for the same
+// member mask every time, so the lane that issues a group of tcgen05.mma
+// products also issues every commit that tracks them.  The kernels' MMA warps
+// run their loops and barrier waits with all 32 lanes and issue from the
+// elected one: a lone issuing lane whose loop holds barrier waits issues every
+// product markedly slower (attn_bench_mma_rate measures both forms).
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // Debug builds (-DGBATTN_DEBUG: libgbattn_debug.so) check every direct global
 // memory access of the kernels -- the ones a TMA tensor map does not bound --
 // against its buffer: elements first .. last of an n-element buffer.  Out of
@@ -153,6 +167,12 @@ int launch_selftest_timeout(cudaStream_t stream);
 // debug builds: a kernel whose index check fails on purpose (no access made)
 int launch_selftest_bounds(cudaStream_t stream);
 unsigned read_and_clear_selftest_error();
+
+// mma_pair_sm103.cu: the cta_group::2 product checked and timed against the
+// single-CTA form (blocking calls; each synchronises `stream`)
+int launch_pair_product(const void* a, const void* b, float* d, cudaStream_t stream);
+int run_mma_rate(int form, int busy, int waits, int steps, int reps, float* ms_out,
+                 double* cycles_out, int* sms_out, cudaStream_t stream);
 
 // merge_sm103.cu
 int launch_merge(int d, const MergeParams& p, int num_sms, cudaStream_t stream);

@@ -234,6 +234,14 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
     }
 }
 
+// The same wait run by every lane of the MMA warp, its result made
+// warp-uniform so that no lane leaves the warp's loops alone (a lane whose wait
+// ran out takes the whole warp with it).
+__device__ __forceinline__ bool wait_uniform(uint32_t bar, uint32_t parity,
+                                             volatile int* abort_flag) {
+    return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag));
+}
+
 }  // namespace
 
 // kRagged: per-sequence lengths (seqlens_q / seqlens_k) are read; the
@@ -375,7 +383,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // product takes to run, so ring slots are released by the softmax of
         // tile 1 instead (see there) and P V completion is only committed at
         // the end of an item.
-        if (lane == 0) {
+        // The whole warp runs this loop and every barrier wait; one elected lane
+        // (elect_one) issues each group of products with its commits.
+        {
             const uint32_t idesc_qk =
                 kFp8 ? umma_idesc_e4m3(kBM, kBN) : umma_idesc_bf16(kBM, kBN, false);
             const uint32_t idesc_pv =
@@ -383,8 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int u = 0;             // ring use of the current K tile
             int iter[2] = {0, 0};  // key tiles processed per query tile, over all items
             auto wait_use = [&](int use) {
-                return wait_or_abort(bars.full(use % C::kSlots), (use / C::kSlots) & 1,
-                                     abort_flag);
+                return wait_uniform(bars.full(use % C::kSlots), (use / C::kSlots) & 1,
+                                    abort_flag);
             };
             // Descriptors are built once; the k-steps only move the start address
             // (bits 0-13 of the low word, in 16-byte units), which never carries.
@@ -441,12 +451,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // (a single-tile item has no tile 1)
                 for (int t = 0; t < 2 && ok; ++t) {
                     if (it.n_kv(t) == 0) continue;
-                    ok = wait_or_abort(bars.q_full(t), kq[t]++ & 1, abort_flag) &&
+                    ok = wait_uniform(bars.q_full(t), kq[t]++ & 1, abort_flag) &&
                          (t == 1 || wait_use(u));
                     if (!ok) break;
                     tc_fence_after();
-                    issue_s(t, u);  // n_kv0 >= 1
-                    if (it.n_kv(t) == 1) umma_commit(bars.q_empty(t));
+                    if (elect_one()) {
+                        issue_s(t, u);  // n_kv0 >= 1
+                        if (it.n_kv(t) == 1) umma_commit(bars.q_empty(t));
+                    }
+                    __syncwarp();
                 }
                 if (!ok) break;
                 for (int j = 0; j < nmax && ok; ++j) {
@@ -457,23 +470,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // shared memory (the relay warp's arrival) and, at j = 0, the
                         // previous item's O_t read by its epilogue (the softmax warps
                         // arrive here only after their epilogue's loads completed)
-                        if (!(ok = wait_or_abort(bars.p_ready(t), iter[t] & 1, abort_flag)))
+                        if (!(ok = wait_uniform(bars.p_ready(t), iter[t] & 1, abort_flag)))
                             break;
                         tc_fence_after();
-                        issue_pv(t, uv, j == 0);
-                        ++iter[t];
-                        if (j + 1 < it.n_kv(t)) {
-                            issue_s(t, uk);
-                            if (j + 2 == it.n_kv(t)) umma_commit(bars.q_empty(t));
-                        } else {
-                            umma_commit(bars.pv_done(t));  // O_t of this item is complete
+                        if (elect_one()) {
+                            issue_pv(t, uv, j == 0);
+                            if (j + 1 < it.n_kv(t)) {
+                                issue_s(t, uk);
+                                if (j + 2 == it.n_kv(t)) umma_commit(bars.q_empty(t));
+                            } else {
+                                umma_commit(bars.pv_done(t));  // O_t of this item is complete
+                            }
                         }
+                        __syncwarp();
+                        ++iter[t];
                     }
                     u += 2;
                 }
             }
             // every MMA this thread issued has completed once `fin` flips
-            umma_commit(bars.fin);
+            if (elect_one()) umma_commit(bars.fin);
+            __syncwarp();
             mbar_wait(bars.fin, 0);
         }
         __syncwarp();

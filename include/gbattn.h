@@ -411,6 +411,45 @@ int attn_selftest_timeout(void *stream);
 int attn_debug_build(void);
 int attn_selftest_bounds(void *stream);
 
+/*
+ * The CTA-pair product (PDC Lecture 7 §7.13, CTA pair / MMA.2SM): one thread
+ * issues tcgen05.mma.cta_group::2 for a cluster of two CTAs on two SMs, M = 256
+ * rows of which each CTA holds 128 in its shared memory and receives 128 in its
+ * Tensor Memory, while B's N rows are split N/2 per CTA.  The attention kernels
+ * use the single-CTA form; these two calls check the pair form and measure both
+ * forms' issue rates.  Both block: they synchronise `stream` before returning.
+ *
+ * attn_pair_product -- D = A · Bᵀ through four pair products (K = 64 in steps
+ * of 16).  a: 256 x 64 bf16, b: 128 x 64 bf16, d: 256 x 128 fp32, all
+ * row-major device buffers owned by the caller, 16-byte aligned.  Returns
+ * ATTN_OK, ATTN_ERR_INVALID_ARG (a null pointer), ATTN_ERR_MISALIGNED,
+ * ATTN_ERR_CUDA, or ATTN_ERR_TIMEOUT (a bounded wait ran out; d is then not
+ * valid).
+ *
+ * attn_bench_mma_rate -- the sustained rate of one issuing thread.
+ *   form   1: each CTA issues 128 x 128 x 16 bf16 products (cta_group::1);
+ *          2: the even CTA of each pair issues 256 x 128 x 16 products
+ *             (cta_group::2).  Either way every product keeps each SM's
+ *             tensor core busy for 64 cycles, and both forms run on the same
+ *             SMs: as many CTA pairs as the device holds at once (sms_out
+ *             receives how many SMs that is).
+ *   busy   0: the issuing thread runs alone; 1: eight more warps per CTA (two
+ *          on each SM sub-partition, where the attention kernels' softmax
+ *          warps sit) loop over Tensor Memory loads, packed FMAs, exponentials
+ *          and bf16 packs until the products are done.
+ *   waits  0: a commit after every 8 products, no wait until the last;
+ *          1: after issuing group s, wait for group s-1 to complete.
+ *   steps  groups of 8 products per issuing thread, 1 to 65536.
+ *   reps   timed launches (after one untimed), 1 to 1000.
+ *   ms_out (host) mean launch time by CUDA events; cycles_out (host, may be
+ *   NULL) mean clock64 cycles of an issuing thread from its first product to
+ *   the completion of its last; sms_out (host, may be NULL).
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_CUDA or ATTN_ERR_TIMEOUT.
+ */
+int attn_pair_product(const void *a, const void *b, float *d, void *stream);
+int attn_bench_mma_rate(int form, int busy, int waits, int steps, int reps, float *ms_out,
+                        double *cycles_out, int *sms_out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

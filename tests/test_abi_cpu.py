@@ -237,3 +237,22 @@ def test_release_and_debug_builds_identify_themselves(lib):
     assert dbg.attn_debug_build() == 1
     for name in declared_functions():
         assert hasattr(dbg, name), f"libgbattn_debug.so does not export {name}"
+
+
+def test_pair_entry_points_reject_before_launch(lib):
+    """The CTA-pair product and the issue-rate measurement check their
+    arguments on the host before any CUDA call."""
+    P = ctypes.c_void_p
+    assert lib.attn_pair_product(P(0), P(FAKE), P(FAKE), P(0)) == INVALID
+    assert lib.attn_pair_product(P(FAKE), P(FAKE), P(0), P(0)) == INVALID
+    assert lib.attn_pair_product(P(FAKE + 4), P(FAKE), P(FAKE), P(0)) == MISALIGNED
+    ms = ctypes.c_float()
+
+    def rate(form=1, busy=0, waits=0, steps=16, reps=1, out=True):
+        return lib.attn_bench_mma_rate(form, busy, waits, steps, reps,
+                                       ctypes.byref(ms) if out else P(0), P(0), P(0), P(0))
+
+    assert rate(form=0) == INVALID and rate(form=3) == INVALID
+    assert rate(busy=2) == INVALID and rate(waits=-1) == INVALID
+    assert rate(steps=0) == INVALID and rate(steps=(1 << 16) + 1) == INVALID
+    assert rate(reps=0) == INVALID and rate(out=False) == INVALID
