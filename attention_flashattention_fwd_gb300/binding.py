@@ -87,7 +87,7 @@ def _configure():
     lib.attn_debug_build.restype = I
     lib.attn_pair_product.argtypes = [P, P, P, P]
     lib.attn_pair_product.restype = I
-    lib.attn_bench_mma_rate.argtypes = [I, I, I, I, I, P, P, P, P]
+    lib.attn_bench_mma_rate.argtypes = [I, I, I, I, I, I, P, P, P, P]
     lib.attn_bench_mma_rate.restype = I
     return lib
 
@@ -448,15 +448,18 @@ def attn_pair_product(a, b, d=None, stream=None):
     return d
 
 
-def bench_mma_rate(form, busy=0, waits=0, steps=4096, reps=5, device=None, stream=None):
-    """Time one issuing thread's products (``attn_bench_mma_rate``): form 1 is
-    the single-CTA 128 x 128 x 16 product, form 2 the CTA-pair 256 x 128 x 16
-    one.  Returns {"ms": mean launch time, "cycles": mean issuing-thread
-    cycles, "sms": SMs used}."""
+def bench_mma_rate(form, issuer=1, busy=0, waits=0, steps=4096, reps=5, device=None,
+                   stream=None):
+    """Time one issuer's products (``attn_bench_mma_rate``): form 1 is the
+    single-CTA 128 x 128 x 16 product, form 2 the CTA-pair 256 x 128 x 16 one;
+    issuer 0 a lone lane, 1 a converged warp with an elected issuing lane.
+    Returns {"ms": mean launch time, "cycles": mean issuer cycles, "sms": SMs
+    used}."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
     ms, cyc, sms = ctypes.c_float(), ctypes.c_double(), ctypes.c_int()
     with _on(dev, stream):
-        _check(load().attn_bench_mma_rate(int(form), int(busy), int(waits), int(steps), int(reps),
+        _check(load().attn_bench_mma_rate(int(form), int(issuer), int(busy), int(waits), int(steps),
+                                          int(reps),
                                           ctypes.byref(ms), ctypes.byref(cyc), ctypes.byref(sms),
                                           _stream_ptr(stream)),
                "attn_bench_mma_rate")

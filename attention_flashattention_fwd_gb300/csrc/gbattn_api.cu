@@ -595,12 +595,13 @@ int attn_pair_product(const void* a, const void* b, float* d, void* stream) {
     return launch_pair_product(a, b, d, static_cast<cudaStream_t>(stream));
 }
 
-int attn_bench_mma_rate(int form, int busy, int waits, int steps, int reps, float* ms_out,
-                        double* cycles_out, int* sms_out, void* stream) {
-    if ((form != 1 && form != 2) || (busy != 0 && busy != 1) || (waits != 0 && waits != 1) ||
-        steps < 1 || steps > (1 << 16) || reps < 1 || reps > 1000 || !ms_out)
+int attn_bench_mma_rate(int form, int issuer, int busy, int waits, int steps, int reps,
+                        float* ms_out, double* cycles_out, int* sms_out, void* stream) {
+    if ((form != 1 && form != 2) || (issuer != 0 && issuer != 1) || (busy != 0 && busy != 1) ||
+        (waits != 0 && waits != 1) || steps < 1 || steps > (1 << 16) || reps < 1 || reps > 1000 ||
+        !ms_out)
         return ATTN_ERR_INVALID_ARG;
-    return run_mma_rate(form, busy, waits, steps, reps, ms_out, cycles_out, sms_out,
+    return run_mma_rate(form, issuer, busy, waits, steps, reps, ms_out, cycles_out, sms_out,
                         static_cast<cudaStream_t>(stream));
 }
 

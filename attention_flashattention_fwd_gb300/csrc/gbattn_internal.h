@@ -171,7 +171,7 @@ unsigned read_and_clear_selftest_error();
 // mma_pair_sm103.cu: the cta_group::2 product checked and timed against the
 // single-CTA form (blocking calls; each synchronises `stream`)
 int launch_pair_product(const void* a, const void* b, float* d, cudaStream_t stream);
-int run_mma_rate(int form, int busy, int waits, int steps, int reps, float* ms_out,
+int run_mma_rate(int form, int issuer, int busy, int waits, int steps, int reps, float* ms_out,
                  double* cycles_out, int* sms_out, cudaStream_t stream);
 
 // merge_sm103.cu

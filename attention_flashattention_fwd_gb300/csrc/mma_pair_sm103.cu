@@ -15,14 +15,16 @@
 //   * attn_pair_product_kernel -- D = A Bᵀ for A 256 x 64 and B 128 x 64 (bf16)
 //     by four pair products, read back from both CTAs' Tensor Memory, so a test
 //     can check the operand split against a host matrix product;
-//   * attn_mma_rate_kernel<kPair> -- the sustained issue rate of either form:
-//     one thread per issuing CTA issues `steps` groups of eight 128 x 128 x 16
-//     (cta_group::1) or 256 x 128 x 16 (cta_group::2) products, optionally with
-//     eight more warps per CTA running a softmax-like loop (Tensor Memory
-//     loads, packed fp32 FMA, exponentials, bf16 packs: two warps on every SM
-//     sub-partition, as the attention kernels place their softmax warps) and
-//     optionally waiting, after each group, for the previous group to finish
-//     (the dependency depth of the attention kernels' pipelines).
+//   * attn_mma_rate_kernel<kPair, kWaits, kWarp> -- the sustained issue rate of
+//     either form: the issuer issues `steps` groups of eight 128 x 128 x 16
+//     (cta_group::1) or 256 x 128 x 16 (cta_group::2) products, with or
+//     without a barrier wait in its loop (after group s, wait for group s-1:
+//     the dependency depth of the attention kernels' pipelines), as a lone
+//     lane or as a converged warp whose elected lane issues, and optionally
+//     with eight more warps per CTA running a softmax-like loop (Tensor
+//     Memory loads, packed fp32 FMA, exponentials, bf16 packs: two warps on
+//     every SM sub-partition, as the attention kernels place their softmax
+//     warps).
 // Each product of either form keeps every SM's tensor core busy for 64 cycles,
 // so the issuing thread's cycles per product give the tensor-busy fraction.
 //
@@ -176,11 +178,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
 
 // The issue-rate kernel.  kPair: cta_group::2 products issued by the even CTA
 // of each cluster (launched with a cluster of 2); otherwise cta_group::1 products
-// issued in every CTA.  cycles[i] receives issuing CTA i's clock64 cycles from
-// its first product to the completion of its last.
-template <bool kPair>
+// issued in every CTA.  kWaits: the loop waits for group s-1 after issuing group
+// s.  kWarp: all 32 lanes of warp 0 run the loop and the waits and the lane
+// elect_one() picks issues; otherwise lane 0 alone.  cycles[i] receives issuing
+// CTA i's clock64 cycles from its first product to the completion of its last.
+template <bool kPair, bool kWaits, bool kWarp>
 __global__ void __launch_bounds__(kRateThreads, 1)
-    attn_mma_rate_kernel(int steps, int busy, int waits, long long* __restrict__ cycles,
+    attn_mma_rate_kernel(int steps, int busy, long long* __restrict__ cycles,
                          unsigned* __restrict__ sink) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
@@ -214,35 +218,48 @@ __global__ void __launch_bounds__(kRateThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        if (issuer_cta && lane == 0) {
+        if (issuer_cta && (kWarp || lane == 0)) {
             const uint32_t idesc = umma_idesc_bf16(kPair ? 2 * kTileRows : kTileRows, kProductN, false);
             const uint64_t da = umma_desc_sw128(smem_addr(sA), 16, 1024);
             const uint64_t db = umma_desc_sw128(smem_addr(sB), 16, 1024);
+            auto wait = [&](uint32_t bar, uint32_t parity) {
+                const bool w = mbar_wait(bar, parity);
+                return kWarp ? __all_sync(0xffffffffu, w) : w;
+            };
             const long long t0 = clock64();
             bool ok = true;
             for (int s = 0; s < steps && ok; ++s) {
-                // eight products into two 128-column accumulators, as one key-tile
-                // step of one query tile issues (S = Q Kᵀ, then O += P V)
+                if (!kWarp || elect_one()) {
+                    // eight products into two 128-column accumulators, as one
+                    // key-tile step of one query tile issues (S = Q Kᵀ, O += P V)
 #pragma unroll
-                for (int p = 0; p < 8; ++p) {
-                    const uint32_t dst = tmem + static_cast<uint32_t>((p >> 2) * 128);
-                    const int kk = p & 3;
-                    if constexpr (kPair) umma_ss_pair(dst, da + kk * 2, db + kk * 2, idesc, 1u);
-                    else umma_ss(dst, da + kk * 2, db + kk * 2, idesc, 1u);
+                    for (int p = 0; p < 8; ++p) {
+                        const uint32_t dst = tmem + static_cast<uint32_t>((p >> 2) * 128);
+                        const int kk = p & 3;
+                        if constexpr (kPair) umma_ss_pair(dst, da + kk * 2, db + kk * 2, idesc, 1u);
+                        else umma_ss(dst, da + kk * 2, db + kk * 2, idesc, 1u);
+                    }
+                    const uint32_t sb = smem_addr(&bars[s & 1]);
+                    if constexpr (kPair) umma_commit_pair(sb, 0x1);
+                    else umma_commit(sb);
                 }
-                const uint32_t sb = smem_addr(&bars[s & 1]);
-                if constexpr (kPair) umma_commit_pair(sb, 0x1);
-                else umma_commit(sb);
-                if (waits && s >= 1) ok = mbar_wait(smem_addr(&bars[(s - 1) & 1]), ((s - 1) >> 1) & 1);
+                if constexpr (kWarp) __syncwarp();
+                if constexpr (kWaits)
+                    if (s >= 1) ok = wait(smem_addr(&bars[(s - 1) & 1]), ((s - 1) >> 1) & 1);
             }
             const uint32_t db_done = smem_addr(&bars[2]);
-            if constexpr (kPair) umma_commit_pair(db_done, 0x3);
-            else umma_commit(db_done);
-            ok = mbar_wait(db_done, 0) && ok;
+            if (!kWarp || elect_one()) {
+                if constexpr (kPair) umma_commit_pair(db_done, 0x3);
+                else umma_commit(db_done);
+            }
+            if constexpr (kWarp) __syncwarp();
+            ok = wait(db_done, 0) && ok;
             const long long t1 = clock64();
-            if (!ok) atomicOr(&g_pair_error, kErrBitTimeout);
-            cycles[kPair ? blockIdx.x / 2 : blockIdx.x] = t1 - t0;
-            *stop_flag = 1;
+            if (lane == 0) {
+                if (!ok) atomicOr(&g_pair_error, kErrBitTimeout);
+                cycles[kPair ? blockIdx.x / 2 : blockIdx.x] = t1 - t0;
+                *stop_flag = 1;
+            }
         } else if (!issuer_cta && lane == 0) {
             // the odd CTA of a pair: its tensor core and Tensor Memory take the
             // even CTA's products; wait for the last one
@@ -304,12 +321,20 @@ int launch_pair_product(const void* a, const void* b, float* d, cudaStream_t str
     return read_and_clear_pair_error();
 }
 
-int run_mma_rate(int form, int busy, int waits, int steps, int reps, float* ms_out,
+using RateKernel = void (*)(int, int, long long*, unsigned*);
+
+template <bool kPair>
+RateKernel rate_kernel(int waits, int issuer) {
+    if (waits) return issuer ? attn_mma_rate_kernel<kPair, true, true> : attn_mma_rate_kernel<kPair, true, false>;
+    return issuer ? attn_mma_rate_kernel<kPair, false, true> : attn_mma_rate_kernel<kPair, false, false>;
+}
+
+int run_mma_rate(int form, int issuer, int busy, int waits, int steps, int reps, float* ms_out,
                  double* cycles_out, int* sms_out, cudaStream_t stream) {
     const bool pair = form == 2;
-    auto kern = pair ? attn_mma_rate_kernel<true> : attn_mma_rate_kernel<false>;
-    // both forms' attributes: the pair kernel's also serves the occupancy query
-    for (auto k : {attn_mma_rate_kernel<false>, attn_mma_rate_kernel<true>})
+    const RateKernel kern = pair ? rate_kernel<true>(waits, issuer) : rate_kernel<false>(waits, issuer);
+    const RateKernel probe = attn_mma_rate_kernel<true, false, false>;  // occupancy query
+    for (RateKernel k : {kern, probe})
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kRateSmemBytes) !=
             cudaSuccess)
             return ATTN_ERR_CUDA;
@@ -330,7 +355,7 @@ int run_mma_rate(int form, int busy, int waits, int steps, int reps, float* ms_o
     if (current_sm_count(&sms) != ATTN_OK || sms < 2) return ATTN_ERR_CUDA;
     cfg.gridDim = dim3(sms & ~1);
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, attn_mma_rate_kernel<true>, &cfg) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveClusters(&clusters, probe, &cfg) != cudaSuccess ||
         clusters <= 0) {
         (void)cudaGetLastError();  // not sticky: leave no error for the next call
         return ATTN_ERR_CUDA;
@@ -357,7 +382,7 @@ int run_mma_rate(int form, int busy, int waits, int steps, int reps, float* ms_o
     std::vector<long long> h(issuers);
     for (int rep = -1; rep < reps && rc == ATTN_OK; ++rep) {  // rep -1 warms up
         cudaEventRecord(e0, stream);
-        if (cudaLaunchKernelEx(&cfg, kern, steps, busy, waits, d_cycles, d_sink) != cudaSuccess) {
+        if (cudaLaunchKernelEx(&cfg, kern, steps, busy, d_cycles, d_sink) != cudaSuccess) {
             rc = ATTN_ERR_CUDA;
             break;
         }

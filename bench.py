@@ -57,6 +57,10 @@ def parse_args():
                     help="run only this workload's kernel(s) (profiling runs); prints its time")
     ap.add_argument("--shape", default=None,
                     help="with --case custom: B,H,Nq,Nk,d,causal of a profiling workload")
+    ap.add_argument("--mma-rates", action="store_true",
+                    help="time the tensor-core issue forms (attn_bench_mma_rate) and print "
+                         "one JSON line: single-CTA and CTA-pair products, lone and "
+                         "converged issuer, with and without waits and softmax-like warps")
     ap.add_argument("--pass", dest="which", choices=["fwd", "bwd", "fp8", "mx", "merge"],
                     default="fwd",
                     help="with --case: time the forward (default), the backward call, the "
@@ -307,6 +311,36 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ GPU arm
+
+def run_mma_rates(steps=4096, reps=5):
+    """The tensor-core issue rates behind the kernels' issuer design (PDC
+    Lecture 7 §7.13 for the CTA pair): every product of either form keeps each
+    SM's tensor core busy for 64 cycles, so 64 x products / issuer cycles is the
+    fraction of the time the tensor core is busy."""
+    import torch
+
+    from attention_flashattention_fwd_gb300 import binding
+    torch.cuda.init()
+    rows = []
+    for busy in (0, 1):
+        for waits in (0, 1):
+            for issuer in (0, 1):
+                for form in (1, 2):
+                    r = binding.bench_mma_rate(form, issuer=issuer, busy=busy, waits=waits,
+                                               steps=steps, reps=reps)
+                    products = steps * 8
+                    flops = products * 2 * 128 * 128 * 16 * r["sms"]  # either form, per SM
+                    rows.append({"form": "cta_pair_m256" if form == 2 else "single_cta_m128",
+                                 "issuer": "warp" if issuer else "lane", "busy": busy,
+                                 "waits": waits, "sms": r["sms"], "ms": round(r["ms"], 4),
+                                 "cycles_per_product": round(r["cycles"] / products, 1),
+                                 "tensor_busy": round(64 * products / r["cycles"], 3),
+                                 "tflops": round(flops / (r["ms"] * 1e-3) / 1e12, 1)})
+    if binding.device_error() != 0:
+        raise RuntimeError("attn_bench_mma_rate: a bounded wait ran out")
+    print(json.dumps({"metric": "tensor-core issue rate", "steps": steps, "reps": reps,
+                      "rows": rows}), flush=True)
+
 
 def run_case(args):
     """One workload alone: W warm-up launches then K timed launches (used to
@@ -793,6 +827,9 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.mma_rates:
+        run_mma_rates()
         return
     if args.case:
         run_case(args)

@@ -426,29 +426,32 @@ int attn_selftest_bounds(void *stream);
  * ATTN_ERR_CUDA, or ATTN_ERR_TIMEOUT (a bounded wait ran out; d is then not
  * valid).
  *
- * attn_bench_mma_rate -- the sustained rate of one issuing thread.
+ * attn_bench_mma_rate -- the sustained rate of one issuer.
  *   form   1: each CTA issues 128 x 128 x 16 bf16 products (cta_group::1);
  *          2: the even CTA of each pair issues 256 x 128 x 16 products
  *             (cta_group::2).  Either way every product keeps each SM's
  *             tensor core busy for 64 cycles, and both forms run on the same
  *             SMs: as many CTA pairs as the device holds at once (sms_out
  *             receives how many SMs that is).
- *   busy   0: the issuing thread runs alone; 1: eight more warps per CTA (two
+ *   issuer 0: lane 0 of warp 0 alone runs the issuing loop;
+ *          1: all 32 lanes of warp 0 run it (and its waits) and one lane
+ *             chosen by elect.sync issues, as the attention kernels do.
+ *   busy   0: the issuing warp runs alone; 1: eight more warps per CTA (two
  *          on each SM sub-partition, where the attention kernels' softmax
  *          warps sit) loop over Tensor Memory loads, packed FMAs, exponentials
  *          and bf16 packs until the products are done.
- *   waits  0: a commit after every 8 products, no wait until the last;
- *          1: after issuing group s, wait for group s-1 to complete.
- *   steps  groups of 8 products per issuing thread, 1 to 65536.
+ *   waits  0: the loop holds no barrier wait (a commit after every 8
+ *          products); 1: after issuing group s it waits for group s-1.
+ *   steps  groups of 8 products per issuer, 1 to 65536.
  *   reps   timed launches (after one untimed), 1 to 1000.
  *   ms_out (host) mean launch time by CUDA events; cycles_out (host, may be
- *   NULL) mean clock64 cycles of an issuing thread from its first product to
- *   the completion of its last; sms_out (host, may be NULL).
+ *   NULL) mean clock64 cycles of an issuer from its first product to the
+ *   completion of its last; sms_out (host, may be NULL).
  * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_CUDA or ATTN_ERR_TIMEOUT.
  */
 int attn_pair_product(const void *a, const void *b, float *d, void *stream);
-int attn_bench_mma_rate(int form, int busy, int waits, int steps, int reps, float *ms_out,
-                        double *cycles_out, int *sms_out, void *stream);
+int attn_bench_mma_rate(int form, int issuer, int busy, int waits, int steps, int reps,
+                        float *ms_out, double *cycles_out, int *sms_out, void *stream);
 
 #ifdef __cplusplus
 }

@@ -248,11 +248,12 @@ def test_pair_entry_points_reject_before_launch(lib):
     assert lib.attn_pair_product(P(FAKE + 4), P(FAKE), P(FAKE), P(0)) == MISALIGNED
     ms = ctypes.c_float()
 
-    def rate(form=1, busy=0, waits=0, steps=16, reps=1, out=True):
-        return lib.attn_bench_mma_rate(form, busy, waits, steps, reps,
+    def rate(form=1, issuer=1, busy=0, waits=0, steps=16, reps=1, out=True):
+        return lib.attn_bench_mma_rate(form, issuer, busy, waits, steps, reps,
                                        ctypes.byref(ms) if out else P(0), P(0), P(0), P(0))
 
     assert rate(form=0) == INVALID and rate(form=3) == INVALID
+    assert rate(issuer=2) == INVALID and rate(issuer=-1) == INVALID
     assert rate(busy=2) == INVALID and rate(waits=-1) == INVALID
     assert rate(steps=0) == INVALID and rate(steps=(1 << 16) + 1) == INVALID
     assert rate(reps=0) == INVALID and rate(out=False) == INVALID

@@ -44,13 +44,14 @@ def test_pair_product_rows_and_columns_land_where_stated():
 
 
 @pytest.mark.parametrize("form", [1, 2])
+@pytest.mark.parametrize("issuer", [0, 1])
 @pytest.mark.parametrize("busy,waits", [(0, 0), (1, 1)])
-def test_mma_rate_is_bounded_by_the_tensor_core(form, busy, waits):
+def test_mma_rate_is_bounded_by_the_tensor_core(form, issuer, busy, waits):
     """Each product keeps every SM's tensor core busy for 64 cycles, so an
-    issuing thread cannot finish `steps` groups of 8 in fewer than
-    steps x 8 x 64 cycles; far more than that would mean a hung pipeline."""
+    issuer cannot finish `steps` groups of 8 in fewer than steps x 8 x 64
+    cycles; far more than that would mean a hung pipeline."""
     steps = 512
-    r = binding.bench_mma_rate(form, busy=busy, waits=waits, steps=steps, reps=2)
+    r = binding.bench_mma_rate(form, issuer=issuer, busy=busy, waits=waits, steps=steps, reps=2)
     floor = steps * 8 * 64
     assert r["sms"] >= 2 and r["sms"] % 2 == 0
     assert 0.95 * floor <= r["cycles"] <= 20 * floor, r
