@@ -53,6 +53,8 @@ def _configure():
     P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]
     lib.attn_fwd.restype = I
+    lib.attn_fwd_cta_pair.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]
+    lib.attn_fwd_cta_pair.restype = I
     lib.attn_fwd_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, F, F, F, P]
     lib.attn_fwd_fp8.restype = I
     lib.attn_fwd_decode_workspace_bytes.argtypes = [I, I, I, I]
@@ -184,6 +186,21 @@ def attn_fwd(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None)
         st = load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nk, d,
                              int(bool(causal)), float(scale), _stream_ptr(stream))
     _check(st, "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_cta_pair(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None):
+    """The C entry point ``attn_fwd_cta_pair``: attn_fwd with CTA-pair
+    (cta_group::2) tensor-core products, d = 128; bit-identical output."""
+    B, H, Nq, Nk, d = _check_inputs(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = _out(out, (B, H, Nq, d), torch.bfloat16, q.device, "out")
+    lse = _out(lse, (B, H, Nq), torch.float32, q.device, "lse")
+    with _on(q.device, stream):
+        st = load().attn_fwd_cta_pair(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq,
+                                      Nk, d, int(bool(causal)), float(scale), _stream_ptr(stream))
+    _check(st, "attn_fwd_cta_pair")
     return out, lse
 
 

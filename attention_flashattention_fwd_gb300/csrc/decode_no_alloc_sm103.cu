@@ -29,20 +29,19 @@
 namespace {
 
 constexpr size_t kScratchBytes = ATTN_DECODE_NO_ALLOC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
 
 // Partial outputs and logsumexps of the splits.  Every device that loads the
 // library holds this array until the process exits.
 static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
 std::mutex g_scratch_lock;
-void* g_scratch_addr[kMaxDevices] = {};
+void* g_scratch_addr[gbattn::kMaxDevices] = {};
 
 // Device address of g_decode_scratch on the current device (looked up once).
 int scratch_address(void** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+    if (dev < 0 || dev >= gbattn::kMaxDevices) return ATTN_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_scratch_lock);
     if (g_scratch_addr[dev] == nullptr) {
         void* p = nullptr;

@@ -38,7 +38,6 @@ int validate_fwd(const void* q, const void* k, const void* v, const void* o, con
     return ATTN_OK;
 }
 
-constexpr int kMaxDevices = 64;
 
 // The driver's tensor-map encoder: looked up once per process.
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -69,6 +68,7 @@ int ensure_init() {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
     std::call_once(g_attr_once[dev], [dev] {
         int st = prefill_set_attributes();
+        if (st == ATTN_OK) st = prefill_pair_set_attributes();
         if (st == ATTN_OK) st = bwd_set_attributes();
         g_attr_status[dev] = st;
     });
@@ -104,14 +104,15 @@ int current_sm_count(int* out) {
 
 namespace {
 
-// [BH, N, d] bf16 viewed as a 3-D tensor (d innermost), boxes of 64 x 128 x 1
-// with the 128-byte swizzle the tcgen05 operand descriptors expect.
-int encode_bhnd(CUtensorMap* m, const void* base, long long BH, int N, int d) {
+// [BH, N, d] bf16 viewed as a 3-D tensor (d innermost), boxes of 64 x rows x 1
+// (rows 128, or 64 for the half key tiles of the CTA-pair prefill) with the
+// 128-byte swizzle the tcgen05 operand descriptors expect.
+int encode_bhnd(CUtensorMap* m, const void* base, long long BH, int N, int d, unsigned rows = 128) {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                           static_cast<cuuint64_t>(BH)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                              static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t box[3] = {64, rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
                                 dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -153,9 +154,12 @@ int encode_dq_acc(CUtensorMap* m, void* base, long long BH, int nq_pad, int d) {
     return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// cta_pair: the products as CTA-pair (cta_group::2) products (bf16, d = 128,
+// no per-sequence lengths); otherwise the single-CTA kernel.
 int enqueue_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                 int Nq, int Nk, int d, int causal, float scale, cudaStream_t stream,
-                const int* seqlens_q = nullptr, const int* seqlens_k = nullptr) {
+                const int* seqlens_q = nullptr, const int* seqlens_k = nullptr,
+                bool cta_pair = false) {
     int st = ensure_init();
     if (st != ATTN_OK) return st;
     int num_sms = 0;
@@ -179,6 +183,13 @@ int enqueue_fwd(const void* q, const void* k, const void* v, void* o, float* lse
     p.seqlens_q = seqlens_q;
     p.seqlens_k = seqlens_k;
     p.o_scale = 1.f;
+    if (cta_pair) {
+        // quads of four query tiles per item, K in half tiles of 64 keys
+        CUtensorMap tk64;
+        if ((st = encode_bhnd(&tk64, k, BH, Nk, d, 64)) != ATTN_OK) return st;
+        p.num_pairs = (Nq + 511) / 512;
+        return launch_prefill_pair(tq, tk64, tv, to, p, stream);
+    }
     return launch_prefill(d, tq, tk, tv, to, p, num_sms, stream);
 }
 
@@ -306,6 +317,17 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
         return ATTN_ERR_MISALIGNED;
     return enqueue_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale,
                        static_cast<cudaStream_t>(stream));
+}
+
+int attn_fwd_cta_pair(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int H, int Nq, int Nk, int d, int causal, float scale, void* stream) {
+    int st = validate_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale);
+    if (st != ATTN_OK) return st;
+    if (d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return ATTN_ERR_MISALIGNED;
+    return enqueue_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale,
+                       static_cast<cudaStream_t>(stream), nullptr, nullptr, true);
 }
 
 size_t attn_fwd_decode_workspace_bytes(int B, int H, int Nk, int d) {
@@ -570,7 +592,8 @@ const char* attn_status_string(int status) {
 
 int attn_device_error(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
-    const unsigned e = read_and_clear_prefill_error() | read_and_clear_bwd_error() |
+    const unsigned e = read_and_clear_prefill_error() | read_and_clear_prefill_pair_error() |
+                       read_and_clear_bwd_error() |
                        read_and_clear_decode_error() | read_and_clear_selftest_error() |
                        read_and_clear_merge_error();
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;

@@ -107,6 +107,15 @@ int launch_prefill_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        cudaStream_t stream);
 int prefill_smem_bytes(int d);
 unsigned read_and_clear_prefill_error();
+
+// prefill_pair_sm103.cu: bf16, d = 128, no per-sequence lengths, on CTA pairs.
+// p.num_pairs counts quads (four 128-row query tiles) per head; tk64 maps K in
+// boxes of 64 x 64 x 1 (the half key tile each CTA of a pair holds).
+int prefill_pair_set_attributes();
+int launch_prefill_pair(const CUtensorMap& tq, const CUtensorMap& tk64, const CUtensorMap& tv,
+                        const CUtensorMap& to, const PrefillParams& p, cudaStream_t stream);
+unsigned read_and_clear_prefill_pair_error();
+constexpr int kMaxDevices = 64;  // device ordinals the per-device caches cover
 // Device error bits (shared by the kernels' error words)
 constexpr unsigned kErrBitTimeout = 1u;  // a bounded barrier wait ran out
 constexpr unsigned kErrBitLengths = 4u;  // a per-sequence length was out of range

@@ -130,6 +130,24 @@ int attn_fwd_fp8(const void *q, const void *k, const void *vt, void *o, float *l
                  float descale_q, float descale_k, float descale_v, void *stream);
 
 /*
+ * attn_fwd_cta_pair -- attn_fwd with every tensor-core product issued as a
+ * CTA-pair product (tcgen05.mma.cta_group::2, PDC course Lecture 7, section
+ * 7.13: two CTAs of a cluster on two SMs share each product, M = 256, each
+ * holding half of every key and value tile).  Same arguments, layouts,
+ * ownership and result as attn_fwd; the products are the same and accumulate
+ * in the same order, so the output is bit-identical to attn_fwd's.
+ *   d = 128 only.
+ * Measured on GB300 it is slower than attn_fwd (about 0.75x at 4096 tokens):
+ * every key-tile step waits for the second SM's softmax to signal across the
+ * pair.  attn_fwd keeps the single-CTA products.
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED (d != 128, or as
+ * attn_fwd), ATTN_ERR_MISALIGNED or ATTN_ERR_CUDA.
+ */
+int attn_fwd_cta_pair(const void *q, const void *k, const void *v, void *o, float *lse,
+                      int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                      void *stream);
+
+/*
  * attn_fwd_decode_workspace_bytes -- bytes of device workspace attn_fwd_decode
  * needs for these sizes: room for the split partials of the largest split
  * plan any device takes (at most one split per 512 keys and 64 splits per

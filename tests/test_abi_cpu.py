@@ -257,3 +257,17 @@ def test_pair_entry_points_reject_before_launch(lib):
     assert rate(busy=2) == INVALID and rate(waits=-1) == INVALID
     assert rate(steps=0) == INVALID and rate(steps=(1 << 16) + 1) == INVALID
     assert rate(reps=0) == INVALID and rate(out=False) == INVALID
+
+
+def test_cta_pair_entry_rejects_before_launch(lib):
+    """attn_fwd_cta_pair validates like attn_fwd and takes d = 128 only."""
+    P = ctypes.c_void_p
+
+    def pair(q=FAKE, o=FAKE, d=128, Nq=128, Nk=128, causal=0, scale=0.1):
+        return lib.attn_fwd_cta_pair(P(q), P(FAKE), P(FAKE), P(o), P(FAKE), 1, 2, Nq, Nk, d, causal,
+                                     scale, P(0))
+
+    assert pair(q=0) == INVALID and pair(Nq=0) == INVALID and pair(scale=0.0) == INVALID
+    assert pair(d=64) == UNSUPPORTED and pair(d=96) == UNSUPPORTED
+    assert pair(causal=1, Nq=256, Nk=128) == UNSUPPORTED
+    assert pair(o=FAKE + 2) == MISALIGNED
