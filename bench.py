@@ -61,11 +61,12 @@ def parse_args():
                     help="time the tensor-core issue forms (attn_bench_mma_rate) and print "
                          "one JSON line: single-CTA and CTA-pair products, lone and "
                          "converged issuer, with and without waits and softmax-like warps")
-    ap.add_argument("--pass", dest="which", choices=["fwd", "bwd", "fp8", "mx", "merge"],
-                    default="fwd",
+    ap.add_argument("--pass", dest="which",
+                    choices=["fwd", "bwd", "fp8", "mx", "merge", "pair"], default="fwd",
                     help="with --case: time the forward (default), the backward call, the "
-                         "forward on FP8 (E4M3) operands, (decode) MXFP8 keys and values, or "
-                         "attn_merge of 4 shard results of the workload's shape")
+                         "forward on FP8 (E4M3) operands, (decode) MXFP8 keys and values, "
+                         "attn_merge of 4 shard results of the workload's shape, or the "
+                         "forward on CTA-pair products (attn_fwd_cta_pair)")
     a = ap.parse_args()
     a.warmup = max(3, a.warmup)
     a.steps = max(1, a.steps)
@@ -90,9 +91,10 @@ def _sources_sha(names):
     return h.hexdigest()[:16]
 
 
-PREFILL_SOURCES = ["prefill_sm103.cu", "sm103_ptx.cuh"]
-DECODE_SOURCES = ["decode_sm103.cu", "sm103_ptx.cuh"]
-BACKWARD_SOURCES = ["backward_sm103.cu", "sm103_ptx.cuh"]
+PREFILL_SOURCES = ["prefill_sm103.cu", "sm103_ptx.cuh", "gbattn_internal.h"]
+PAIR_SOURCES = ["prefill_pair_sm103.cu", "sm103_ptx.cuh", "gbattn_internal.h"]
+DECODE_SOURCES = ["decode_sm103.cu", "sm103_ptx.cuh", "gbattn_internal.h"]
+BACKWARD_SOURCES = ["backward_sm103.cu", "sm103_ptx.cuh", "gbattn_internal.h"]
 FP8_PEAK_RATIO = 2.0  # nominal dense fp8 : bf16 tensor rate (4.5 : 2.25 PFLOP/s)
 # ex2.approx.f32 per clock per SM on GB300 (measured: 4 cycles per warp instruction
 # per SM sub-partition); the SFU roofline of the softmax's exponentials
@@ -106,7 +108,7 @@ def visible_pairs(w):
     off = w.Nk - w.Nq  # query i sees keys j <= i + off
     return w.B * w.H * (w.Nq * (off + 1) + w.Nq * (w.Nq - 1) // 2)
 MERGE_PARTS = 4  # key shards merged by attn_merge in the context-parallel measurement
-MERGE_SOURCES = ["merge_sm103.cu", "sm103_ptx.cuh"]
+MERGE_SOURCES = ["merge_sm103.cu", "sm103_ptx.cuh", "gbattn_internal.h"]
 # FLOPs of the backward: five products of the forward's size (S and dP
 # recomputed, dV, dK, dQ) against the forward's two.
 BWD_FLOP_RATIO = 2.5
@@ -408,6 +410,12 @@ def run_case(args):
         def launch():  # noqa: F811  (the timed call is the MX decode)
             binding.attn_fwd_decode_mx(qx, k8x, ksx, v8x, vsx, scale=w.scale, out=o, lse=lse,
                                        workspace=ws)
+    elif args.which == "pair":
+        if w.decode or w.d != 128:
+            raise SystemExit("--pass pair needs a d = 128 prefill workload")
+
+        def launch():  # noqa: F811  (the timed call is the CTA-pair forward)
+            binding.attn_fwd_cta_pair(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)
     elif args.which == "fp8":
         if w.decode or w.d != 128:
             raise SystemExit("--pass fp8 needs a d = 128 prefill workload")
@@ -660,6 +668,32 @@ def run_gpu(args):
     noncausal["calls"] = bwd_reps
     del qn, kn, vn, on, ln
 
+    # ---- the same headline workload through attn_fwd_cta_pair: CTA-pair
+    # (cta_group::2) products, bit-identical output (not part of the timed step)
+    op, lp = torch.empty_like(o3), torch.empty_like(l3)
+    for _ in range(3):
+        binding.attn_fwd_cta_pair(q3, k3, v3, causal=True, scale=w3.scale, out=op, lse=lp,
+                                  stream=stream)
+    torch.cuda.synchronize()
+    c_ms = 0.0
+    for _ in range(bwd_reps):
+        flush_l2()
+        torch.cuda._sleep(LAUNCH_COVER_CYCLES)
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        binding.attn_fwd_cta_pair(q3, k3, v3, causal=True, scale=w3.scale, out=op, lse=lp,
+                                  stream=stream)
+        b1.record(stream)
+        torch.cuda.synchronize()
+        c_ms += b0.elapsed_time(b1)
+    if binding.device_error() != 0:
+        raise RuntimeError("a kernel reported a device-side error in the CTA-pair forward")
+    (c_ms,) = max_over_ranks([c_ms], world, device=dev)
+    cta_pair = prefill_part(w3, c_ms * K / bwd_reps, PAIR_SOURCES, "ncu_prefill_pair_" + w3.name)
+    cta_pair["calls"] = bwd_reps
+    cta_pair["entry"] = "attn_fwd_cta_pair (tcgen05.mma.cta_group::2, M = 256 over two SMs)"
+    del op, lp
+
     # ---- FP8 (E4M3) operands on the headline workload (not part of the timed
     # step): the same Gaussian draws, per-tensor scaled to E4M3
     from attention_flashattention_fwd_gb300.inputs import make_workload_fp8
@@ -787,6 +821,7 @@ def run_gpu(args):
         "gpu_launches": launches_per_step * K,
         "parts": {HEADLINE: p3, LONG: p4, DECODE: p5},
         "noncausal": noncausal,
+        "cta_pair": cta_pair,
         "fp8": fp8,
         "decode_mx": decode_mx,
         "backward": backward,
@@ -812,6 +847,7 @@ def run_gpu(args):
         "prefill_" + LONG: brief(p4, "ms_per_launch"),
         "prefill_" + HEADLINE: brief(p3, "ms_per_launch"),
         "prefill_" + wn.name: brief(noncausal, "ms_per_launch"),
+        "cta_pair_" + w3.name: brief(cta_pair, "ms_per_launch"),
         "decode_" + w5.name.replace("decode_", ""): brief(p5, "ms_per_call"),
         "decode_mx_" + w5.name.replace("decode_", ""): brief(decode_mx, "ms_per_call"),
         "fp8_" + w3.name: brief(fp8, "ms_per_call"),
