@@ -49,6 +49,19 @@ SCRIPT = textwrap.dedent(r"""
         ro, rl = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), causal=c)
         close(o, lse, ro, rl, ("fwd", B, H, Nq, Nk, d, c))
 
+    # the CTA-pair forward: bit-identical to attn_fwd; the pair product
+    for (B, H, Nq, Nk, c) in [(1, 2, 1000, 1300, True), (2, 3, 300, 513, False)]:
+        q, k, v = make_qkv(B, H, Nq, Nk, 128, seed=7 + Nq, device=dev)
+        o2, l2 = nan((B, H, Nq, 128), torch.bfloat16), nan((B, H, Nq), torch.float32)
+        binding.attn_fwd_cta_pair(q, k, v, causal=c, out=o2, lse=l2)
+        o1, l1 = binding.attn_fwd(q, k, v, causal=c)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2), ("pair", B, H, Nq, Nk, c)
+    a = torch.randn(256, 64, device=dev).to(torch.bfloat16)
+    bm = torch.randn(128, 64, device=dev).to(torch.bfloat16)
+    d = binding.attn_pair_product(a, bm).double().cpu()
+    ref = a.double().cpu() @ bm.double().cpu().T
+    assert (d - ref).abs().max().item() <= 1e-3 * max(1.0, ref.abs().max().item())
+
     # ragged: sequence lengths; rows past them stay untouched
     B, H, Nq, Nk, d = 2, 2, 256, 300, 128
     q, k, v = make_qkv(B, H, Nq, Nk, d, seed=9, device=dev)
