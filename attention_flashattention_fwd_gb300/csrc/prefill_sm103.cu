@@ -62,12 +62,14 @@ constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr int kRelayWarp = 10;
 // Register split.  The launch gives every thread 168 registers (65536 / 384,
-// rounded down to 8): 384 x 168 = 64512.  The warpgroup of the MMA and TMA warps
-// gives part of its share to the two softmax warpgroups:
-// 128 x 112 + 256 x 176 = 59392 <= 64512.  176 is the least the softmax
-// compiles in without spills; more (or a different split) measured slower.
-constexpr uint32_t kSoftmaxRegs = 176;
-constexpr uint32_t kControlRegs = 112;
+// rounded down to 8): 384 x 168 = 64512.  The warpgroup of the MMA, TMA and
+// relay warps gives part of its share to the two softmax warpgroups, which
+// needs 2 (S - 168) <= 168 - C.  d = 128: 256 x 192 + 128 x 96 = 61440; the
+// converged MMA warp fits in 96 and the softmax runs faster with 192 than with
+// 176 (measured: 176/112, 184/96, 200/96 and 208/88 slower or no better,
+// 168/128 spills).  d = 64: 256 x 176 + 128 x 112 = 59392 (192/96 spills there).
+template <int D> constexpr uint32_t softmax_regs() { return D == 128 ? 192u : 176u; }
+template <int D> constexpr uint32_t control_regs() { return D == 128 ? 96u : 112u; }
 constexpr uint32_t kTmemCols = 512;
 constexpr int kStageBufBytes = 32 * 64;  // one O staging buffer: 32 rows x 64 bytes
 // A key tile whose row sum against the stale reference max exceeds this moves
@@ -301,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp >= 8) {
     // ====================================================== control warpgroup
-    setmaxnreg_dec<kControlRegs>();
+    setmaxnreg_dec<control_regs<D>()>();
     if (warp == kLoadWarp) {
         // ================================================= TMA producer
         if (lane == 0) {
@@ -536,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }  // warp 11 has no role
     } else {
         // ================================================= softmax warpgroups
-        setmaxnreg_inc<kSoftmaxRegs>();
+        setmaxnreg_inc<softmax_regs<D>()>();
         const int t = warp >> 2;          // query tile 0 or 1
         const int wq = warp & 3;          // TMEM lane quarter
         const int r = wq * 32 + lane;     // row within the tile
