@@ -29,6 +29,8 @@ struct PrefillParams {
     // the two halves of query-tile pair split_start + i; no split when
     // split_start == n_items).
     int n_items, split_start;
+    // Set by the launcher: causal items are dealt in groups of this many heads.
+    int head_group;
 };
 
 // Arguments of the split-K decode kernels.
