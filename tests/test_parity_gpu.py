@@ -406,3 +406,44 @@ def test_decode_8192_heads_sampled():
     og = o.reshape(B * H, d)[torch.as_tensor(heads, device=o.device)].float().cpu().numpy()
     lg = lse.reshape(B * H)[torch.as_tensor(heads, device=o.device)].cpu().numpy()
     _assert_close(og, lg, ro, rl, "decode 8192 heads")
+
+
+@pytest.mark.parametrize("name", ["b2h16n4096d128_causal", "b2h16n4096d128",
+                                  "b1h32n16384d128_causal"])
+def test_full_workload_every_row_against_fp32_recompute(name):
+    """Every row of every head of the full-size workloads, against an fp32
+    recomputation of the definition on the GPU (torch products, head by head:
+    S = scale Q K^T with the causal mask, lse = log sum exp S, O = softmax(S) V)
+    -- a check independent of the library beside the fp64 oracle's full head and
+    sampled rows above.  The outputs start as NaN, so a tile no work item wrote
+    fails here wherever it is."""
+    from attention_flashattention_fwd_gb300.inputs import EXTRA_WORKLOADS
+    w = WORKLOADS.get(name) or EXTRA_WORKLOADS[name]
+    q, k, v = make_workload(w, device=_dev())
+    o, lse = binding.attn_fwd(q, k, v, causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    BH = w.B * w.H
+    qf, kf, vf = (t.reshape(BH, -1, w.d) for t in (q, k, v))
+    of, lf = o.reshape(BH, w.Nq, w.d), lse.reshape(BH, w.Nq)
+    mask = None
+    if w.causal:
+        i = torch.arange(w.Nq, device=_dev()).view(-1, 1)
+        j = torch.arange(w.Nk, device=_dev()).view(1, -1)
+        mask = j > i + (w.Nk - w.Nq)
+    worst_o = worst_l = 0.0
+    sum_o = 0.0
+    for h in range(BH):
+        s = (qf[h].float() @ kf[h].float().T) * w.scale
+        if mask is not None:
+            s.masked_fill_(mask, float("-inf"))
+        rl = torch.logsumexp(s, dim=1)
+        ro = torch.softmax(s, dim=1) @ vf[h].float()
+        e = (of[h].float() - ro).abs()
+        worst_o = max(worst_o, e.max().item())
+        sum_o += e.mean().item()
+        worst_l = max(worst_l, (lf[h] - rl).abs().max().item())
+        del s, ro, rl, e
+    assert worst_o <= O_MAX and sum_o / BH <= O_MEAN and worst_l <= LSE_MAX, \
+        (name, worst_o, sum_o / BH, worst_l)
+    assert binding.device_error() == 0
