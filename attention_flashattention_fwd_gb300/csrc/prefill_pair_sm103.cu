@@ -40,7 +40,6 @@
 #include <cuda.h>
 
 #include <atomic>
-#include <mutex>
 
 #include "gbattn_internal.h"
 #include "sm103_ptx.cuh"
