@@ -59,8 +59,8 @@ constexpr int kThreads = 384;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr int kRelayWarp = 10;
-constexpr uint32_t kSoftmaxRegs = 176;  // the single-CTA kernel's split: 128 x 112 + 256 x 176
-constexpr uint32_t kControlRegs = 112;
+constexpr uint32_t kSoftmaxRegs = 192;  // the single-CTA kernel's split at d = 128: 128 x 96 + 256 x 192
+constexpr uint32_t kControlRegs = 96;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kStageBufBytes = 32 * 64;
 constexpr float kTileSumLimit = 4.611686018427387904e18f;  // 2^62, as the single-CTA kernel
