@@ -447,3 +447,28 @@ def test_full_workload_every_row_against_fp32_recompute(name):
     assert worst_o <= O_MAX and sum_o / BH <= O_MEAN and worst_l <= LSE_MAX, \
         (name, worst_o, sum_o / BH, worst_l)
     assert binding.device_error() == 0
+
+
+def test_causal_head_groups_uneven_last_group_and_chunk():
+    """Causal work whose K and V exceed L2 several times over is dealt in head
+    groups (32 MB of K and V per head here: groups of 3, 3, 3 and 1 heads), with
+    a causal query chunk shorter than the keys (Nq < Nk): sampled rows of every
+    head against the oracle, first and last rows of each pair of query tiles
+    included, and every output written (NaN-filled before the call)."""
+    from attention_flashattention_fwd_gb300.inputs import Workload
+    w = Workload("b1h10q2048k65536d128_causal", 1, 10, 2048, 65536, 128, True, seed=2100)
+    q, k, v = make_workload(w, device=_dev())
+    o, lse = binding.attn_fwd(q, k, v, causal=True, scale=w.scale)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    rng = np.random.default_rng(77)
+    rows = [(h, i) for h in range(10) for i in (0, 255, 256, 511, 1792, 2047)]
+    rows += [(int(rng.integers(10)), int(rng.integers(2048))) for _ in range(60)]
+    rows = np.array(rows, dtype=np.int64)
+    ro, rl = oracle.attention_rows(bf16_bits(q), bf16_bits(k), bf16_bits(v), rows, causal=True,
+                                   scale=w.scale)
+    idx = torch.as_tensor(rows[:, 0] * w.Nq + rows[:, 1], device=o.device)
+    og = o.reshape(10 * w.Nq, w.d).index_select(0, idx).float().cpu().numpy()
+    lg = lse.reshape(10 * w.Nq).index_select(0, idx).cpu().numpy()
+    _assert_close(og, lg, ro, rl, w.name)
+    assert binding.device_error() == 0
