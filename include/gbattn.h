@@ -137,7 +137,7 @@ int attn_fwd_fp8(const void *q, const void *k, const void *vt, void *o, float *l
  * ownership and result as attn_fwd; the products are the same and accumulate
  * in the same order, so the output is bit-identical to attn_fwd's.
  *   d = 128 only.
- * Measured on GB300 it is slower than attn_fwd (about 0.75x at 4096 tokens):
+ * Measured on GB300 it is slower than attn_fwd (about 0.72x at 4096 tokens):
  * every key-tile step waits for the second SM's softmax to signal across the
  * pair.  attn_fwd keeps the single-CTA products.
  * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED (d != 128, or as
