@@ -14,9 +14,11 @@
  *       o  bf16 [B, H, Nq, d]      lse   fp32 [B, H, Nq]  (natural log)
  *     "bf16" is IEEE bfloat16 (1-8-7) stored in 2 bytes.
  *   - Device pointers must be 16-byte aligned.  The caller owns every buffer;
- *     the library allocates nothing on any call.
- *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Compute calls
- *     are asynchronous: ATTN_OK means "enqueued".  Faults inside a kernel
+ *     the attention calls allocate nothing (attn_bench_mma_rate, a measurement
+ *     of the product forms, allocates its own result buffer).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  The attention
+ *     calls are asynchronous: ATTN_OK means "enqueued" (attn_pair_product and
+ *     attn_bench_mma_rate synchronise before returning).  Faults inside a kernel
  *     surface at the caller's next synchronisation, as in CUDA.
  *   - Arguments are validated on the host before anything is launched; a
  *     rejected call launches nothing and touches no buffer.
