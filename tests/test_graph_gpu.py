@@ -64,6 +64,7 @@ def _buffers(dev):
         # outputs
         "o": z((B, H, NQ, D), bf), "lse": z((B, H, NQ), f32),
         "o8": z((B, H, NQ, D), bf), "lse8": z((B, H, NQ), f32),
+        "oc": z((B, H, NQ, D), bf), "lc": z((B, H, NQ), f32),
         "op": z((2, B, H, NQ, D), bf), "lp": z((2, B, H, NQ), f32),
         "om": z((B, H, NQ, D), bf), "lm": z((B, H, NQ), f32),
         "od": z((B, H, 1, D), bf), "ld": z((B, H, 1), f32),
@@ -73,14 +74,15 @@ def _buffers(dev):
     }
 
 
-OUTPUTS = ("o", "lse", "o8", "lse8", "op", "lp", "om", "lm", "od", "ld", "ox", "lx", "dk", "dv")
+OUTPUTS = ("o", "lse", "oc", "lc", "o8", "lse8", "op", "lp", "om", "lm", "od", "ld", "ox", "lx", "dk", "dv")
 
 
 def _step(b):
-    """One pass over the entry points: causal prefill, FP8 prefill, two key
-    shards merged, one decode row (bf16 and MXFP8 keys and values), and the
-    backward of the causal prefill."""
+    """One pass over the entry points: causal prefill (single-CTA and CTA-pair
+    products), FP8 prefill, two key shards merged, one decode row (bf16 and
+    MXFP8 keys and values), and the backward of the causal prefill."""
     binding.attn_fwd(b["q"], b["k"], b["v"], causal=True, out=b["o"], lse=b["lse"])
+    binding.attn_fwd_cta_pair(b["q"], b["k"], b["v"], causal=True, out=b["oc"], lse=b["lc"])
     binding.attn_fwd_fp8(b["q8"], b["k8"], b["vt8"], 0.05, 0.05, 0.05, causal=True,
                          out=b["o8"], lse=b["lse8"])
     binding.attn_fwd(b["q"], b["k0"], b["v0"], out=b["op"][0], lse=b["lp"][0])
@@ -119,6 +121,7 @@ def test_graph_replay_matches_eager_calls():
         # against the fp64 oracle on this seed's inputs
         ro, rl = oracle.attention(bf16_bits(b["q"]), bf16_bits(b["k"]), bf16_bits(b["v"]),
                                   causal=True)
+        assert torch.equal(replayed["oc"], replayed["o"]) and torch.equal(replayed["lc"], replayed["lse"])
         e = np.abs(replayed["o"].float().cpu().numpy() - ro)
         el = np.abs(replayed["lse"].cpu().numpy() - rl)
         assert e.max() <= 2e-2 and e.mean() <= 1e-3 and el.max() <= 2e-3
