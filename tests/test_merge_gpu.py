@@ -69,3 +69,51 @@ def test_empty_parts_have_no_weight():
         o, lse = binding.attn_merge(torch.stack([junk] * n), torch.stack([ninf] * n))
         torch.cuda.synchronize()
         assert (o.float() == 0).all() and torch.isinf(lse).all() and (lse < 0).all()
+
+
+def test_merge_of_the_bench_shards_closed_form():
+    """The bench's merge call at full size (four shards of the B2 H16 N4096 d128
+    shape, every o_s the same o and lse_s = lse - s): the merged row is the same
+    convex combination of identical rows, o, and the merged logsumexp is
+    lse + ln(1 + e^-1 + e^-2 + e^-3)."""
+    from attention_flashattention_fwd_gb300.inputs import WORKLOADS, make_workload
+    w = WORKLOADS["b2h16n4096d128_causal"]
+    q, k, v = make_workload(w, device="cuda")
+    o, lse = binding.attn_fwd(q, k, v, causal=True, scale=w.scale)
+    o_parts = torch.stack([o] * 4).contiguous()
+    l_parts = torch.stack([lse - float(s) for s in range(4)]).contiguous()
+    om, lm = binding.attn_merge(o_parts, l_parts)
+    torch.cuda.synchronize()
+    shift = float(np.log(sum(np.exp(-s) for s in range(4))))
+    eo = (om.float() - o.float()).abs().max().item()
+    el = (lm - (lse + shift)).abs().max().item()
+    assert eo <= 2.0 ** -8 * o.float().abs().max().item() and el <= 1e-5, (eo, el)
+    assert binding.device_error() == 0
+
+
+def test_merge_full_size_key_shards():
+    """Four key shards of the non-causal B2 H16 N4096 d128 workload (1024 keys
+    each), attended one by one and merged: against the fp64 oracle on sampled
+    rows, and every row against one call over all keys."""
+    from attention_flashattention_fwd_gb300.inputs import EXTRA_WORKLOADS, make_workload
+    w = EXTRA_WORKLOADS["b2h16n4096d128"]
+    q, k, v = make_workload(w, device="cuda")
+    parts = [binding.attn_fwd(q, k[:, :, a:a + 1024].contiguous(), v[:, :, a:a + 1024].contiguous(),
+                              scale=w.scale) for a in range(0, 4096, 1024)]
+    om, lm = binding.attn_merge(torch.stack([p[0] for p in parts]),
+                                torch.stack([p[1] for p in parts]))
+    of, lf = binding.attn_fwd(q, k, v, scale=w.scale)
+    torch.cuda.synchronize()
+    assert (om.float() - of.float()).abs().max().item() <= 2e-2
+    assert (lm - lf).abs().max().item() <= 2e-3
+    rng = np.random.default_rng(5)
+    BH = w.B * w.H
+    rows = np.array([(int(rng.integers(BH)), int(rng.integers(w.Nq))) for _ in range(128)],
+                    dtype=np.int64)
+    ro, rl = oracle.attention_rows(bf16_bits(q), bf16_bits(k), bf16_bits(v), rows, causal=False,
+                                   scale=w.scale)
+    idx = torch.as_tensor(rows[:, 0] * w.Nq + rows[:, 1], device=om.device)
+    og = om.reshape(BH * w.Nq, w.d).index_select(0, idx)
+    lg = lm.reshape(BH * w.Nq).index_select(0, idx)
+    _check(og, lg, ro, rl, "4 key shards of b2h16n4096d128")
+    assert binding.device_error() == 0
