@@ -472,3 +472,26 @@ def test_causal_head_groups_uneven_last_group_and_chunk():
     lg = lse.reshape(10 * w.Nq).index_select(0, idx).cpu().numpy()
     _assert_close(og, lg, ro, rl, w.name)
     assert binding.device_error() == 0
+
+
+def test_from_host_long_workload_bit_identical():
+    """The bench's end-to-end call at full size: the long workload (B1 H32 N16384
+    d128 causal) from pinned host buffers through attn_fwd_from_host (five head
+    chunks on three streams) gives the same bits as attn_fwd on the device copy
+    (every row's products run in the same order whichever heads share a launch),
+    which the tests above check against the oracle and an fp32 recomputation."""
+    w = WORKLOADS["b1h32n16384d128_causal"]
+    q, k, v = make_workload(w, device=_dev())
+    o1, l1 = binding.attn_fwd(q, k, v, causal=True, scale=w.scale)
+    qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+    oh = nan_full(o1.shape, torch.bfloat16, pin=True)
+    lh = nan_full(l1.shape, torch.float32, pin=True)
+    dq, dk, dv = (nan_full(t.shape, t.dtype, _dev()) for t in (q, k, v))
+    do_ = nan_full(o1.shape, torch.bfloat16, _dev())
+    dl = nan_full(l1.shape, torch.float32, _dev())
+    s = torch.cuda.Stream()
+    binding.attn_fwd_from_host(qh, kh, vh, oh, lh, dq, dk, dv, do_, dl, causal=True,
+                               scale=w.scale, stream=s)
+    s.synchronize()
+    assert torch.equal(oh, o1.cpu()) and torch.equal(lh, l1.cpu())
+    assert binding.device_error() == 0
