@@ -594,11 +594,63 @@ def run_gpu(args):
     e1.record(stream)
     torch.cuda.synchronize()
     (e2e_ms,) = max_over_ranks([e0.elapsed_time(e1)], world, device=dev)
+    # the host link's own rate right now: the same step's bytes as plain
+    # copies, inputs in on `stream` while the results go out on a second
+    # stream, no kernel.  A copy-only step is the floor under an end-to-end
+    # step, and the link is shared with the rest of the machine, so it is
+    # measured beside the number it bounds.
+    out_stream = torch.cuda.Stream(device=dev)
+    h2d_b = int(qh.nbytes + kh.nbytes + vh.nbytes)
+    d2h_b = int(oh.nbytes + lh.nbytes)
+
+    def link_pass():
+        out_stream.wait_stream(stream)  # both directions start after the last pass
+        with torch.cuda.stream(stream):
+            for dst, src in ((q4, qh), (k4, kh), (v4, vh)):
+                dst.copy_(src, non_blocking=True)
+        with torch.cuda.stream(out_stream):
+            oh.copy_(o4, non_blocking=True)
+            lh.copy_(l4, non_blocking=True)
+
+    def link_rate(fn):
+        fn()
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(e2e_steps):
+            fn()
+            stream.wait_stream(out_stream)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        return c0.elapsed_time(c1) / e2e_steps
+
+    def h2d_only():
+        with torch.cuda.stream(stream):
+            for dst, src in ((q4, qh), (k4, kh), (v4, vh)):
+                dst.copy_(src, non_blocking=True)
+
+    def d2h_only():
+        with torch.cuda.stream(out_stream):
+            out_stream.wait_stream(stream)
+            oh.copy_(o4, non_blocking=True)
+            lh.copy_(l4, non_blocking=True)
+
+    # one pass in: concurrent copies in both directions ends when the inputs
+    # have landed (they are the larger side); the copies alone give each
+    # direction's rate
+    copy_ms = link_rate(link_pass)
+    h2d_ms, d2h_ms = link_rate(h2d_only), link_rate(d2h_only)
+    (copy_ms, h2d_ms, d2h_ms) = max_over_ranks([copy_ms, h2d_ms, d2h_ms], world, device=dev)
     e2e = {"value": world * e2e_steps * w4.flops() / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-           "h2d_bytes_per_step": int(qh.nbytes + kh.nbytes + vh.nbytes),
-           "d2h_bytes_per_step": int(oh.nbytes + lh.nbytes),
+           "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b,
            "ms_per_step": e2e_ms / e2e_steps,
-           "path": "attn_fwd_from_host (pinned host q,k,v -> device -> kernel -> host o,lse)"}
+           "path": "attn_fwd_from_host (pinned host q,k,v -> device -> kernel -> host o,lse)",
+           # the end-to-end step against the copy-only step of the same bytes
+           "link": {"copy_only_ms_per_step": copy_ms,
+                    "h2d_gbs": h2d_b / (h2d_ms * 1e-3) / 1e9,
+                    "d2h_gbs": d2h_b / (d2h_ms * 1e-3) / 1e9,
+                    "frac": copy_ms / (e2e_ms / e2e_steps),
+                    "note": "frac = copy-only ms / end-to-end ms, both measured in this run"}}
     del qh, kh, vh, oh, lh
 
     # ---- the backward pass (next-row widening; not part of the timed step):
@@ -853,7 +905,8 @@ def run_gpu(args):
         "fp8_" + w3.name: brief(fp8, "ms_per_call"),
         "backward_" + w3.name: brief(backward, "ms_per_call"),
         "merge4_" + w3.name: brief(merge, "ms_per_call"),
-        "e2e_" + LONG: [round(e2e["value"], 1), e2e["unit"], None, round(e2e["ms_per_step"], 4)],
+        "e2e_" + LONG: [round(e2e["value"], 1), e2e["unit"], round(e2e["link"]["frac"], 3),
+                         round(e2e["ms_per_step"], 4)],
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
