@@ -121,8 +121,9 @@ struct Bars {
 
 // Geometry of work item `idx` (0 <= idx < n_items).  Items below split_start
 // are pairs of query tiles; the ones from split_start on are single query
-// tiles, the two halves of the pairs left for the last wave (tile slot 0 only,
-// n_kv1 = 0).  With per-sequence lengths, nq / nk are sequence b's; an item
+// tiles, the two halves of a pair (tile slot 0 only, n_kv1 = 0): the pairs a
+// non-causal launch leaves for a part-full last wave, or every pair of a
+// causal launch of at most one wave (see plan_items).  With per-sequence lengths, nq / nk are sequence b's; an item
 // whose rows all lie past nq is empty and every role skips it.
 struct Item {
     int bh, row0, n_kv0, n_kv1;
@@ -814,11 +815,17 @@ int prefill_set_attributes() {
     return ATTN_OK;
 }
 
-// The persistent grid (one CTA per SM, at most one per pair) and the work
+// The persistent grid (one CTA per SM, at most one per item) and the work
 // items.  Without a causal mask or per-sequence lengths every pair costs the
 // same, so pairs that would leave the last wave part-full run as two
 // single-tile items instead, when those fit in one wave: e.g. 512 pairs on 152
 // SMs take 3 waves of pairs and one of 112 single tiles instead of 4 waves.
+// A causal launch of at most one wave of pairs (few heads) lasts as long as its
+// heaviest pair, so there every pair runs as two single tiles, heaviest first:
+// 5-8 % faster on B1 H1-H2 N16384 and B1 H1-H8 N4096 (d = 128), same output.
+// A tile alone still takes ~0.95 of a pair's time per key tile (nothing
+// overlaps its softmax), so where the tiles would fill more than one wave the
+// split measured slower (0.6-0.75x) and pairs stay whole.
 // kv_bytes: one head's K and V (0: no head groups).  Causal items are dealt
 // heaviest first; for bf16 operands without sequence lengths, when the
 // K and V of all heads exceed 96 MB (three quarters of L2) by three times or
@@ -829,9 +836,13 @@ int prefill_set_attributes() {
 // hence the three-group minimum.
 static long long plan_items(PrefillParams& p, int num_sms, long long kv_bytes) {
     const long long pairs = static_cast<long long>(p.num_pairs) * p.BH;
-    const long long grid = pairs < num_sms ? pairs : num_sms;
+    long long grid = pairs < num_sms ? pairs : num_sms;
     long long items = pairs, split = pairs;
-    if (!p.causal && !p.seqlens_q && !p.seqlens_k && pairs > grid) {
+    if (p.causal && !p.seqlens_q && !p.seqlens_k && pairs <= num_sms) {
+        split = 0;
+        items = 2 * pairs;
+        grid = items < num_sms ? items : num_sms;
+    } else if (!p.causal && !p.seqlens_q && !p.seqlens_k && pairs > grid) {
         const long long full = pairs / grid * grid, tail = pairs - full;
         if (tail > 0 && 2 * tail <= grid && full + 2 * tail <= 0x7fffffffLL) {
             split = full;
@@ -844,7 +855,7 @@ static long long plan_items(PrefillParams& p, int num_sms, long long kv_bytes) {
     long long hg = (kv_bytes > 0 && p.causal && !p.seqlens_q && !p.seqlens_k) ? budget / kv_bytes
                                                                               : p.BH;
     if (hg < 1) hg = 1;
-    if (hg >= p.BH || (p.BH + hg - 1) / hg < 3) hg = p.BH;
+    if (hg >= p.BH || (p.BH + hg - 1) / hg < 3 || split < pairs) hg = p.BH;
     p.head_group = static_cast<int>(hg);
     return grid;
 }

@@ -101,6 +101,29 @@ def test_last_wave_single_tiles_match_oracle(B, H, Nq, Nk, d):
     _full_check(q, k, v, False, what=f"{(B, H, Nq, Nk, d)} split tail")
 
 
+# A causal launch of at most one wave of query-tile pairs runs every pair as
+# two single tiles, heaviest first.  On a 152-SM GB300: 19 heads of 2048 rows
+# are 152 pairs (split into 304 tiles, two rounds), 20 heads 160 pairs (kept
+# whole); rows 384..511 of 300 are an empty half; Nq < Nk moves the diagonal.
+# Every row is checked.
+@pytest.mark.parametrize("B,H,Nq,Nk,d", [
+    (1, 19, 2048, 2048, 128),
+    (1, 20, 2048, 2048, 128),
+    (1, 4, 300, 300, 128),
+    (2, 3, 1000, 1500, 64),
+    (1, 2, 640, 4096, 128),
+])
+def test_one_wave_causal_single_tiles_match_oracle(B, H, Nq, Nk, d):
+    q, k, v = make_qkv(B, H, Nq, Nk, d, seed=31 + Nq + Nk + d, device=_dev())
+    _full_check(q, k, v, True, what=f"{(B, H, Nq, Nk, d)} causal single tiles")
+
+
+def test_one_wave_causal_16384_token_head_sampled():
+    # 64 pairs as 128 single tiles; the last tiles see every key
+    _sampled_custom(1, 1, 16384, 16384, 128, True, seed=3004,
+                    extra_rows=[0, 127, 128, 255, 8191, 16255, 16256, 16383])
+
+
 def test_chunked_prefill_equals_prefill_at_once():
     """A 1000-token causal prefill run as three query chunks, each against the
     keys and values of every token up to its end (the KV cache so far), gives
